@@ -1,0 +1,497 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 MoE expert layer: tokens/s per layer vs prefill quantum.
+
+One step = one moe_layer_forward over one serving step's token batch (router, top-k, grouping,
+grouped gate/up + SwiGLU, down, combine, shared expert), inputs resident in HBM.
+
+Default workload: the mixed prefill+decode step of the Qwen-A3B-like layer (d_model 2048,
+256 experts, top-8, d_ff 512, one shared expert d_ff 512, bf16 weights) at prefill quantum
+2048, i.e. T = 2048 + 3 tokens.  The line also carries the sweep over quantum 128..8192.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--quantum Q] [--workload NAME]
+  python bench.py --impl reference ...     # the fp64 CPU oracle on the same workload
+
+Under torchrun (N > 1) every rank runs its own independent layer step on its own GPU with its
+own token batch (replicas, weak scaling; no collective on the data path); time is the max over
+ranks and value is all ranks' tokens over that time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "MoE layer tokens/s vs prefill quantum (1 GB300); % of HBM/tensor roofline"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------------------------
+# distributed helpers (also exercised by the CPU gloo test)
+# ----------------------------------------------------------------------------------------------
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a float over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each rank draws its own token batch (weights are the same layer on every rank)."""
+    return base + 1000003 * rank
+
+
+# ----------------------------------------------------------------------------------------------
+# peaks, clocks, roofline bookkeeping
+# ----------------------------------------------------------------------------------------------
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, log_path: str | None = None):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.log_path = log_path
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        if self.log_path:
+            with open(self.log_path, "w") as fh:
+                fh.write(self.FIELDS + "\n" + "\n".join(self.lines) + "\n")
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s in sm if s >= 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def layer_bytes_flops(w: synth.Workload, counts: np.ndarray) -> dict:
+    """Algorithmic bytes and FLOPs of one layer step (touched experts only)."""
+    s = w.spec
+    touched = int((counts > 0).sum())
+    wbytes = 2.0 if s.wdtype == "bf16" else 0.5 + 1.0 / 32.0
+    expert = 3.0 * s.d * s.f * wbytes
+    shared = 3.0 * s.d * s.f_s * 2.0 * s.n_shared
+    router = s.d * s.E * 4.0 + s.E * 4.0
+    act = w.T * s.d * 2.0 * 2 + w.T * s.k * 8.0
+    flops = 2.0 * w.T * s.d * s.E + 6.0 * w.T * s.k * s.d * s.f + 6.0 * w.T * s.n_shared * s.d * s.f_s
+    return {"touched": touched, "bytes": touched * expert + shared + router + act, "flops": flops,
+            "gateup_bytes": touched * 2.0 * s.d * s.f * wbytes + 2.0 * s.d * s.f_s * 2.0 * s.n_shared
+            + w.T * s.d * 2.0 + (w.T * s.k * s.f + w.T * s.n_shared * s.f_s) * 2.0,
+            "down_bytes": touched * s.d * s.f * wbytes + s.d * s.f_s * 2.0 * s.n_shared
+            + (w.T * s.k * s.f + w.T * s.n_shared * s.f_s) * 2.0 + (w.T * s.k + (w.T if s.n_shared else 0)) * s.d * 2.0,
+            "weight_bytes": touched * expert + shared}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "decode_batches_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str):
+    """dram bytes per launch from the committed ncu summary, if taken on the current sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            tr = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    ent = tr.get(kernel)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent
+
+
+# ----------------------------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------------------------
+def workload_from_args(args, seed=0) -> synth.Workload:
+    return synth.workload(args.workload, quantum=args.quantum, seed=seed)
+
+
+def upload_plan(w: synth.Workload, T_max: int):
+    import torch
+    from decode_batches_gb300 import MoePlan
+
+    s = w.spec
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    bf = lambda a: dev(a).view(torch.bfloat16)
+    plan = MoePlan(s.E, s.k, s.d, s.f, s.n_shared, s.wdtype)
+    ex = w.experts()
+    b = w.router_bias()
+    if s.wdtype == "bf16":
+        plan.set_weights(dev(w.router_weight()), dev(b) if b is not None else None, bf(ex.gate), bf(ex.up), bf(ex.down))
+    else:
+        plan.set_weights(dev(w.router_weight()), dev(b) if b is not None else None, dev(ex.gate), dev(ex.up),
+                         dev(ex.down), dev(ex.gate_scale), dev(ex.up_scale), dev(ex.down_scale))
+    sh = w.shared()
+    if sh is not None:
+        plan.set_shared(s.f_s, bf(sh[0]), bf(sh[1]), bf(sh[2]))
+    plan.allocate_workspace(T_max)
+    w.drop_cache()          # host copies of the weights are no longer needed
+    return plan
+
+
+def time_forward(plan, x, n_prefill, steps, warmup, world, timing=False):
+    """Device time of `steps` forwards (CUDA events on the launching stream), max over ranks."""
+    import torch
+    st = torch.cuda.current_stream()
+    out = torch.empty_like(x)
+    for _ in range(warmup):
+        plan.forward(x, n_prefill, out=out)
+    plan.timing_report()  # discard warm-up events
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    if timing:
+        plan.enable_timing(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(steps):
+        plan.forward(x, n_prefill, out=out)
+    e1.record(st)
+    torch.cuda.synchronize()
+    plan.enable_timing(False)
+    ms = e0.elapsed_time(e1)
+    kernels = plan.timing_report() if timing else {}
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    return reduce_max(ms, world, device="cuda" if world > 1 else None) / steps, kernels, out
+
+
+def time_e2e(plan, x_host, n_prefill, steps, warmup, world):
+    """Same metric through host buffers: pinned x -> device, forward, out -> pinned host."""
+    import torch
+    st = torch.cuda.current_stream()
+    x_dev = torch.empty(x_host.shape, dtype=x_host.dtype, device="cuda")
+    out_dev = torch.empty_like(x_dev)
+    out_host = torch.empty(x_host.shape, dtype=x_host.dtype, pin_memory=True)
+
+    def step():
+        x_dev.copy_(x_host, non_blocking=True)
+        plan.forward(x_dev, n_prefill, out=out_dev)
+        out_host.copy_(out_dev, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(steps):
+        step()
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = reduce_max(e0.elapsed_time(e1), world, device="cuda" if world > 1 else None) / steps
+    nbytes = x_host.numel() * x_host.element_size()
+    return ms, nbytes, nbytes
+
+
+def routing_counts(plan, x):
+    _, ids, _ = plan.route(x, want_logits=False)
+    counts, _, _, _ = plan.permute(ids)
+    return counts.cpu().numpy()
+
+
+def run_gpu(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    tflops = float(peaks["bf16_tflops"])
+
+    w = workload_from_args(args, seed=rank_seed(0, rank) if world > 1 else 0)
+    x_np = w.x()
+    T = w.T
+    sweep_q = [q for q in synth.QUANTA] if (args.workload == "mixed" and not args.no_sweep) else []
+    T_max = max([T] + [q + 3 for q in sweep_q])
+    # weights: identical layer on every rank (seed 0); tokens per rank from the rank's seed
+    wl_weights = synth.workload(args.workload, quantum=args.quantum, seed=0)
+    plan = upload_plan(wl_weights, T_max)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    x = dev(x_np).view(torch.bfloat16)
+    counts = routing_counts(plan, x)
+    bf = layer_bytes_flops(w, counts)
+
+    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv") if os.path.isdir(
+        os.path.join(ROOT, "gpurun_out")) else None)
+    clocks.start()
+    ms, kernels, _ = time_forward(plan, x, w.n_prefill, args.steps, args.warmup, world, timing=True)
+    clk = clocks.stop()
+    launches_per_step = plan.last_launch_count()
+
+    tokens_per_s = world * T / (ms * 1e-3)
+    t_roof = max(bf["bytes"] / (hbm * 1e9), bf["flops"] / (tflops * 1e12))
+    # dominant kernel by total time inside the timed region
+    dom = max(kernels.items(), key=lambda kv: kv[1][1]) if kernels else None
+    roofline = None
+    if dom:
+        name, (n, tot_ms) = dom
+        per_launch_s = tot_ms / n * 1e-3
+        if name == "tc_gateup":
+            alg, bound = bf["gateup_bytes"], "hbm"
+        elif name == "tc_down":
+            alg, bound = bf["down_bytes"], "hbm"
+        else:
+            alg, bound = bf["bytes"], "hbm"
+        achieved = alg / per_launch_s / 1e9
+        tr = committed_traffic(name)
+        roofline = {"bound": bound, "kernel": name, "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                    "frac": round(achieved / hbm, 4), "traffic": tr["bytes_per_launch"] if tr else None,
+                    "algorithmic_bytes": alg, "launch_us": round(per_launch_s * 1e6, 2),
+                    "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else peak_src}
+
+    # e2e through host buffers
+    x_host = torch.from_numpy(np.ascontiguousarray(x_np)).view(torch.bfloat16).pin_memory()
+    e2e_ms, h2d, d2h = time_e2e(plan, x_host, w.n_prefill, max(3, args.steps // 4), max(3, args.warmup), world)
+
+    sweep = []
+    for q in sweep_q:
+        wq = synth.workload("mixed", quantum=q, seed=rank_seed(0, rank) if world > 1 else 0)
+        xq = dev(wq.x()).view(torch.bfloat16)
+        cq = routing_counts(plan, xq)
+        bq = layer_bytes_flops(wq, cq)
+        msq, _, _ = time_forward(plan, xq, wq.n_prefill, max(20, min(args.steps, 400)), max(3, args.warmup), world)
+        tq = max(bq["bytes"] / (hbm * 1e9), bq["flops"] / (tflops * 1e12))
+        sweep.append({"quantum": q, "T": wq.T, "tokens_per_s": round(world * wq.T / (msq * 1e-3), 1),
+                      "ms_per_step": round(msq, 5), "touched_experts": bq["touched"],
+                      "roofline_frac": round(tq / (msq * 1e-3), 4),
+                      "bound": "hbm" if bq["bytes"] / (hbm * 1e9) >= bq["flops"] / (tflops * 1e12) else "tensor"})
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_subprocess(args)
+
+    line = {
+        "metric": METRIC, "value": round(tokens_per_s, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.spec.wdtype == "bf16" else "bf16 activations, mxfp4 weights",
+        "data": "synthetic (seeded counter-based normals; random-init weights of the layer's shape)",
+        "config": {
+            "workload": workload_desc(w), "T": T, "n_prefill": w.n_prefill, "quantum": args.quantum
+            if args.workload == "mixed" else None, "d_model": w.spec.d, "experts": w.spec.E, "top_k": w.spec.k,
+            "d_ff": w.spec.f, "n_shared": w.spec.n_shared, "d_ff_shared": w.spec.f_s, "weights": w.spec.wdtype,
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+            "l2": "inputs larger than L2: the touched expert weights (%.2f GB) stream from HBM every step"
+                  % (bf["weight_bytes"] / 1e9),
+            "touched_experts": bf["touched"]},
+        "layer_roofline": {"bytes": bf["bytes"], "flops": bf["flops"], "t_roofline_us": round(t_roof * 1e6, 2),
+                           "frac": round(t_roof / (ms * 1e-3), 4), "hbm_gbs": hbm, "bf16_tflops": tflops,
+                           "peak_source": peak_src,
+                           "weight_bytes_per_token": round(bf["weight_bytes"] / T, 1)},
+        "roofline": roofline,
+        "kernels": {k: {"launches": v[0], "total_ms": round(v[1], 4), "avg_us": round(v[1] / v[0] * 1e3, 2)}
+                    for k, v in kernels.items()},
+        "e2e": {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": launches_per_step * args.steps,
+        "launches_per_step": launches_per_step,
+        "clocks": clk,
+        "sweep": sweep,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def workload_desc(w: synth.Workload) -> str:
+    s = w.spec
+    if w.name.startswith("mixed"):
+        return (f"mixed prefill+decode step: quantum {w.n_prefill} + {w.T - w.n_prefill} decode tokens (T={w.T}), "
+                f"d_model {s.d}, {s.E} experts top-{s.k}, d_ff {s.f}, {s.n_shared} shared d_ff {s.f_s}, {s.wdtype}")
+    return f"{w.name}: T={w.T}, d_model {s.d}, {s.E} experts top-{s.k}, d_ff {s.f}, shared {s.n_shared}x{s.f_s}, {s.wdtype}"
+
+
+# ----------------------------------------------------------------------------------------------
+# CPU oracle arm (baseline and --impl reference)
+# ----------------------------------------------------------------------------------------------
+def oracle_tokens(w: synth.Workload, rows: np.ndarray) -> float:
+    """Run the fp64 oracle layer on the given token rows; returns seconds."""
+    import oracle
+    ex = w.experts()
+    dec = oracle.DecodedExperts(ex.gate, ex.up, ex.down, ex.gate_scale, ex.up_scale, ex.down_scale)
+    t0 = time.perf_counter()
+    oracle.moe_layer(w.x()[rows], w.router_weight(), w.router_bias(), w.spec.k, dec, w.shared())
+    return time.perf_counter() - t0
+
+
+def cpu_worker(args):
+    """Child process (BLAS pinned to one thread): time the oracle on a bounded token sample."""
+    w = workload_from_args(args)
+    rng = np.random.default_rng(123)
+    n = min(args.sample, w.T)
+    rows = np.sort(rng.choice(w.T, size=n, replace=False))
+    oracle_tokens(w, rows[:1])             # warm (page in weights, import)
+    dt = oracle_tokens(w, rows)
+    print(json.dumps({"value": n / dt, "seconds": dt, "tokens": n, "T": w.T}))
+
+
+def cpu_baseline_subprocess(args) -> dict | None:
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               RANK="0", WORLD_SIZE="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-worker", "--workload", args.workload, "--quantum",
+           str(args.quantum), "--sample", str(args.cpu_sample)]
+    try:
+        res = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+        out = json.loads(res.stdout.strip().splitlines()[-1])
+    except Exception as exc:  # noqa: BLE001 - reported, never fatal for the GPU line
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "error": str(exc)[:200]}
+    return {"value": round(out["value"], 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{out['tokens']} of the step's {out['T']} tokens (seeded), full fp64 layer per token "
+                      f"(router, top-k, grouping, expert FFNs, combine, shared expert); "
+                      f"{out['seconds']:.1f} s single-threaded numpy"}
+
+
+def run_reference(args):
+    """--impl reference: the fp64 oracle timed as it stands on the host cores, rank 0 only."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    w = workload_from_args(args)
+    rng = np.random.default_rng(7)
+    # calibrate: one token, then size each step so the whole run stays within ~2 minutes
+    dt1 = oracle_tokens(w, np.array([0]))
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    per_step = int(max(1, min(w.T, budget / max(dt1, 1e-3))))
+    times, toks = [], 0
+    for i in range(args.warmup + args.steps):
+        rows = np.sort(rng.choice(w.T, size=per_step, replace=False))
+        dt = oracle_tokens(w, rows)
+        if i >= args.warmup:
+            times.append(dt)
+            toks += per_step
+    total = sum(times)
+    value = toks / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / len(times) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(w), "T": w.T, "n_prefill": w.n_prefill},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "kind": "oracle", "cores": 1,
+                         "sample": f"{per_step} seeded tokens of the {w.T}-token step per timed step"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mixed", choices=["tiny", "decode", "mixed", "fp4_zipf", "verify"])
+    ap.add_argument("--quantum", type=int, default=2048)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample", type=int, default=256)
+    ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--sample", type=int, default=256, help=argparse.SUPPRESS)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.cpu_worker:
+        return cpu_worker(args)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

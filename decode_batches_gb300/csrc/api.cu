@@ -1,0 +1,691 @@
+// C ABI of the MoE layer: plan, validation, weight set-up, workspace carving and the launch
+// sequence of each entry point (see include/moe.h for the contract of every call).
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace moe;
+
+// ============================================================================================
+// errors
+// ============================================================================================
+static thread_local std::string g_last_error;
+
+static moe_status fail(moe_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+#define MOE_CUDA_TRY(expr)                                                                  \
+  do {                                                                                      \
+    cudaError_t _e = (expr);                                                                \
+    if (_e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(_e)); \
+  } while (0)
+
+extern "C" const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+// ============================================================================================
+// plan
+// ============================================================================================
+namespace {
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+  size_t logits, ids, gates, masks, chunk_base, counts, offsets, perm, inv, segs, n_segs, h, h_s, y, y_s;
+  size_t total;
+  int max_segs;
+};
+
+struct TimedLaunch {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+
+}  // namespace
+
+struct moe_plan {
+  int E = 0, k = 0, d = 0, f = 0, n_shared = 0, f_s = 0;
+  moe_wdtype wdtype = MOE_W_BF16;
+  moe_path path = MOE_PATH_AUTO;
+  int device = 0, num_sms = 0;
+  // plan-owned device memory
+  float* w_router = nullptr;
+  float* b_router = nullptr;
+  uint8_t* w_gu = nullptr;
+  uint8_t* s_gu = nullptr;
+  uint8_t* w_down = nullptr;
+  uint8_t* s_down = nullptr;
+  uint16_t* w_gu_s = nullptr;
+  uint16_t* w_down_s = nullptr;
+  uint32_t* err = nullptr;
+  bool weights_set = false, shared_set = false;
+  // workspace (caller-owned)
+  uint8_t* ws = nullptr;
+  size_t ws_bytes = 0;
+  int T_max = 0;
+  WsLayout L{};
+  TcMaps maps{};
+  bool maps_weights = false, maps_ws = false;
+  // timing
+  bool timing = false;
+  std::vector<TimedLaunch> timed;
+  std::vector<cudaEvent_t> event_pool;
+  int launch_count = 0;
+};
+
+static WsLayout layout_for(const moe_plan* p, int T_max) {
+  WsLayout L{};
+  const size_t T = static_cast<size_t>(T_max > 0 ? T_max : 1);
+  const size_t R = T * p->k;
+  const size_t n_chunks = (T + kChunk - 1) / kChunk;
+  L.max_segs = p->E + static_cast<int>((R + kSegRowsMax - 1) / kSegRowsMax) + 1;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  L.logits = take(T * p->E * sizeof(float));
+  L.ids = take(R * sizeof(int32_t));
+  L.gates = take(R * sizeof(float));
+  L.masks = take(n_chunks * p->E * sizeof(uint32_t));
+  L.chunk_base = take(n_chunks * p->E * sizeof(int32_t));
+  L.counts = take(p->E * sizeof(int32_t));
+  L.offsets = take((p->E + 1) * sizeof(int32_t));
+  L.perm = take(R * sizeof(int32_t));
+  L.inv = take(R * sizeof(int32_t));
+  L.segs = take(static_cast<size_t>(L.max_segs) * sizeof(Seg));
+  L.n_segs = take(sizeof(int32_t));
+  L.h = take(R * p->f * 2);
+  L.h_s = take(T * static_cast<size_t>(p->n_shared) * p->f_s * 2);
+  L.y = take(R * p->d * 2);
+  L.y_s = take(T * p->d * 2);
+  L.total = o;
+  return L;
+}
+
+template <typename Tp>
+static Tp* ws_ptr(moe_plan* p, size_t off) {
+  return reinterpret_cast<Tp*>(p->ws + off);
+}
+
+static bool tc_shape_ok(const moe_plan* p) {
+  return p->wdtype == MOE_W_BF16 && p->d % 128 == 0 && p->f % 64 == 0 &&
+         (p->n_shared == 0 || p->f_s % 64 == 0);
+}
+
+static bool use_tc(const moe_plan* p) {
+  if (p->path == MOE_PATH_SIMT) return false;
+  return tc_shape_ok(p);
+}
+
+// ---- timing -----------------------------------------------------------------------------------
+static cudaEvent_t pool_event(moe_plan* p) {
+  if (!p->event_pool.empty()) {
+    cudaEvent_t e = p->event_pool.back();
+    p->event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+struct LaunchScope {
+  moe_plan* p;
+  const char* name;
+  cudaStream_t st;
+  cudaEvent_t start = nullptr;
+  LaunchScope(moe_plan* p_, const char* n, cudaStream_t s) : p(p_), name(n), st(s) {
+    ++p->launch_count;
+    if (p->timing) {
+      start = pool_event(p);
+      if (start) cudaEventRecord(start, st);
+    }
+  }
+  ~LaunchScope() {
+    if (p->timing && start) {
+      cudaEvent_t stop = pool_event(p);
+      if (stop) {
+        cudaEventRecord(stop, st);
+        p->timed.push_back(TimedLaunch{name, start, stop});
+      } else {
+        p->event_pool.push_back(start);
+      }
+    }
+  }
+};
+
+#define LAUNCH(plan, name, stream, call)                                                    \
+  do {                                                                                      \
+    LaunchScope _ls(plan, name, stream);                                                    \
+    cudaError_t _e = (call);                                                                \
+    if (_e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s launch: %s", name, cudaGetErrorString(_e)); \
+  } while (0)
+
+// ---- tensor maps --------------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2-D 16-bit tensor [rows][inner] (row pitch inner*2 bytes), box {64, box_rows}, 128-byte
+// swizzle; dtype is CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 or _FLOAT16.
+static moe_status make_map_16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                              uint32_t box_rows, CUtensorMapDataType dtype) {
+  auto fn = encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return MOE_OK;
+}
+
+static moe_status build_weight_maps(moe_plan* p) {
+  p->maps_weights = false;
+  if (!tc_shape_ok(p) || !p->weights_set) return MOE_OK;
+  moe_status s;
+  const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if ((s = make_map_16(&p->maps.w_gu, p->w_gu, p->d, static_cast<uint64_t>(p->E) * 2 * p->f, 128, BF)) != MOE_OK) return s;
+  if ((s = make_map_16(&p->maps.w_down, p->w_down, p->f, static_cast<uint64_t>(p->E) * p->d, 128, F16)) != MOE_OK) return s;
+  if (p->n_shared > 0) {
+    if (!p->shared_set) return MOE_OK;
+    if ((s = make_map_16(&p->maps.w_gu_s, p->w_gu_s, p->d, static_cast<uint64_t>(p->n_shared) * 2 * p->f_s, 128, BF)) != MOE_OK)
+      return s;
+    if ((s = make_map_16(&p->maps.w_down_s, p->w_down_s, p->f_s, static_cast<uint64_t>(p->n_shared) * p->d, 128, F16)) != MOE_OK)
+      return s;
+  }
+  p->maps_weights = true;
+  return MOE_OK;
+}
+
+static moe_status build_ws_maps(moe_plan* p) {
+  p->maps_ws = false;
+  if (!tc_shape_ok(p) || !p->ws) return MOE_OK;
+  const uint64_t R = static_cast<uint64_t>(p->T_max) * p->k;
+  moe_status s;
+  const CUtensorMapDataType F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if ((s = make_map_16(&p->maps.h, p->ws + p->L.h, p->f, R, 32, F16)) != MOE_OK) return s;
+  if (p->n_shared > 0 && p->f_s > 0) {
+    if ((s = make_map_16(&p->maps.h_s, p->ws + p->L.h_s, static_cast<uint64_t>(p->n_shared) * p->f_s, p->T_max, 32, F16)) != MOE_OK)
+      return s;
+  }
+  p->maps_ws = true;
+  return MOE_OK;
+}
+
+// ============================================================================================
+// creation / destruction
+// ============================================================================================
+extern "C" moe_plan* moe_plan_create(int E, int k, int d_model, int d_ff, int n_shared, moe_wdtype weight_dtype) {
+  if (E < 1 || E > 1024 || k < 1 || k > 32 || k > E) {
+    fail(MOE_ERR_INVALID_ARG, "need 1 <= k <= E <= 1024 and k <= 32 (E=%d k=%d)", E, k);
+    return nullptr;
+  }
+  if (weight_dtype != MOE_W_BF16 && weight_dtype != MOE_W_MXFP4) {
+    fail(MOE_ERR_INVALID_ARG, "unknown weight dtype %d", static_cast<int>(weight_dtype));
+    return nullptr;
+  }
+  const int mult = weight_dtype == MOE_W_MXFP4 ? 32 : 8;
+  if (d_model <= 0 || d_ff <= 0 || d_model % mult || d_ff % mult) {
+    fail(MOE_ERR_INVALID_ARG, "d_model and d_ff must be positive multiples of %d (d=%d f=%d)", mult, d_model, d_ff);
+    return nullptr;
+  }
+  if (n_shared < 0 || n_shared > 64) {
+    fail(MOE_ERR_INVALID_ARG, "n_shared must be in [0, 64] (%d)", n_shared);
+    return nullptr;
+  }
+  moe_plan* p = new moe_plan();
+  p->E = E;
+  p->k = k;
+  p->d = d_model;
+  p->f = d_ff;
+  p->n_shared = n_shared;
+  p->wdtype = weight_dtype;
+  cudaGetDevice(&p->device);
+  cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+  if (p->num_sms <= 0) p->num_sms = 1;
+  if (const char* env = getenv("MOE_FORCE_PATH")) {
+    if (!strcmp(env, "simt")) p->path = MOE_PATH_SIMT;
+    else if (!strcmp(env, "tc")) p->path = MOE_PATH_TC;
+  }
+  g_last_error.clear();
+  return p;
+}
+
+static void free_weights(moe_plan* p) {
+  cudaFree(p->w_router);
+  cudaFree(p->b_router);
+  cudaFree(p->w_gu);
+  cudaFree(p->s_gu);
+  cudaFree(p->w_down);
+  cudaFree(p->s_down);
+  p->w_router = p->b_router = nullptr;
+  p->w_gu = p->s_gu = p->w_down = p->s_down = nullptr;
+  p->weights_set = false;
+}
+
+extern "C" void moe_plan_destroy(moe_plan* p) {
+  if (!p) return;
+  cudaDeviceSynchronize();
+  free_weights(p);
+  cudaFree(p->w_gu_s);
+  cudaFree(p->w_down_s);
+  cudaFree(p->err);
+  for (auto& t : p->timed) {
+    cudaEventDestroy(t.start);
+    cudaEventDestroy(t.stop);
+  }
+  for (auto e : p->event_pool) cudaEventDestroy(e);
+  delete p;
+}
+
+static moe_status ensure_err_word(moe_plan* p) {
+  if (p->err) return MOE_OK;
+  MOE_CUDA_TRY(cudaMalloc(&p->err, sizeof(uint32_t)));
+  MOE_CUDA_TRY(cudaMemset(p->err, 0, sizeof(uint32_t)));
+  return MOE_OK;
+}
+
+// ============================================================================================
+// weights
+// ============================================================================================
+// Copy n bf16 values into an fp16 plan buffer; MOE_ERR_UNSUPPORTED if any is outside the fp16
+// range (the down projection runs fp16 x fp16 on the tensor cores).
+static moe_status copy_bf16_as_f16(uint16_t* dst, const void* src, size_t n) {
+  uint32_t* flag = nullptr;
+  MOE_CUDA_TRY(cudaMalloc(&flag, sizeof(uint32_t)));
+  cudaMemset(flag, 0, sizeof(uint32_t));
+  cudaError_t e = launch_bf16_to_f16(static_cast<const uint16_t*>(src), dst, n, flag, 0);
+  uint32_t bad = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&bad, flag, sizeof bad, cudaMemcpyDeviceToHost);
+  cudaFree(flag);
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "bf16 -> fp16 weight copy: %s", cudaGetErrorString(e));
+  if (bad) return fail(MOE_ERR_UNSUPPORTED, "a down-projection weight is outside the fp16 range (|w| > 65504)");
+  return MOE_OK;
+}
+extern "C" moe_status moe_plan_set_weights(moe_plan* p, const float* w_router, const float* b_router,
+                                           const void* w_gate, const void* w_up, const void* w_down,
+                                           const uint8_t* s_gate, const uint8_t* s_up, const uint8_t* s_down) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+  if (!w_router || !w_gate || !w_up || !w_down)
+    return fail(MOE_ERR_INVALID_ARG, "w_router, w_gate, w_up and w_down are required");
+  const bool fp4 = p->wdtype == MOE_W_MXFP4;
+  if (fp4 && (!s_gate || !s_up || !s_down))
+    return fail(MOE_ERR_INVALID_ARG, "MOE_W_MXFP4 needs s_gate, s_up and s_down");
+  if (!fp4 && (s_gate || s_up || s_down))
+    return fail(MOE_ERR_INVALID_ARG, "scales are only valid with MOE_W_MXFP4");
+  moe_status s = ensure_err_word(p);
+  if (s != MOE_OK) return s;
+  cudaDeviceSynchronize();
+  free_weights(p);
+  const size_t E = p->E, d = p->d, f = p->f;
+  MOE_CUDA_TRY(cudaMalloc(&p->w_router, E * d * sizeof(float)));
+  MOE_CUDA_TRY(cudaMemcpy(p->w_router, w_router, E * d * sizeof(float), cudaMemcpyDeviceToDevice));
+  MOE_CUDA_TRY(cudaMalloc(&p->b_router, E * sizeof(float)));
+  if (b_router)
+    MOE_CUDA_TRY(cudaMemcpy(p->b_router, b_router, E * sizeof(float), cudaMemcpyDeviceToDevice));
+  else
+    MOE_CUDA_TRY(cudaMemset(p->b_router, 0, E * sizeof(float)));
+  const size_t gu_row = fp4 ? d / 2 : d * 2;     // bytes per gate/up row
+  const size_t dn_row = fp4 ? f / 2 : f * 2;     // bytes per down row
+  MOE_CUDA_TRY(cudaMalloc(&p->w_gu, E * 2 * f * gu_row));
+  MOE_CUDA_TRY(launch_interleave_gate_up(static_cast<const uint8_t*>(w_gate), static_cast<const uint8_t*>(w_up), p->w_gu,
+                                         p->E, p->f, gu_row, 0));
+  MOE_CUDA_TRY(cudaMalloc(&p->w_down, E * d * dn_row));
+  if (fp4) {
+    MOE_CUDA_TRY(cudaMemcpy(p->w_down, w_down, E * d * dn_row, cudaMemcpyDeviceToDevice));
+  } else {
+    s = copy_bf16_as_f16(reinterpret_cast<uint16_t*>(p->w_down), w_down, E * d * f);
+    if (s != MOE_OK) {
+      free_weights(p);
+      return s;
+    }
+  }
+  if (fp4) {
+    MOE_CUDA_TRY(cudaMalloc(&p->s_gu, E * 2 * f * (d / 32)));
+    MOE_CUDA_TRY(launch_interleave_gate_up(s_gate, s_up, p->s_gu, p->E, p->f, d / 32, 0));
+    MOE_CUDA_TRY(cudaMalloc(&p->s_down, E * d * (f / 32)));
+    MOE_CUDA_TRY(cudaMemcpy(p->s_down, s_down, E * d * (f / 32), cudaMemcpyDeviceToDevice));
+  }
+  MOE_CUDA_TRY(cudaDeviceSynchronize());
+  p->weights_set = true;
+  return build_weight_maps(p);
+}
+
+extern "C" moe_status moe_plan_set_shared(moe_plan* p, int d_ff_shared, const void* w_gate, const void* w_up,
+                                          const void* w_down) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+  if (p->n_shared == 0) return fail(MOE_ERR_INVALID_ARG, "plan was created with n_shared = 0");
+  if (d_ff_shared <= 0 || d_ff_shared % 8) return fail(MOE_ERR_INVALID_ARG, "d_ff_shared must be a positive multiple of 8");
+  if (!w_gate || !w_up || !w_down) return fail(MOE_ERR_INVALID_ARG, "shared weights are required");
+  if (p->ws && d_ff_shared != p->f_s)
+    return fail(MOE_ERR_INVALID_ARG, "d_ff_shared changed after the workspace was set; set the workspace again");
+  moe_status s = ensure_err_word(p);
+  if (s != MOE_OK) return s;
+  cudaDeviceSynchronize();
+  cudaFree(p->w_gu_s);
+  cudaFree(p->w_down_s);
+  p->w_gu_s = p->w_down_s = nullptr;
+  p->f_s = d_ff_shared;
+  const size_t n = p->n_shared, d = p->d, fs = d_ff_shared;
+  MOE_CUDA_TRY(cudaMalloc(&p->w_gu_s, n * 2 * fs * d * 2));
+  MOE_CUDA_TRY(launch_interleave_gate_up(static_cast<const uint8_t*>(w_gate), static_cast<const uint8_t*>(w_up),
+                                         reinterpret_cast<uint8_t*>(p->w_gu_s), p->n_shared, p->f_s, d * 2, 0));
+  MOE_CUDA_TRY(cudaMalloc(&p->w_down_s, n * d * fs * 2));
+  s = copy_bf16_as_f16(p->w_down_s, w_down, n * d * fs);
+  if (s != MOE_OK) return s;
+  MOE_CUDA_TRY(cudaDeviceSynchronize());
+  p->shared_set = true;
+  return build_weight_maps(p);
+}
+
+// ============================================================================================
+// workspace and options
+// ============================================================================================
+extern "C" size_t moe_plan_workspace_bytes(const moe_plan* p, int T_max) {
+  if (!p || T_max < 0) return 0;
+  if (p->n_shared > 0 && p->f_s == 0) {
+    // width of the shared experts unknown yet: size for the routed width
+    moe_plan tmp = *p;
+    tmp.f_s = p->f;
+    return layout_for(&tmp, T_max).total;
+  }
+  return layout_for(p, T_max).total;
+}
+
+extern "C" moe_status moe_plan_set_workspace(moe_plan* p, void* dev_ptr, size_t bytes, int T_max) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+  if (!dev_ptr || T_max < 1) return fail(MOE_ERR_INVALID_ARG, "workspace pointer and T_max >= 1 required");
+  if (reinterpret_cast<uintptr_t>(dev_ptr) & 255) return fail(MOE_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (p->n_shared > 0 && !p->shared_set)
+    return fail(MOE_ERR_NOT_READY, "set the shared experts before the workspace (their width sizes it)");
+  const WsLayout L = layout_for(p, T_max);
+  if (bytes < L.total)
+    return fail(MOE_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed for T_max=%d", bytes, L.total, T_max);
+  p->ws = static_cast<uint8_t*>(dev_ptr);
+  p->ws_bytes = bytes;
+  p->T_max = T_max;
+  p->L = L;
+  moe_status s = ensure_err_word(p);
+  if (s != MOE_OK) return s;
+  return build_ws_maps(p);
+}
+
+extern "C" moe_status moe_plan_set_path(moe_plan* p, moe_path path) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+  if (path != MOE_PATH_AUTO && path != MOE_PATH_SIMT && path != MOE_PATH_TC)
+    return fail(MOE_ERR_INVALID_ARG, "unknown path %d", static_cast<int>(path));
+  if (path == MOE_PATH_TC && !tc_shape_ok(p))
+    return fail(MOE_ERR_UNSUPPORTED, "tensor-core path needs bf16 weights, d %% 128 == 0, d_ff %% 64 == 0, d_ff_shared %% 64 == 0");
+  p->path = path;
+  return MOE_OK;
+}
+
+// ============================================================================================
+// step entry points
+// ============================================================================================
+static moe_status check_ready(moe_plan* p, int T, bool need_ws) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T must be >= 0 (%d)", T);
+  if (!p->weights_set) return fail(MOE_ERR_NOT_READY, "weights not set");
+  if (p->n_shared > 0 && !p->shared_set) return fail(MOE_ERR_NOT_READY, "shared experts not set");
+  if (need_ws) {
+    if (!p->ws) return fail(MOE_ERR_NOT_READY, "workspace not set");
+    if (T > p->T_max) return fail(MOE_ERR_WORKSPACE, "T=%d exceeds the workspace's T_max=%d", T, p->T_max);
+  }
+  return MOE_OK;
+}
+
+static FfnWeights ffn_weights(const moe_plan* p) {
+  FfnWeights w;
+  w.w_gu = p->w_gu;
+  w.s_gu = p->s_gu;
+  w.w_down = p->w_down;
+  w.s_down = p->s_down;
+  w.fp4 = p->wdtype == MOE_W_MXFP4;
+  w.w_gu_s = p->w_gu_s;
+  w.w_down_s = p->w_down_s;
+  w.n_shared = p->n_shared;
+  w.f_s = p->f_s;
+  w.E = p->E;
+  w.k = p->k;
+  w.d = p->d;
+  w.f = p->f;
+  w.err = p->err;
+  return w;
+}
+
+// Expert FFN over grouped rows; y/y_s outputs, h/h_s in the workspace.  For the tensor-core
+// path `segs`/`n_segs` must already describe the routed segments.
+static moe_status run_experts(moe_plan* p, const uint16_t* x, int T, const int32_t* offsets, const int32_t* perm,
+                              uint16_t* y, uint16_t* y_s, cudaStream_t st) {
+  uint16_t* h = ws_ptr<uint16_t>(p, p->L.h);
+  uint16_t* h_s = ws_ptr<uint16_t>(p, p->L.h_s);
+  if (use_tc(p)) {
+    if (!p->maps_weights || !p->maps_ws) return fail(MOE_ERR_NOT_READY, "tensor maps not built");
+    TcArgs a;
+    a.segs = ws_ptr<Seg>(p, p->L.segs);
+    a.n_segs = ws_ptr<int32_t>(p, p->L.n_segs);
+    a.perm = perm;
+    a.x = x;
+    a.h = h;
+    a.h_s = h_s;
+    a.y = y;
+    a.y_s = y_s;
+    a.err = p->err;
+    a.T = T;
+    a.E = p->E;
+    a.k = p->k;
+    a.d = p->d;
+    a.f = p->f;
+    a.n_shared = p->n_shared;
+    a.f_s = p->f_s;
+    a.n_shared_segs = p->n_shared > 0 ? (T + kSegRowsMax - 1) / kSegRowsMax : 0;
+    LAUNCH(p, "tc_gateup", st, launch_tc_gateup(&p->maps, a, p->num_sms, st));
+    LAUNCH(p, "tc_down", st, launch_tc_down(&p->maps, a, p->num_sms, st));
+  } else {
+    FfnWeights w = ffn_weights(p);
+    LAUNCH(p, "simt_ffn", st, launch_ffn_simt(w, x, T, offsets, perm, h, h_s, y, y_s, st));
+    p->launch_count += 1;  // the SIMT FFN is two kernels
+  }
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_layer_forward(moe_plan* p, const void* x, int T, int n_prefill, void* out,
+                                        moe_stream_t stream) {
+  moe_status s = check_ready(p, T, true);
+  if (s != MOE_OK) return s;
+  if (n_prefill < 0 || n_prefill > T) return fail(MOE_ERR_INVALID_ARG, "n_prefill=%d outside [0, T=%d]", n_prefill, T);
+  p->launch_count = 0;
+  if (T == 0) return MOE_OK;
+  if (!x || !out) return fail(MOE_ERR_INVALID_ARG, "x and out are required");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const uint16_t* xb = static_cast<const uint16_t*>(x);
+  float* logits = ws_ptr<float>(p, p->L.logits);
+  int32_t* ids = ws_ptr<int32_t>(p, p->L.ids);
+  float* gates = ws_ptr<float>(p, p->L.gates);
+  uint32_t* masks = ws_ptr<uint32_t>(p, p->L.masks);
+  int32_t* chunk_base = ws_ptr<int32_t>(p, p->L.chunk_base);
+  int32_t* counts = ws_ptr<int32_t>(p, p->L.counts);
+  int32_t* offsets = ws_ptr<int32_t>(p, p->L.offsets);
+  int32_t* perm = ws_ptr<int32_t>(p, p->L.perm);
+  int32_t* inv = ws_ptr<int32_t>(p, p->L.inv);
+  uint16_t* y = ws_ptr<uint16_t>(p, p->L.y);
+  uint16_t* y_s = p->n_shared > 0 ? ws_ptr<uint16_t>(p, p->L.y_s) : nullptr;
+  const int n_chunks = (T + kChunk - 1) / kChunk;
+  const bool tc = use_tc(p);
+  LAUNCH(p, "router_logits", st, launch_router_logits(xb, p->w_router, p->b_router, T, p->E, p->d, logits, st));
+  LAUNCH(p, "topk", st, launch_topk(logits, T, p->E, p->k, ids, gates, masks, p->err, st));
+  LAUNCH(p, "group_scan", st,
+         launch_group_scan(masks, n_chunks, p->E, chunk_base, counts, offsets, tc ? ws_ptr<Seg>(p, p->L.segs) : nullptr,
+                           ws_ptr<int32_t>(p, p->L.n_segs), p->L.max_segs, p->err, st));
+  LAUNCH(p, "scatter", st, launch_scatter(ids, masks, chunk_base, offsets, T, p->E, p->k, perm, inv, st));
+  s = run_experts(p, xb, T, offsets, perm, y, y_s, st);
+  if (s != MOE_OK) return s;
+  LAUNCH(p, "combine", st, launch_combine(y, gates, inv, y_s, T, p->k, p->d, static_cast<uint16_t*>(out), st));
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_route(moe_plan* p, const void* x, int T, float* logits, int32_t* ids, float* gates,
+                                moe_stream_t stream) {
+  moe_status s = check_ready(p, T, true);
+  if (s != MOE_OK) return s;
+  p->launch_count = 0;
+  if (T == 0) return MOE_OK;
+  if (!x || !ids || !gates) return fail(MOE_ERR_INVALID_ARG, "x, ids and gates are required");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  float* lg = logits ? logits : ws_ptr<float>(p, p->L.logits);
+  LAUNCH(p, "router_logits", st,
+         launch_router_logits(static_cast<const uint16_t*>(x), p->w_router, p->b_router, T, p->E, p->d, lg, st));
+  LAUNCH(p, "topk", st, launch_topk(lg, T, p->E, p->k, ids, gates, nullptr, p->err, st));
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_route_logits(moe_plan* p, const float* logits, int T, int32_t* ids, float* gates,
+                                       moe_stream_t stream) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T must be >= 0");
+  moe_status s = ensure_err_word(p);
+  if (s != MOE_OK) return s;
+  p->launch_count = 0;
+  if (T == 0) return MOE_OK;
+  if (!logits || !ids || !gates) return fail(MOE_ERR_INVALID_ARG, "logits, ids and gates are required");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  LAUNCH(p, "topk", st, launch_topk(logits, T, p->E, p->k, ids, gates, nullptr, p->err, st));
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_permute(moe_plan* p, const int32_t* ids, int T, int32_t* counts, int32_t* offsets,
+                                  int32_t* perm, int32_t* inv_perm, moe_stream_t stream) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T must be >= 0");
+  if (!p->ws) return fail(MOE_ERR_NOT_READY, "workspace not set");
+  if (T > p->T_max) return fail(MOE_ERR_WORKSPACE, "T=%d exceeds the workspace's T_max=%d", T, p->T_max);
+  if (!counts || !offsets || !perm || !inv_perm || (T > 0 && !ids))
+    return fail(MOE_ERR_INVALID_ARG, "ids, counts, offsets, perm and inv_perm are required");
+  moe_status s = ensure_err_word(p);
+  if (s != MOE_OK) return s;
+  p->launch_count = 0;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int n_chunks = (T + kChunk - 1) / kChunk;
+  uint32_t* masks = ws_ptr<uint32_t>(p, p->L.masks);
+  int32_t* chunk_base = ws_ptr<int32_t>(p, p->L.chunk_base);
+  if (T > 0) LAUNCH(p, "masks_from_ids", st, launch_masks_from_ids(ids, T, p->E, p->k, masks, p->err, st));
+  LAUNCH(p, "group_scan", st,
+         launch_group_scan(masks, n_chunks, p->E, chunk_base, counts, offsets, nullptr, nullptr, 0, p->err, st));
+  if (T > 0) LAUNCH(p, "scatter", st, launch_scatter(ids, masks, chunk_base, offsets, T, p->E, p->k, perm, inv_perm, st));
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_experts(moe_plan* p, const void* x, int T, const int32_t* offsets, const int32_t* perm,
+                                  void* y, void* shared_y, moe_stream_t stream) {
+  moe_status s = check_ready(p, T, true);
+  if (s != MOE_OK) return s;
+  p->launch_count = 0;
+  if (T == 0) return MOE_OK;
+  if (!x || !offsets || !perm || !y) return fail(MOE_ERR_INVALID_ARG, "x, offsets, perm and y are required");
+  if (p->n_shared > 0 && !shared_y) return fail(MOE_ERR_INVALID_ARG, "shared_y is required when n_shared > 0");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (use_tc(p))
+    LAUNCH(p, "segments", st,
+           launch_segments_from_offsets(offsets, p->E, ws_ptr<Seg>(p, p->L.segs), ws_ptr<int32_t>(p, p->L.n_segs),
+                                        p->L.max_segs, p->err, st));
+  return run_experts(p, static_cast<const uint16_t*>(x), T, offsets, perm, static_cast<uint16_t*>(y),
+                     p->n_shared > 0 ? static_cast<uint16_t*>(shared_y) : nullptr, st);
+}
+
+extern "C" moe_status moe_combine(moe_plan* p, const void* y, const float* gates, const int32_t* inv_perm,
+                                  const void* shared_y, int T, void* out, moe_stream_t stream) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T must be >= 0");
+  p->launch_count = 0;
+  if (T == 0) return MOE_OK;
+  if (!y || !gates || !inv_perm || !out) return fail(MOE_ERR_INVALID_ARG, "y, gates, inv_perm and out are required");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  LAUNCH(p, "combine", st,
+         launch_combine(static_cast<const uint16_t*>(y), gates, inv_perm, static_cast<const uint16_t*>(shared_y), T, p->k,
+                        p->d, static_cast<uint16_t*>(out), st));
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_plan_get_device_error(moe_plan* p, uint32_t* code) {
+  if (!p || !code) return fail(MOE_ERR_INVALID_ARG, "plan and code are required");
+  *code = 0;
+  MOE_CUDA_TRY(cudaDeviceSynchronize());
+  if (!p->err) return MOE_OK;
+  MOE_CUDA_TRY(cudaMemcpy(code, p->err, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+  MOE_CUDA_TRY(cudaMemset(p->err, 0, sizeof(uint32_t)));
+  if (*code) return fail(MOE_ERR_DEVICE, "device error bits 0x%x", *code);
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_plan_enable_timing(moe_plan* p, int enable) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+  p->timing = enable != 0;
+  return MOE_OK;
+}
+
+extern "C" size_t moe_plan_timing_report(moe_plan* p, char* buf, size_t len) {
+  if (!p) return 0;
+  std::map<std::string, std::pair<long, double>> agg;
+  std::vector<std::string> order;
+  for (auto& t : p->timed) {
+    float ms = 0.f;
+    cudaEventSynchronize(t.stop);
+    cudaEventElapsedTime(&ms, t.start, t.stop);
+    auto it = agg.find(t.name);
+    if (it == agg.end()) {
+      order.push_back(t.name);
+      agg[t.name] = {1, ms};
+    } else {
+      it->second.first += 1;
+      it->second.second += ms;
+    }
+    p->event_pool.push_back(t.start);
+    p->event_pool.push_back(t.stop);
+  }
+  p->timed.clear();
+  std::string rep;
+  for (auto& n : order) {
+    char line[256];
+    snprintf(line, sizeof line, "%s %ld %.6f\n", n.c_str(), agg[n].first, agg[n].second);
+    rep += line;
+  }
+  if (buf && len > 0) {
+    const size_t n = rep.size() < len - 1 ? rep.size() : len - 1;
+    memcpy(buf, rep.data(), n);
+    buf[n] = '\0';
+  }
+  return rep.size() + 1;
+}
+
+extern "C" int moe_plan_last_launch_count(const moe_plan* p) { return p ? p->launch_count : 0; }

@@ -1,0 +1,361 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), sm_103a.
+//
+// The grouped problem is a list of segments: consecutive grouped rows of one routed expert
+// (at most 256), or consecutive tokens for the shared experts.  Each unit of work is one
+// segment times one 128-row tile of that expert's weight matrix.  The MMA computes
+//     D[weight row][token] = W[128 x K] . X[N x K]^T
+// ("swap-AB": the weight tile is the M=128 operand, the segment's tokens are N <= 256), so the
+// weights -- the bytes that bound this layer -- stream through shared memory exactly once per
+// segment, whatever the number of rows routed to the expert.
+//
+//   gate/up kernel (bf16 x bf16): A = 128 interleaved rows of W_gate|W_up (8 gate rows, then
+//     the same 8 features' up rows, repeated), TMA-loaded; B = the segment's token rows of x,
+//     gathered with cp.async (the permutation is applied on the fly, x is never copied);
+//     epilogue: h = fp16(silu(gate) * up), the gate-first SwiGLU of "Why SSD-streamed MoE was
+//     slow: 8GB Jetson Orin Nano, part 2" (section re-checking part 1), rounded inside the
+//     producer as in the Decode paragraph of "DeepSeek V4.1F Q4 with native DSpark MTP on M3
+//     Ultra" (there in bf16; fp16 here keeps 3 more bits for the same bytes).
+//   down kernel (fp16 x fp16): A = 128 rows of W_down (held as fp16 by the plan), B = the
+//     segment's rows of h (TMA); epilogue writes y (fp16) in grouped row order for the combine.
+//   Intermediates that leave the fp16 range are clamped and flag MOE_DEVERR_RANGE.
+//
+// Roles (persistent CTAs, one per SM, every role walks the same unit sequence):
+//   warp 0      TMA producer (A, and B for the down kernel)
+//   warp 1      TMEM owner and MMA issuer (one thread)
+//   warps 2-5   epilogue (TMEM lanes 32*(warp%4) .. +31)
+//   warps 6-9   gate/up only: cp.async gather of the token rows
+// Pipeline: 4 shared-memory stages of (A 16 KB + B up to 32 KB), two TMEM accumulators of up
+// to 256 fp32 columns so the epilogue of one unit overlaps the main loop of the next.
+// Every wait is bounded (see common.cuh); on a timeout the CTA stops issuing work, drains its
+// MMAs, frees TMEM and returns with MOE_DEVERR_TIMEOUT set.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace tc {
+
+constexpr int BM = 128;                          // weight rows per unit (MMA M)
+constexpr int BK = 64;                           // K elements per stage (128-byte rows)
+constexpr int kStages = 4;
+constexpr int kLag = 2;                          // gather completion lag (stages)
+constexpr int kABytes = BM * BK * 2;             // 16 KB
+constexpr int kBBytes = kSegRowsMax * BK * 2;    // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kTmemCols = 512;                   // 2 accumulators x 256 columns
+constexpr int kAccCols = 256;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*align slack*/;
+constexpr int kGatherThreads = 128;
+
+struct Unit {
+  int shared;     // 1: shared-expert segment
+  int expert;     // routed expert (shared: -1)
+  int row_start;  // grouped row (routed) or token (shared) of column 0
+  int rows;       // valid columns
+  int tile;       // 128-row weight tile index
+};
+
+MOE_DEVICE Unit decode_unit(int u, const TcArgs& a, int tiles_r, int tiles_s, int n_shared_units) {
+  Unit un;
+  if (u < n_shared_units) {
+    const int ss = u / tiles_s;
+    const int nss = a.n_shared_segs;
+    const int q = a.T / nss, rem = a.T % nss;
+    un.shared = 1;
+    un.expert = -1;
+    un.tile = u % tiles_s;
+    un.row_start = ss * q + min(ss, rem);
+    un.rows = q + (ss < rem ? 1 : 0);
+  } else {
+    const int v = u - n_shared_units;
+    const Seg s = a.segs[v / tiles_r];
+    un.shared = 0;
+    un.expert = s.expert;
+    un.tile = v % tiles_r;
+    un.row_start = s.row_start;
+    un.rows = s.rows;
+  }
+  return un;
+}
+
+MOE_DEVICE int pad16(int rows) { return rows <= 16 ? 16 : ((rows + 15) & ~15); }
+
+template <bool kGateUp>
+__global__ void __launch_bounds__(kGateUp ? 320 : 192, 1)
+    tc_ffn_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], kGateUp ? 1 + kGatherThreads : 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(kGateUp ? &maps.w_gu : &maps.w_down);
+    if (a.n_shared) tma_prefetch_map(kGateUp ? &maps.w_gu_s : &maps.w_down_s);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int tiles_r = kGateUp ? a.f / 64 : a.d / BM;
+  const int tiles_s = kGateUp ? (a.n_shared * a.f_s) / 64 : a.d / BM;
+  const int n_shared_units = a.n_shared ? a.n_shared_segs * tiles_s : 0;
+  const int n_routed_units = (*a.n_segs) * tiles_r;
+  const int total_units = n_shared_units + n_routed_units;
+  const int nk_r = kGateUp ? a.d / BK : a.f / BK;
+  const int nk_s = kGateUp ? a.d / BK : (a.n_shared * a.f_s) / BK;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_act = l2_policy_evict_last();
+      uint32_t g = 0;
+      for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
+        const Unit un = decode_unit(u, a, tiles_r, tiles_s, n_shared_units);
+        const int nk = un.shared ? nk_s : nk_r;
+        const int nbox = kGateUp ? 0 : (pad16(un.rows) + 31) / 32;
+        bool ok = true;
+        for (int kk = 0; kk < nk; ++kk, ++g) {
+          const int slot = g % kStages;
+          const uint32_t use = g / kStages;
+          if (!mbar_wait(&empty[slot], (use & 1u) ^ 1u, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + slot * kStageBytes;
+          uint8_t* sb = sa + kABytes;
+          mbar_arrive_expect_tx(&full[slot], kABytes + nbox * 32 * BK * 2);
+          if (kGateUp) {
+            if (un.shared)
+              tma_load_2d(sa, &maps.w_gu_s, &full[slot], kk * BK, un.tile * BM, pol_w);
+            else
+              tma_load_2d(sa, &maps.w_gu, &full[slot], kk * BK, un.expert * 2 * a.f + un.tile * BM, pol_w);
+          } else {
+            if (un.shared) {
+              const int kglob = kk * BK;
+              const int s = kglob / a.f_s, kin = kglob % a.f_s;
+              tma_load_2d(sa, &maps.w_down_s, &full[slot], kin, s * a.d + un.tile * BM, pol_w);
+              for (int i = 0; i < nbox; ++i)
+                tma_load_2d(sb + i * 32 * BK * 2, &maps.h_s, &full[slot], kglob, un.row_start + 32 * i, pol_act);
+            } else {
+              tma_load_2d(sa, &maps.w_down, &full[slot], kk * BK, un.expert * a.d + un.tile * BM, pol_w);
+              for (int i = 0; i < nbox; ++i)
+                tma_load_2d(sb + i * 32 * BK * 2, &maps.h, &full[slot], kk * BK, un.row_start + 32 * i, pol_act);
+            }
+          }
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t g = 0, j = 0;
+      for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x, ++j) {
+        const Unit un = decode_unit(u, a, tiles_r, tiles_s, n_shared_units);
+        const int nk = un.shared ? nk_s : nk_r;
+        const uint32_t N = static_cast<uint32_t>(pad16(un.rows));
+        const uint32_t buf = j & 1u, use_acc = j >> 1;
+        if (!mbar_wait(&acc_empty[buf], (use_acc & 1u) ^ 1u, abort_flag, a.err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + buf * kAccCols;
+        // gate/up: bf16 weights x bf16 tokens; down: fp16 weights x fp16 hidden vectors
+        const uint32_t idesc = kGateUp ? idesc_bf16_f32(BM, N) : idesc_f16_f32(BM, N);
+        bool ok = true;
+        for (int kk = 0; kk < nk; ++kk, ++g) {
+          const int slot = g % kStages;
+          const uint32_t use = g / kStages;
+          if (!mbar_wait(&full[slot], use & 1u, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + slot * kStageBytes);
+          const uint64_t adesc = smem_desc_sw128(sa);
+          const uint64_t bdesc = smem_desc_sw128(sa + kABytes);
+#pragma unroll
+          for (int ks = 0; ks < BK / 16; ++ks)  // K = 16 per MMA: +32 bytes = +2 in the address field
+            mma_f16_ss(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc, (kk | ks) != 0);
+          mma_commit(&empty[slot]);
+        }
+        if (!ok) break;
+        mma_commit(&acc_full[buf]);
+      }
+      // all MMAs issued by this thread have finished once `drain` completes
+      mma_commit(drain);
+      mbar_wait(drain, 0, nullptr, a.err);
+    }
+  } else if (warp < 6) {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    uint32_t j = 0;
+    for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x, ++j) {
+      const Unit un = decode_unit(u, a, tiles_r, tiles_s, n_shared_units);
+      const uint32_t buf = j & 1u, use_acc = j >> 1;
+      if (!mbar_wait(&acc_full[buf], use_acc & 1u, abort_flag, a.err)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * kAccCols;
+      const int L = 32 * q + lane;  // accumulator row (= weight row of the tile)
+      if (kGateUp) {
+        const int w16 = L & 15;
+        const bool is_gate = w16 < 8;
+        const int feat = un.tile * 64 + 8 * (L >> 4) + (w16 & 7);
+        uint16_t* hout;
+        int ldh;
+        if (un.shared) {
+          hout = a.h_s;
+          ldh = a.n_shared * a.f_s;
+        } else {
+          hout = a.h;
+          ldh = a.f;
+        }
+        bool sat = false;
+        for (int c0 = 0; c0 < un.rows; c0 += 16) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(tbase + c0, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const uint32_t send = is_gate ? r[2 * jj + 1] : r[2 * jj];
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 8);
+            const int col = c0 + 2 * jj + (is_gate ? 0 : 1);
+            const float gv = __uint_as_float(is_gate ? r[2 * jj] : recv);
+            const float uv = __uint_as_float(is_gate ? recv : r[2 * jj + 1]);
+            float hv = swiglu(gv, uv);
+            if (!(fabsf(hv) <= kF16Max)) {
+              sat = true;
+              hv = fminf(fmaxf(hv, -kF16Max), kF16Max);
+            }
+            if (col < un.rows) hout[static_cast<size_t>(un.row_start + col) * ldh + feat] = f32_to_f16_bits_rn(hv);
+          }
+        }
+        if (__any_sync(0xffffffffu, sat) && lane == 0) set_error(a.err, MOE_DEVERR_RANGE);
+      } else {
+        const int feat = un.tile * BM + L;
+        uint16_t* yout = un.shared ? a.y_s : a.y;
+        bool sat = false;
+        for (int c0 = 0; c0 < un.rows; c0 += 16) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(tbase + c0, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            float v = __uint_as_float(r[c]);
+            if (!(fabsf(v) <= kF16Max)) {
+              sat = true;
+              v = fminf(fmaxf(v, -kF16Max), kF16Max);
+            }
+            if (c0 + c < un.rows) yout[static_cast<size_t>(un.row_start + c0 + c) * a.d + feat] = f32_to_f16_bits_rn(v);
+          }
+        }
+        if (__any_sync(0xffffffffu, sat) && lane == 0) set_error(a.err, MOE_DEVERR_RANGE);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+  } else if (kGateUp) {
+    // ---------------- token-row gather (cp.async) ----------------
+    const int p = threadIdx.x - 192;  // 0..127
+    uint32_t g = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
+      const Unit un = decode_unit(u, a, tiles_r, tiles_s, n_shared_units);
+      int tok[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int n = p + kGatherThreads * i;
+        tok[i] = -1;
+        if (n < un.rows) tok[i] = un.shared ? un.row_start + n : a.perm[un.row_start + n] / a.k;
+      }
+      for (int kk = 0; kk < nk_r; ++kk, ++g) {
+        const int slot = g % kStages;
+        const uint32_t use = g / kStages;
+        if (!mbar_wait(&empty[slot], (use & 1u) ^ 1u, abort_flag, a.err)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sb = smem_u32(smem + slot * kStageBytes + kABytes);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          if (tok[i] < 0) continue;
+          const int n = p + kGatherThreads * i;
+          const uint16_t* src = a.x + static_cast<size_t>(tok[i]) * a.d + kk * BK;
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            cp_async_16(sb + n * 128 + ((ch ^ (n & 7)) << 4), src + ch * 8);
+        }
+        cp_async_commit();
+        if (g >= kLag) {
+          cp_async_wait<kLag>();
+          fence_proxy_async_smem();
+          mbar_arrive(&full[(g - kLag) % kStages]);
+        }
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    if (ok && !*abort_flag) {
+      const uint32_t first = g >= kLag ? g - kLag : 0;
+      for (uint32_t s = first; s < g; ++s) mbar_arrive(&full[s % kStages]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace tc
+
+static bool g_tc_attr_set[2] = {false, false};
+
+template <bool kGateUp>
+static cudaError_t launch_tc(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st) {
+  auto kern = tc::tc_ffn_kernel<kGateUp>;
+  if (!g_tc_attr_set[kGateUp]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    g_tc_attr_set[kGateUp] = true;
+  }
+  kern<<<num_sms, kGateUp ? 320 : 192, tc::kSmemBytes, st>>>(*maps, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_gateup(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st) {
+  return launch_tc<true>(maps, a, num_sms, st);
+}
+
+cudaError_t launch_tc_down(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st) {
+  return launch_tc<false>(maps, a, num_sms, st);
+}
+
+}  // namespace moe

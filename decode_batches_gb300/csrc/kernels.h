@@ -1,0 +1,114 @@
+// Internal launch interface between the plan/ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Tokens per chunk of the grouping step: one 32-bit mask word per (chunk, expert).
+constexpr int kChunk = 32;
+// Largest number of rows one tensor-core unit handles (the MMA's N <= 256).
+constexpr int kSegRowsMax = 256;
+
+// One segment of the grouped problem: `rows` consecutive grouped rows of one expert starting
+// at `row_start` (expert >= 0), or `rows` consecutive tokens starting at token `row_start` for
+// the shared experts (expert == -1).
+struct Seg {
+  int expert;
+  int row_start;
+  int rows;
+  int pad;
+};
+
+// ---- routing and grouping (route.cu) --------------------------------------------------------
+// logits[t][e] = x[t] . w_router[e] + b[e] (fp32 accumulation).
+cudaError_t launch_router_logits(const uint16_t* x, const float* w_router, const float* b_router, int T,
+                                 int E, int d, float* logits, cudaStream_t st);
+// Top-k + softmax gates per token; if masks != nullptr also writes the per-chunk expert masks
+// (bit t of masks[c][e] <=> token c*32+t chose e).
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* gates,
+                        uint32_t* masks, uint32_t* err, cudaStream_t st);
+// Per-chunk expert masks from given ids (validates range / duplicates).
+cudaError_t launch_masks_from_ids(const int32_t* ids, int T, int E, int k, uint32_t* masks,
+                                  uint32_t* err, cudaStream_t st);
+// Exclusive scan over experts and chunks; counts, offsets, chunk bases, and (if segs) the
+// segment list of the routed experts for the grouped GEMMs.
+cudaError_t launch_group_scan(const uint32_t* masks, int n_chunks, int E, int32_t* chunk_base,
+                              int32_t* counts, int32_t* offsets, Seg* segs, int32_t* n_segs,
+                              int max_segs, uint32_t* err, cudaStream_t st);
+// perm / inv_perm from masks, bases and offsets.
+cudaError_t launch_scatter(const int32_t* ids, const uint32_t* masks, const int32_t* chunk_base,
+                           const int32_t* offsets, int T, int E, int k, int32_t* perm, int32_t* inv,
+                           cudaStream_t st);
+// Segment list from offsets only (used by the separate experts entry point).
+cudaError_t launch_segments_from_offsets(const int32_t* offsets, int E, Seg* segs, int32_t* n_segs,
+                                         int max_segs, uint32_t* err, cudaStream_t st);
+
+// ---- expert FFN, CUDA-core reference path (ffn_simt.cu) -------------------------------------
+struct FfnWeights {
+  // Routed experts.  bf16: w_gu [E][2f][d] with gate/up rows interleaved in groups of 8
+  // (rows 16q..16q+7 = gate rows 8q..8q+7, rows 16q+8..16q+15 = up rows 8q..8q+7),
+  // w_down [E][d][f] held as fp16.  MXFP4: the same row order for codes [.][.][K/2] and scales
+  // [.][.][K/32]; w_down codes [E][d][f/2].
+  const void* w_gu = nullptr;
+  const uint8_t* s_gu = nullptr;
+  const void* w_down = nullptr;
+  const uint8_t* s_down = nullptr;
+  int fp4 = 0;
+  // Shared experts, n_shared concatenated: w_gu_s bf16 [n_s*2*f_s][d] interleaved the same
+  // way per expert, w_down_s fp16 [n_s][d][f_s].
+  const uint16_t* w_gu_s = nullptr;
+  const uint16_t* w_down_s = nullptr;
+  int n_shared = 0;
+  int f_s = 0;
+  int E = 0, k = 0, d = 0, f = 0;
+  uint32_t* err = nullptr;
+};
+
+// h, h_s, y, y_s are fp16.
+cudaError_t launch_ffn_simt(const FfnWeights& w, const uint16_t* x, int T, const int32_t* offsets,
+                            const int32_t* perm, uint16_t* h, uint16_t* h_s, uint16_t* y,
+                            uint16_t* y_s, cudaStream_t st);
+
+// ---- expert FFN, tcgen05 path (gemm_tc.cu) ---------------------------------------------------
+struct TcMaps {
+  CUtensorMap w_gu;      // A for gate/up: [E*2f rows][d], box 64 x 128
+  CUtensorMap w_gu_s;    // A for shared gate/up: [n_s*2f_s rows][d]
+  CUtensorMap w_down;    // A for down: [E*d rows][f], box 64 x 128
+  CUtensorMap w_down_s;  // A for shared down: [n_s*d rows][f_s]
+  CUtensorMap h;         // B for down: [R_max rows][f], box 64 x 32
+  CUtensorMap h_s;       // B for shared down: [T_max rows][n_s*f_s], box 64 x 32
+};
+
+struct TcArgs {
+  const Seg* segs = nullptr;
+  const int32_t* n_segs = nullptr;
+  const int32_t* perm = nullptr;
+  const uint16_t* x = nullptr;
+  uint16_t* h = nullptr;
+  uint16_t* h_s = nullptr;
+  uint16_t* y = nullptr;
+  uint16_t* y_s = nullptr;
+  uint32_t* err = nullptr;
+  int T = 0, E = 0, k = 0, d = 0, f = 0, n_shared = 0, f_s = 0;
+  int n_shared_segs = 0;   // ceil(T / kSegRowsMax) when n_shared > 0
+};
+
+cudaError_t launch_tc_gateup(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_tc_down(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st);
+
+// ---- combine (combine.cu): y and shared_y fp16, out bf16 ----------------------------------------
+cudaError_t launch_combine(const uint16_t* y, const float* gates, const int32_t* inv,
+                           const uint16_t* shared_y, int T, int k, int d, uint16_t* out,
+                           cudaStream_t st);
+
+// ---- weight repacking at set-up (repack.cu) --------------------------------------------------
+// dst [n][2f][K*elem] <- gate [n][f][K*elem], up [n][f][K*elem], rows interleaved by 8.
+cudaError_t launch_interleave_gate_up(const uint8_t* gate, const uint8_t* up, uint8_t* dst, int n,
+                                      int f, size_t row_bytes, cudaStream_t st);
+// dst fp16 <- src bf16 (round to nearest even); *bad |= 1 if a value is outside the fp16 range.
+cudaError_t launch_bf16_to_f16(const uint16_t* src, uint16_t* dst, size_t n, uint32_t* bad, cudaStream_t st);
+
+}  // namespace moe

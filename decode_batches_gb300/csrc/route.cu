@@ -1,0 +1,453 @@
+// Routing and grouping kernels of the MoE layer.
+//
+//   router logits      l[t,e] = x[t] . W_r[e] + b[e]        (fp32 accumulation)
+//   top-k + gates      warp per token; total order (value desc, index asc), NaN lowest;
+//                      gates = softmax of the k selected logits (fp32)
+//   grouping           per 32-token chunk a 32-bit mask per expert; a scan over
+//                      (chunk, expert) gives counts, exclusive offsets and chunk bases; the
+//                      scatter ranks each assignment inside its chunk with one popcount, so
+//                      the permutation is a stable counting sort with no atomics-order
+//                      dependence (identical on every run).
+// Sources: "DeepSeek V4.1F Q4 with native DSpark MTP on M3 Ultra", Decode paragraph (the
+// 384-expert router and its top-k in one dispatch); "Why SSD-streamed MoE was slow: 8GB Jetson
+// Orin Nano, part 2", the `mul_mat_id` grouped matmul and the section on generated text
+// changing between runs (every chosen expert computed exactly once -> bijection checks).
+#include <float.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// ============================================================================================
+// Router logits
+// ============================================================================================
+
+// Small T: one warp per expert and up to kTokTile tokens per block row (grid.y covers T).
+// Each lane walks its 8-element slices of d; W_r[e] is read once per block row.
+template <int kTokTile>
+__global__ void __launch_bounds__(256) router_logits_small_kernel(const uint16_t* __restrict__ x,
+                                                                  const float* __restrict__ wr,
+                                                                  const float* __restrict__ br, int T,
+                                                                  int E, int d,
+                                                                  float* __restrict__ logits) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + warp;
+  const int t0 = blockIdx.y * kTokTile;
+  if (e >= E) return;
+  const int nt = min(kTokTile, T - t0);
+  float acc[kTokTile];
+#pragma unroll
+  for (int t = 0; t < kTokTile; ++t) acc[t] = 0.f;
+  const float* w = wr + static_cast<size_t>(e) * d;
+  for (int i = lane * 8; i < d; i += 256) {
+    const float4 w0 = *reinterpret_cast<const float4*>(w + i);
+    const float4 w1 = *reinterpret_cast<const float4*>(w + i + 4);
+#pragma unroll
+    for (int t = 0; t < kTokTile; ++t) {
+      if (t < nt) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(t0 + t) * d + i);
+        float xf[8];
+        bf16x8_to_f32(xv, xf);
+        float a = acc[t];
+        a = fmaf(xf[0], w0.x, a);
+        a = fmaf(xf[1], w0.y, a);
+        a = fmaf(xf[2], w0.z, a);
+        a = fmaf(xf[3], w0.w, a);
+        a = fmaf(xf[4], w1.x, a);
+        a = fmaf(xf[5], w1.y, a);
+        a = fmaf(xf[6], w1.z, a);
+        a = fmaf(xf[7], w1.w, a);
+        acc[t] = a;
+      }
+    }
+  }
+  const float bias = br ? br[e] : 0.f;
+#pragma unroll
+  for (int t = 0; t < kTokTile; ++t) {
+    if (t < nt) {
+      float v = acc[t];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) logits[static_cast<size_t>(t0 + t) * E + e] = v + bias;
+    }
+  }
+}
+
+// Large T: 64 tokens x 64 experts per block, 32-deep K slices staged in shared memory,
+// 4 x 4 outputs per thread.
+__global__ void __launch_bounds__(256) router_logits_tiled_kernel(const uint16_t* __restrict__ x,
+                                                                  const float* __restrict__ wr,
+                                                                  const float* __restrict__ br, int T,
+                                                                  int E, int d,
+                                                                  float* __restrict__ logits) {
+  constexpr int BM = 64, BN = 64, BK = 32;
+  __shared__ float xs[BK][BM + 4];
+  __shared__ float ws[BK][BN + 4];
+  const int tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;
+  const int t0 = blockIdx.x * BM, e0 = blockIdx.y * BN;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < d; k0 += BK) {
+    // x tile: 64 rows x 32 bf16 = 256 chunks of 8
+    {
+      const int r = tid >> 2, c = (tid & 3) * 8;
+      float xf[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (t0 + r < T) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(t0 + r) * d + k0 + c);
+        bf16x8_to_f32(xv, xf);
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) xs[c + q][r] = xf[q];
+    }
+    // w tile: 64 rows x 32 fp32 = 512 float4
+#pragma unroll
+    for (int rep = 0; rep < 2; ++rep) {
+      const int idx = tid + rep * 256;
+      const int r = idx >> 3, c = (idx & 7) * 4;
+      float4 wv = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e0 + r < E) wv = *reinterpret_cast<const float4*>(wr + static_cast<size_t>(e0 + r) * d + k0 + c);
+      ws[c + 0][r] = wv.x;
+      ws[c + 1][r] = wv.y;
+      ws[c + 2][r] = wv.z;
+      ws[c + 3][r] = wv.w;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < BK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = xs[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = ws[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e < E) logits[static_cast<size_t>(t) * E + e] = acc[i][j] + (br ? br[e] : 0.f);
+    }
+  }
+}
+
+cudaError_t launch_router_logits(const uint16_t* x, const float* w_router, const float* b_router, int T,
+                                 int E, int d, float* logits, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  if (T <= 128) {
+    dim3 grid((E + 7) / 8, (T + 15) / 16);
+    router_logits_small_kernel<16><<<grid, 256, 0, st>>>(x, w_router, b_router, T, E, d, logits);
+  } else {
+    dim3 grid((T + 63) / 64, (E + 63) / 64);
+    router_logits_tiled_kernel<<<grid, 256, 0, st>>>(x, w_router, b_router, T, E, d, logits);
+  }
+  return cudaGetLastError();
+}
+
+// ============================================================================================
+// Top-k with gates
+// ============================================================================================
+
+// true if (va, ia) comes before (vb, ib): larger value first, then lower index; NaN after all
+// numbers (NaNs among themselves by index); -0 == +0.
+MOE_DEVICE bool rank_before(float va, int ia, float vb, int ib) {
+  const bool na = isnan(va), nb = isnan(vb);
+  if (na != nb) return nb;
+  if (!na && va != vb) return va > vb;
+  return ia < ib;
+}
+
+constexpr int kMaxPerLane = 32;  // E <= 1024
+
+// One block per 32-token chunk, 8 warps x 4 tokens.
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                   int32_t* __restrict__ ids, float* __restrict__ gates,
+                                                   uint32_t* __restrict__ masks, uint32_t* err) {
+  extern __shared__ uint32_t smask[];  // [E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x;
+  if (masks)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) smask[e] = 0u;
+  __syncthreads();
+  const int per_lane = (E + 31) / 32;
+  for (int tl = warp; tl < kChunk; tl += 8) {
+    const int t = c * kChunk + tl;
+    if (t >= T) break;
+    const float* row = logits + static_cast<size_t>(t) * E;
+    float v[kMaxPerLane];
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = (i < per_lane && e < E) ? row[e] : __int_as_float(0x7fc00000);
+    }
+    uint32_t taken = 0u;
+    float sel_v = 0.f;   // lane j keeps the value chosen in round j
+    int sel_i = 0;
+    for (int j = 0; j < k; ++j) {
+      float bv = __int_as_float(0x7fc00000);
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < kMaxPerLane; ++i) {
+        const int e = lane + 32 * i;
+        if (i < per_lane && e < E && !((taken >> i) & 1u) && rank_before(v[i], e, bv, bi)) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (rank_before(ov, oi, bv, bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == j) {
+        sel_v = bv;
+        sel_i = bi;
+      }
+    }
+    // gates: softmax over the k selected logits, slot 0 holds the maximum
+    const float vmax = __shfl_sync(0xffffffffu, sel_v, 0);
+    float ex = (lane < k) ? expf(sel_v - vmax) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const bool bad = (lane < k) && !isfinite(sel_v);
+    if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(err, MOE_DEVERR_NONFINITE);
+    if (lane < k) {
+      ids[static_cast<size_t>(t) * k + lane] = sel_i;
+      gates[static_cast<size_t>(t) * k + lane] = ex / sum;
+      if (masks) atomicOr(&smask[sel_i], 1u << tl);
+    }
+  }
+  if (masks) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) masks[static_cast<size_t>(c) * E + e] = smask[e];
+  }
+}
+
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* gates,
+                        uint32_t* masks, uint32_t* err, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  const int n_chunks = (T + kChunk - 1) / kChunk;
+  topk_kernel<<<n_chunks, 256, masks ? E * sizeof(uint32_t) : 0, st>>>(logits, T, E, k, ids, gates,
+                                                                      masks, err);
+  return cudaGetLastError();
+}
+
+// ============================================================================================
+// Grouping
+// ============================================================================================
+
+// Assignment (t, j) is used iff its id is in range and no earlier slot of the token has it.
+MOE_DEVICE bool assignment_valid(const int32_t* __restrict__ ids_row, int j, int e, int E) {
+  if (e < 0 || e >= E) return false;
+  for (int q = 0; q < j; ++q)
+    if (ids_row[q] == e) return false;
+  return true;
+}
+
+__global__ void __launch_bounds__(256) masks_from_ids_kernel(const int32_t* __restrict__ ids, int T, int E,
+                                                             int k, uint32_t* __restrict__ masks,
+                                                             uint32_t* err) {
+  extern __shared__ uint32_t smask[];
+  const int c = blockIdx.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) smask[e] = 0u;
+  __syncthreads();
+  for (int a = threadIdx.x; a < kChunk * k; a += blockDim.x) {
+    const int tl = a / k, j = a % k;
+    const int t = c * kChunk + tl;
+    if (t >= T) continue;
+    const int32_t* row = ids + static_cast<size_t>(t) * k;
+    const int e = row[j];
+    if (e < 0 || e >= E) {
+      set_error(err, MOE_DEVERR_EXPERT_RANGE);
+      continue;
+    }
+    if (!assignment_valid(row, j, e, E)) {
+      set_error(err, MOE_DEVERR_EXPERT_RANGE);
+      continue;
+    }
+    atomicOr(&smask[e], 1u << tl);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) masks[static_cast<size_t>(c) * E + e] = smask[e];
+}
+
+cudaError_t launch_masks_from_ids(const int32_t* ids, int T, int E, int k, uint32_t* masks,
+                                  uint32_t* err, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  const int n_chunks = (T + kChunk - 1) / kChunk;
+  masks_from_ids_kernel<<<n_chunks, 256, E * sizeof(uint32_t), st>>>(ids, T, E, k, masks, err);
+  return cudaGetLastError();
+}
+
+// Exclusive scan of one int per thread over a 1024-thread block.  Returns the exclusive
+// prefix; *total receives the block sum.
+MOE_DEVICE int block_exclusive_scan(int v, int* total) {
+  __shared__ int warp_sums[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  if (lane == 31) warp_sums[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    int s = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += n;
+    }
+    warp_sums[lane] = s;  // inclusive over warps
+  }
+  __syncthreads();
+  const int warp_excl = warp == 0 ? 0 : warp_sums[warp - 1];
+  *total = warp_sums[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return warp_excl + inc - v;
+}
+
+// Split `total` rows of expert e (starting at grouped row `start`) into near-equal segments
+// of at most kSegRowsMax rows.
+MOE_DEVICE int num_segments(int total) { return (total + kSegRowsMax - 1) / kSegRowsMax; }
+
+MOE_DEVICE void write_segments(Seg* segs, int base, int max_segs, int e, int start, int total,
+                               uint32_t* err) {
+  const int ns = num_segments(total);
+  if (ns == 0) return;
+  const int q = total / ns, rem = total % ns;
+  int r = start;
+  for (int s = 0; s < ns; ++s) {
+    const int rows = q + (s < rem ? 1 : 0);
+    if (base + s < max_segs) {
+      segs[base + s] = Seg{e, r, rows, 0};
+    } else {
+      set_error(err, MOE_DEVERR_SEGMENT);
+    }
+    r += rows;
+  }
+}
+
+// Single block of 1024 threads; thread e owns expert e (E <= 1024).
+__global__ void __launch_bounds__(1024) group_scan_kernel(const uint32_t* __restrict__ masks, int n_chunks,
+                                                          int E, int32_t* __restrict__ chunk_base,
+                                                          int32_t* __restrict__ counts,
+                                                          int32_t* __restrict__ offsets, Seg* segs,
+                                                          int32_t* n_segs, int max_segs, uint32_t* err) {
+  const int e = threadIdx.x;
+  int run = 0;
+  if (e < E) {
+    int c = 0;
+    for (; c + 4 <= n_chunks; c += 4) {
+      const uint32_t m0 = masks[static_cast<size_t>(c) * E + e];
+      const uint32_t m1 = masks[static_cast<size_t>(c + 1) * E + e];
+      const uint32_t m2 = masks[static_cast<size_t>(c + 2) * E + e];
+      const uint32_t m3 = masks[static_cast<size_t>(c + 3) * E + e];
+      chunk_base[static_cast<size_t>(c) * E + e] = run;
+      run += __popc(m0);
+      chunk_base[static_cast<size_t>(c + 1) * E + e] = run;
+      run += __popc(m1);
+      chunk_base[static_cast<size_t>(c + 2) * E + e] = run;
+      run += __popc(m2);
+      chunk_base[static_cast<size_t>(c + 3) * E + e] = run;
+      run += __popc(m3);
+    }
+    for (; c < n_chunks; ++c) {
+      chunk_base[static_cast<size_t>(c) * E + e] = run;
+      run += __popc(masks[static_cast<size_t>(c) * E + e]);
+    }
+  }
+  int total;
+  const int off = block_exclusive_scan(e < E ? run : 0, &total);
+  if (e < E) {
+    counts[e] = run;
+    offsets[e] = off;
+  }
+  if (e == 0) offsets[E] = total;
+  if (segs) {
+    int seg_total;
+    const int ns = e < E ? num_segments(run) : 0;
+    const int sbase = block_exclusive_scan(ns, &seg_total);
+    if (e < E) write_segments(segs, sbase, max_segs, e, off, run, err);
+    if (e == 0) *n_segs = min(seg_total, max_segs);
+  }
+}
+
+cudaError_t launch_group_scan(const uint32_t* masks, int n_chunks, int E, int32_t* chunk_base,
+                              int32_t* counts, int32_t* offsets, Seg* segs, int32_t* n_segs,
+                              int max_segs, uint32_t* err, cudaStream_t st) {
+  group_scan_kernel<<<1, 1024, 0, st>>>(masks, n_chunks, E, chunk_base, counts, offsets, segs, n_segs,
+                                        max_segs, err);
+  return cudaGetLastError();
+}
+
+__global__ void __launch_bounds__(256) scatter_kernel(const int32_t* __restrict__ ids,
+                                                      const uint32_t* __restrict__ masks,
+                                                      const int32_t* __restrict__ chunk_base,
+                                                      const int32_t* __restrict__ offsets, int T, int E,
+                                                      int k, int32_t* __restrict__ perm,
+                                                      int32_t* __restrict__ inv) {
+  const int c = blockIdx.x;
+  for (int a = threadIdx.x; a < kChunk * k; a += blockDim.x) {
+    const int tl = a / k, j = a % k;
+    const int t = c * kChunk + tl;
+    if (t >= T) continue;
+    const int32_t* row = ids + static_cast<size_t>(t) * k;
+    const int e = row[j];
+    const size_t ai = static_cast<size_t>(t) * k + j;
+    if (!assignment_valid(row, j, e, E)) {
+      inv[ai] = -1;
+      continue;
+    }
+    const uint32_t m = masks[static_cast<size_t>(c) * E + e];
+    const int rank = __popc(m & ((1u << tl) - 1u));
+    const int r = offsets[e] + chunk_base[static_cast<size_t>(c) * E + e] + rank;
+    perm[r] = static_cast<int32_t>(ai);
+    inv[ai] = r;
+  }
+}
+
+cudaError_t launch_scatter(const int32_t* ids, const uint32_t* masks, const int32_t* chunk_base,
+                           const int32_t* offsets, int T, int E, int k, int32_t* perm, int32_t* inv,
+                           cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  const int n_chunks = (T + kChunk - 1) / kChunk;
+  scatter_kernel<<<n_chunks, 256, 0, st>>>(ids, masks, chunk_base, offsets, T, E, k, perm, inv);
+  return cudaGetLastError();
+}
+
+__global__ void __launch_bounds__(1024) segments_from_offsets_kernel(const int32_t* __restrict__ offsets,
+                                                                     int E, Seg* segs, int32_t* n_segs,
+                                                                     int max_segs, uint32_t* err) {
+  const int e = threadIdx.x;
+  const int start = e < E ? offsets[e] : 0;
+  const int total = e < E ? offsets[e + 1] - start : 0;
+  int seg_total;
+  const int sbase = block_exclusive_scan(num_segments(total), &seg_total);
+  if (e < E) write_segments(segs, sbase, max_segs, e, start, total, err);
+  if (e == 0) *n_segs = min(seg_total, max_segs);
+}
+
+cudaError_t launch_segments_from_offsets(const int32_t* offsets, int E, Seg* segs, int32_t* n_segs,
+                                         int max_segs, uint32_t* err, cudaStream_t st) {
+  segments_from_offsets_kernel<<<1, 1024, 0, st>>>(offsets, E, segs, n_segs, max_segs, err);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

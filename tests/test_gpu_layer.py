@@ -1,0 +1,180 @@
+"""GPU parity of the expert FFN, the combine and the whole layer against the fp64 oracle.
+
+Small workloads are compared on every token; the large ones on a seeded sample of tokens plus
+every decode row (exact for those tokens: the layer is per token).  Tokens whose fp64 router
+margin is below 1e-3 are excluded from the output comparison and counted; routing must agree
+with the oracle on every other token."""
+import functools
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from moe_helpers import (TOL_BF16, TOL_FP4, bf16_tensor_to_f64, compare_layer, make_plan, oracle_layer,
+                         sample_rows, to_dev)
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+FULL = [("tiny", 0), ("decode", 0), ("mixed", 128), ("verify", 0)]
+SAMPLED = [("mixed", 2048), ("mixed", 8192), ("fp4_zipf", 0)]
+
+
+@functools.lru_cache(maxsize=None)
+def workload(name, q):
+    return synth.workload(name, quantum=q or 2048)
+
+
+@functools.lru_cache(maxsize=None)
+def plan_for(spec):
+    T_max = {synth.TINY: 64, synth.QWEN_A3B_LIKE: 8195, synth.FP4_ZIPF: 2051}[spec]
+    w = {synth.TINY: workload("tiny", 0), synth.QWEN_A3B_LIKE: workload("mixed", 8192),
+         synth.FP4_ZIPF: workload("fp4_zipf", 0)}[spec]
+    return make_plan(w, T_max=T_max)
+
+
+def paths_for(spec):
+    return ["simt", "tc"] if spec.wdtype == "bf16" else ["simt"]
+
+
+def _cases(lst):
+    return [(n, q, p) for n, q in lst for p in paths_for(workload(n, q).spec)]
+
+
+def _tol(w):
+    return TOL_FP4 if w.spec.wdtype == "mxfp4" else TOL_BF16
+
+
+@pytest.mark.parametrize("name,q,path", _cases(FULL))
+def test_forward_full_vs_oracle(name, q, path):
+    w = workload(name, q)
+    plan = plan_for(w.spec)
+    plan.set_path(path)
+    x = to_dev(w.x(), "bf16")
+    out = bf16_tensor_to_f64(plan.forward(x, n_prefill=w.n_prefill))
+    _, ids, _ = plan.route(x, want_logits=False)
+    ref = oracle_layer(w)
+    rel, excluded = compare_layer(out, ref, w.spec.k, _tol(w), ids.cpu().numpy())
+    assert plan.device_error() == 0
+    print(f"{name} q={q} {path}: max err {rel:.3e} x RMS, {excluded} tokens excluded")
+
+
+@pytest.mark.parametrize("name,q,path", _cases(SAMPLED))
+def test_forward_sampled_vs_oracle(name, q, path):
+    w = workload(name, q)
+    plan = plan_for(w.spec)
+    plan.set_path(path)
+    x = to_dev(w.x(), "bf16")
+    out = bf16_tensor_to_f64(plan.forward(x, n_prefill=w.n_prefill))
+    _, ids, _ = plan.route(x, want_logits=False)
+    rows = sample_rows(w, 96)
+    ref = oracle_layer(w, rows)
+    rel, excluded = compare_layer(out[rows], ref, w.spec.k, _tol(w), ids.cpu().numpy()[rows])
+    assert plan.device_error() == 0
+    print(f"{name} q={q} {path}: {len(rows)} rows, max err {rel:.3e} x RMS, {excluded} excluded")
+
+
+@pytest.mark.parametrize("name,q,path", _cases([("tiny", 0), ("decode", 0), ("mixed", 512), ("verify", 0)]))
+def test_experts_vs_oracle(name, q, path):
+    """The grouped FFN alone, on the oracle's own grouping."""
+    w = workload(name, q)
+    plan = plan_for(w.spec)
+    plan.set_path(path)
+    ref = oracle_layer(w)
+    y, ys = plan.experts(to_dev(w.x(), "bf16"), to_dev(ref["offsets"]), to_dev(ref["perm"]))
+    yg = y.double().cpu().numpy()
+    rms = np.sqrt(np.mean(ref["y_perm"] ** 2))
+    assert np.abs(yg - ref["y_perm"]).max() <= _tol(w) * rms
+    if ref["shared_y"] is not None:
+        sg = ys.double().cpu().numpy()
+        assert np.abs(sg - ref["shared_y"]).max() <= _tol(w) * np.sqrt(np.mean(ref["shared_y"] ** 2))
+
+
+def _bf16_ulp(v):
+    a = np.maximum(np.abs(v), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(a)) - 7)
+
+
+@pytest.mark.parametrize("T,k,d,shared", [(1, 2, 256, False), (33, 8, 2048, True), (257, 8, 4096, True)])
+def test_combine_vs_oracle(T, k, d, shared):
+    from decode_batches_gb300 import MoePlan
+    plan = MoePlan(16, k, d, 64, 0, "bf16")
+    rng = np.random.default_rng(T)
+    y = rng.normal(size=(T * k, d)).astype(np.float16)
+    ys = rng.normal(size=(T, d)).astype(np.float16) if shared else None
+    g = rng.random((T, k)).astype(np.float32)
+    g /= g.sum(1, keepdims=True)
+    inv = rng.permutation(T * k).astype(np.int32)
+    out = plan.combine(to_dev(y), to_dev(g), to_dev(inv), to_dev(ys) if shared else None)
+    y64 = y.astype(np.float64)
+    ys64 = ys.astype(np.float64) if shared else None
+    ref = oracle.combine(y64, g.astype(np.float64), inv, ys64)
+    got = bf16_tensor_to_f64(out)
+    # fp32 accumulation of k + 1 terms (relative rounding 2^-24 each on the running sum), then
+    # one rounding to bf16: within one bf16 ulp of the exact sum plus the fp32 accumulation bound
+    mag = oracle.combine(np.abs(y64), g.astype(np.float64), inv, np.abs(ys64) if shared else None)
+    bound = _bf16_ulp(ref) + (k + 2) * 2.0 ** -24 * mag
+    assert np.all(np.abs(got - ref) <= bound)
+
+
+def test_forward_deterministic_and_prefill_independent():
+    w = workload("mixed", 512)
+    plan = plan_for(w.spec)
+    plan.set_path("auto")
+    x = to_dev(w.x(), "bf16")
+    a = plan.forward(x, n_prefill=w.n_prefill).clone()
+    b = plan.forward(x, n_prefill=0).clone()
+    c = plan.forward(x, n_prefill=w.T).clone()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+
+
+def test_paths_agree():
+    w = workload("mixed", 128)
+    plan = plan_for(w.spec)
+    x = to_dev(w.x(), "bf16")
+    plan.set_path("simt")
+    a = bf16_tensor_to_f64(plan.forward(x, n_prefill=w.n_prefill))
+    plan.set_path("tc")
+    b = bf16_tensor_to_f64(plan.forward(x, n_prefill=w.n_prefill))
+    plan.set_path("auto")
+    rms = np.sqrt(np.mean(a ** 2))
+    # same arithmetic, different fp32 summation order: at most a couple of output ulps apart
+    assert np.all(np.abs(a - b) <= 2 * _bf16_ulp(np.maximum(np.abs(a), np.abs(b))) + 1e-3 * rms)
+
+
+@pytest.mark.parametrize("T", [1, 15, 16, 17, 255, 256, 257, 1000])
+def test_forward_ragged_sizes(T):
+    """T around the 16-column MMA step, the 32-token chunk and the 256-row segment limit."""
+    w = synth.custom(synth.QWEN_A3B_LIKE, T, n_prefill=T // 2, name=f"ragged{T}")
+    plan = plan_for(w.spec)
+    plan.set_path("auto")
+    x = to_dev(w.x(), "bf16")
+    out = bf16_tensor_to_f64(plan.forward(x, n_prefill=w.n_prefill))
+    rows = sample_rows(w, 48)
+    ref = oracle_layer(w, rows)
+    compare_layer(out[rows], ref, w.spec.k, TOL_BF16)
+
+
+def test_forward_edge_arguments_and_canaries():
+    from decode_batches_gb300 import MoeError
+    w = workload("tiny", 0)
+    plan = plan_for(w.spec)
+    x = to_dev(w.x(), "bf16")
+    empty = torch.empty((0, w.spec.d), dtype=torch.bfloat16, device="cuda")
+    plan.forward(empty)                                   # T = 0: no-op
+    with pytest.raises(MoeError):
+        plan.forward(x, n_prefill=w.T + 1)
+    big = synth.custom(w.spec, 65).x()
+    with pytest.raises(MoeError):
+        plan.forward(to_dev(big, "bf16"))                 # T > T_max of the workspace
+    # output written into the middle of a guarded buffer: guards untouched
+    guard = 1024
+    buf = torch.full((guard * 2 + w.T * w.spec.d,), 12345, dtype=torch.int16, device="cuda")
+    out_view = buf[guard:guard + w.T * w.spec.d].view(torch.bfloat16).view(w.T, w.spec.d)
+    plan.forward(x, out=out_view)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:guard] == 12345) and torch.all(buf[-guard:] == 12345)
+    ref = oracle_layer(w)
+    compare_layer(bf16_tensor_to_f64(out_view), ref, w.spec.k, TOL_BF16)
