@@ -342,12 +342,14 @@ def run_gpu(args):
         xq = dev(wq.x()).view(torch.bfloat16)
         cq = routing_counts(plan, xq)
         bq = layer_bytes_flops(wq, cq)
-        msq, _, _ = time_forward(plan, xq, wq.n_prefill, max(20, min(args.steps, 400)), max(3, args.warmup), world)
+        msq, kq, _ = time_forward(plan, xq, wq.n_prefill, max(20, min(args.steps, 400)), max(3, args.warmup), world,
+                                  timing=True)
         tq = max(bq["bytes"] / (hbm * 1e9), bq["flops"] / (tflops * 1e12))
         sweep.append({"quantum": q, "T": wq.T, "tokens_per_s": round(world * wq.T / (msq * 1e-3), 1),
                       "ms_per_step": round(msq, 5), "touched_experts": bq["touched"],
                       "roofline_frac": round(tq / (msq * 1e-3), 4),
-                      "bound": "hbm" if bq["bytes"] / (hbm * 1e9) >= bq["flops"] / (tflops * 1e12) else "tensor"})
+                      "bound": "hbm" if bq["bytes"] / (hbm * 1e9) >= bq["flops"] / (tflops * 1e12) else "tensor",
+                      "kernel_us": {k: round(v[1] / v[0] * 1e3, 2) for k, v in kq.items()}})
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

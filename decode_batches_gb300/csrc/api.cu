@@ -46,7 +46,7 @@ namespace {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t logits, ids, gates, masks, chunk_base, counts, offsets, perm, inv, segs, n_segs, h, h_s, y, y_s;
+  size_t logits, parts, ids, gates, masks, chunk_base, counts, offsets, perm, inv, segs, n_segs, h, h_s, y, y_s;
   size_t total;
   int max_segs;
 };
@@ -66,6 +66,9 @@ struct moe_plan {
   // plan-owned device memory
   float* w_router = nullptr;
   float* b_router = nullptr;
+  uint16_t* w_router3 = nullptr;  // W_r split into three bf16 pieces [3][E][d] (tensor-core router)
+  CUtensorMap map_router3{};
+  bool router_tc = false;
   uint8_t* w_gu = nullptr;
   uint8_t* s_gu = nullptr;
   uint8_t* w_down = nullptr;
@@ -86,6 +89,8 @@ struct moe_plan {
   std::vector<TimedLaunch> timed;
   std::vector<cudaEvent_t> event_pool;
   int launch_count = 0;
+
+  bool router_tc_capable() const { return E % 128 == 0 && d % 64 == 0; }
 };
 
 static WsLayout layout_for(const moe_plan* p, int T_max) {
@@ -101,6 +106,15 @@ static WsLayout layout_for(const moe_plan* p, int T_max) {
     return at;
   };
   L.logits = take(T * p->E * sizeof(float));
+  // partial router logits of the tensor-core router: splits(T') * T' rows for the worst T' <= T
+  size_t part_rows = 0;
+  if (p->router_tc_capable())
+    for (size_t m = 2; 128 * (m - 1) < T; ++m) {  // the largest T' of each 128-token tile count
+      const size_t tt = 128 * m < T ? 128 * m : T;
+      const size_t r = static_cast<size_t>(router_tc_splits(static_cast<int>(tt), p->E, p->d, p->num_sms)) * tt;
+      if (r > part_rows) part_rows = r;
+    }
+  L.parts = take(part_rows * p->E * sizeof(float));
   L.ids = take(R * sizeof(int32_t));
   L.gates = take(R * sizeof(float));
   L.masks = take(n_chunks * p->E * sizeof(uint32_t));
@@ -282,6 +296,9 @@ extern "C" moe_plan* moe_plan_create(int E, int k, int d_model, int d_ff, int n_
 }
 
 static void free_weights(moe_plan* p) {
+  cudaFree(p->w_router3);
+  p->w_router3 = nullptr;
+  p->router_tc = false;
   cudaFree(p->w_router);
   cudaFree(p->b_router);
   cudaFree(p->w_gu);
@@ -350,6 +367,16 @@ extern "C" moe_status moe_plan_set_weights(moe_plan* p, const float* w_router, c
   const size_t E = p->E, d = p->d, f = p->f;
   MOE_CUDA_TRY(cudaMalloc(&p->w_router, E * d * sizeof(float)));
   MOE_CUDA_TRY(cudaMemcpy(p->w_router, w_router, E * d * sizeof(float), cudaMemcpyDeviceToDevice));
+  if (p->router_tc_capable()) {
+    MOE_CUDA_TRY(cudaMalloc(&p->w_router3, 3 * E * d * sizeof(uint16_t)));
+    MOE_CUDA_TRY(launch_split_router(p->w_router, p->w_router3, E * d, 0));
+    s = make_map_16(&p->map_router3, p->w_router3, d, 3 * E, 128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+    if (s != MOE_OK) {
+      free_weights(p);
+      return s;
+    }
+    p->router_tc = true;
+  }
   MOE_CUDA_TRY(cudaMalloc(&p->b_router, E * sizeof(float)));
   if (b_router)
     MOE_CUDA_TRY(cudaMemcpy(p->b_router, b_router, E * sizeof(float), cudaMemcpyDeviceToDevice));
@@ -520,6 +547,23 @@ static moe_status run_experts(moe_plan* p, const uint16_t* x, int T, const int32
   return MOE_OK;
 }
 
+// Router logits + top-k (+ masks).  T > 128 with a tensor-core-capable shape uses the
+// tensor-core router (K-split partials summed by top-k); otherwise the CUDA-core router.
+static moe_status route_step(moe_plan* p, const uint16_t* x, int T, float* logits_out, int32_t* ids, float* gates,
+                             uint32_t* masks, cudaStream_t st) {
+  if (p->router_tc && T > 128) {
+    const int ns = router_tc_splits(T, p->E, p->d, p->num_sms);
+    float* parts = ws_ptr<float>(p, p->L.parts);
+    LAUNCH(p, "router_tc", st, launch_router_tc(&p->map_router3, x, T, p->E, p->d, ns, parts, p->err, st));
+    LAUNCH(p, "topk", st, launch_topk(parts, ns, p->b_router, logits_out, T, p->E, p->k, ids, gates, masks, p->err, st));
+  } else {
+    float* lg = logits_out ? logits_out : ws_ptr<float>(p, p->L.logits);
+    LAUNCH(p, "router_logits", st, launch_router_logits(x, p->w_router, p->b_router, T, p->E, p->d, lg, st));
+    LAUNCH(p, "topk", st, launch_topk(lg, 1, nullptr, nullptr, T, p->E, p->k, ids, gates, masks, p->err, st));
+  }
+  return MOE_OK;
+}
+
 extern "C" moe_status moe_layer_forward(moe_plan* p, const void* x, int T, int n_prefill, void* out,
                                         moe_stream_t stream) {
   moe_status s = check_ready(p, T, true);
@@ -530,7 +574,6 @@ extern "C" moe_status moe_layer_forward(moe_plan* p, const void* x, int T, int n
   if (!x || !out) return fail(MOE_ERR_INVALID_ARG, "x and out are required");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const uint16_t* xb = static_cast<const uint16_t*>(x);
-  float* logits = ws_ptr<float>(p, p->L.logits);
   int32_t* ids = ws_ptr<int32_t>(p, p->L.ids);
   float* gates = ws_ptr<float>(p, p->L.gates);
   uint32_t* masks = ws_ptr<uint32_t>(p, p->L.masks);
@@ -543,8 +586,8 @@ extern "C" moe_status moe_layer_forward(moe_plan* p, const void* x, int T, int n
   uint16_t* y_s = p->n_shared > 0 ? ws_ptr<uint16_t>(p, p->L.y_s) : nullptr;
   const int n_chunks = (T + kChunk - 1) / kChunk;
   const bool tc = use_tc(p);
-  LAUNCH(p, "router_logits", st, launch_router_logits(xb, p->w_router, p->b_router, T, p->E, p->d, logits, st));
-  LAUNCH(p, "topk", st, launch_topk(logits, T, p->E, p->k, ids, gates, masks, p->err, st));
+  s = route_step(p, xb, T, nullptr, ids, gates, masks, st);
+  if (s != MOE_OK) return s;
   LAUNCH(p, "group_scan", st,
          launch_group_scan(masks, n_chunks, p->E, chunk_base, counts, offsets, tc ? ws_ptr<Seg>(p, p->L.segs) : nullptr,
                            ws_ptr<int32_t>(p, p->L.n_segs), p->L.max_segs, p->err, st));
@@ -563,10 +606,7 @@ extern "C" moe_status moe_route(moe_plan* p, const void* x, int T, float* logits
   if (T == 0) return MOE_OK;
   if (!x || !ids || !gates) return fail(MOE_ERR_INVALID_ARG, "x, ids and gates are required");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  float* lg = logits ? logits : ws_ptr<float>(p, p->L.logits);
-  LAUNCH(p, "router_logits", st,
-         launch_router_logits(static_cast<const uint16_t*>(x), p->w_router, p->b_router, T, p->E, p->d, lg, st));
-  LAUNCH(p, "topk", st, launch_topk(lg, T, p->E, p->k, ids, gates, nullptr, p->err, st));
+  return route_step(p, static_cast<const uint16_t*>(x), T, logits, ids, gates, nullptr, st);
   return MOE_OK;
 }
 
@@ -580,7 +620,7 @@ extern "C" moe_status moe_route_logits(moe_plan* p, const float* logits, int T, 
   if (T == 0) return MOE_OK;
   if (!logits || !ids || !gates) return fail(MOE_ERR_INVALID_ARG, "logits, ids and gates are required");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  LAUNCH(p, "topk", st, launch_topk(logits, T, p->E, p->k, ids, gates, nullptr, p->err, st));
+  LAUNCH(p, "topk", st, launch_topk(logits, 1, nullptr, nullptr, T, p->E, p->k, ids, gates, nullptr, p->err, st));
   return MOE_OK;
 }
 

@@ -24,8 +24,11 @@
 //   warp 1      TMEM owner and MMA issuer (one thread)
 //   warps 2-5   epilogue (TMEM lanes 32*(warp%4) .. +31)
 //   warps 6-9   gate/up only: cp.async gather of the token rows
-// Pipeline: 4 shared-memory stages of (A 16 KB + B up to 32 KB), two TMEM accumulators of up
-// to 256 fp32 columns so the epilogue of one unit overlaps the main loop of the next.
+// Pipeline: 6 shared-memory stages of (A 16 KB + B up to 16 KB), two TMEM accumulators of up
+// to 128 fp32 columns so the epilogue of one unit overlaps the main loop of the next.  An
+// expert with more than 128 rows is split into parts; the units of its parts are ordered
+// tile-major (tile 0 of every part, then tile 1, ...) so that CTAs working on the same
+// weight tile run side by side and the second read of the tile is served by L2.
 // Every wait is bounded (see common.cuh); on a timeout the CTA stops issuing work, drains its
 // MMAs, frees TMEM and returns with MOE_DEVERR_TIMEOUT set.
 #include "common.cuh"
@@ -36,13 +39,13 @@ namespace tc {
 
 constexpr int BM = 128;                          // weight rows per unit (MMA M)
 constexpr int BK = 64;                           // K elements per stage (128-byte rows)
-constexpr int kStages = 4;
-constexpr int kLag = 2;                          // gather completion lag (stages)
+constexpr int kStages = 6;
+constexpr int kLag = 4;                          // gather completion lag (stages), < kStages
 constexpr int kABytes = BM * BK * 2;             // 16 KB
-constexpr int kBBytes = kSegRowsMax * BK * 2;    // 32 KB
+constexpr int kBBytes = kSegRowsMax * BK * 2;    // 16 KB (N <= 128)
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kTmemCols = 512;                   // 2 accumulators x 256 columns
-constexpr int kAccCols = 256;
+constexpr int kTmemCols = 2 * kSegRowsMax;       // 2 accumulators x 128 columns
+constexpr int kAccCols = kSegRowsMax;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*align slack*/;
 constexpr int kGatherThreads = 128;
 
@@ -66,11 +69,15 @@ MOE_DEVICE Unit decode_unit(int u, const TcArgs& a, int tiles_r, int tiles_s, in
     un.row_start = ss * q + min(ss, rem);
     un.rows = q + (ss < rem ? 1 : 0);
   } else {
+    // The parts [first, first + nparts) of one expert own units [first, first + nparts) * tiles;
+    // inside that range the tile index is the slow one and the part the fast one.
     const int v = u - n_shared_units;
-    const Seg s = a.segs[v / tiles_r];
+    const Seg any = a.segs[v / tiles_r];
+    const int o = v - any.first * tiles_r;
+    const Seg s = a.segs[any.first + o % any.nparts];
     un.shared = 0;
     un.expert = s.expert;
-    un.tile = v % tiles_r;
+    un.tile = o / any.nparts;
     un.row_start = s.row_start;
     un.rows = s.rows;
   }
@@ -245,12 +252,14 @@ __global__ void __launch_bounds__(kGateUp ? 320 : 192, 1)
             const int col = c0 + 2 * jj + (is_gate ? 0 : 1);
             const float gv = __uint_as_float(is_gate ? r[2 * jj] : recv);
             const float uv = __uint_as_float(is_gate ? recv : r[2 * jj + 1]);
-            float hv = swiglu(gv, uv);
-            if (!(fabsf(hv) <= kF16Max)) {
-              sat = true;
-              hv = fminf(fmaxf(hv, -kF16Max), kF16Max);
+            if (col < un.rows) {  // columns past the segment hold padding, never stored
+              float hv = swiglu(gv, uv);
+              if (!(fabsf(hv) <= kF16Max)) {
+                sat = true;
+                hv = fminf(fmaxf(hv, -kF16Max), kF16Max);
+              }
+              hout[static_cast<size_t>(un.row_start + col) * ldh + feat] = f32_to_f16_bits_rn(hv);
             }
-            if (col < un.rows) hout[static_cast<size_t>(un.row_start + col) * ldh + feat] = f32_to_f16_bits_rn(hv);
           }
         }
         if (__any_sync(0xffffffffu, sat) && lane == 0) set_error(a.err, MOE_DEVERR_RANGE);
@@ -264,12 +273,14 @@ __global__ void __launch_bounds__(kGateUp ? 320 : 192, 1)
           tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
-            float v = __uint_as_float(r[c]);
-            if (!(fabsf(v) <= kF16Max)) {
-              sat = true;
-              v = fminf(fmaxf(v, -kF16Max), kF16Max);
+            if (c0 + c < un.rows) {
+              float v = __uint_as_float(r[c]);
+              if (!(fabsf(v) <= kF16Max)) {
+                sat = true;
+                v = fminf(fmaxf(v, -kF16Max), kF16Max);
+              }
+              yout[static_cast<size_t>(un.row_start + c0 + c) * a.d + feat] = f32_to_f16_bits_rn(v);
             }
-            if (c0 + c < un.rows) yout[static_cast<size_t>(un.row_start + c0 + c) * a.d + feat] = f32_to_f16_bits_rn(v);
           }
         }
         if (__any_sync(0xffffffffu, sat) && lane == 0) set_error(a.err, MOE_DEVERR_RANGE);
@@ -280,17 +291,23 @@ __global__ void __launch_bounds__(kGateUp ? 320 : 192, 1)
     }
   } else if (kGateUp) {
     // ---------------- token-row gather (cp.async) ----------------
+    // 8 consecutive threads copy the 8 16-byte chunks of one row (a full 128-byte line per 8
+    // lanes); thread p handles chunk p % 8 of rows p / 8 + 16 i, i = 0..7.
     const int p = threadIdx.x - 192;  // 0..127
+    const int ch = p & 7, r0 = p >> 3;
     uint32_t g = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
       const Unit un = decode_unit(u, a, tiles_r, tiles_s, n_shared_units);
-      int tok[2];
+      const uint16_t* src[kSegRowsMax / 16];
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int n = p + kGatherThreads * i;
-        tok[i] = -1;
-        if (n < un.rows) tok[i] = un.shared ? un.row_start + n : a.perm[un.row_start + n] / a.k;
+      for (int i = 0; i < kSegRowsMax / 16; ++i) {
+        const int n = r0 + 16 * i;
+        src[i] = nullptr;
+        if (n < un.rows) {
+          const int tok = un.shared ? un.row_start + n : a.perm[un.row_start + n] / a.k;
+          src[i] = a.x + static_cast<size_t>(tok) * a.d + ch * 8;
+        }
       }
       for (int kk = 0; kk < nk_r; ++kk, ++g) {
         const int slot = g % kStages;
@@ -301,13 +318,9 @@ __global__ void __launch_bounds__(kGateUp ? 320 : 192, 1)
         }
         const uint32_t sb = smem_u32(smem + slot * kStageBytes + kABytes);
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          if (tok[i] < 0) continue;
-          const int n = p + kGatherThreads * i;
-          const uint16_t* src = a.x + static_cast<size_t>(tok[i]) * a.d + kk * BK;
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch)
-            cp_async_16(sb + n * 128 + ((ch ^ (n & 7)) << 4), src + ch * 8);
+        for (int i = 0; i < kSegRowsMax / 16; ++i) {
+          const int n = r0 + 16 * i;
+          if (src[i]) cp_async_16(sb + n * 128 + ((ch ^ (n & 7)) << 4), src[i] + kk * BK);
         }
         cp_async_commit();
         if (g >= kLag) {

@@ -9,27 +9,38 @@ namespace moe {
 
 // Tokens per chunk of the grouping step: one 32-bit mask word per (chunk, expert).
 constexpr int kChunk = 32;
-// Largest number of rows one tensor-core unit handles (the MMA's N <= 256).
-constexpr int kSegRowsMax = 256;
+// Largest number of rows one tensor-core unit handles (the MMA's N).
+constexpr int kSegRowsMax = 128;
 
 // One segment of the grouped problem: `rows` consecutive grouped rows of one expert starting
-// at `row_start` (expert >= 0), or `rows` consecutive tokens starting at token `row_start` for
-// the shared experts (expert == -1).
+// at `row_start`.  An expert with more than kSegRowsMax rows has several parts; `first` is
+// the index of its first part in the segment list and `nparts` their number.
 struct Seg {
   int expert;
   int row_start;
   int rows;
-  int pad;
+  int first;
+  int nparts;
+  int pad0, pad1, pad2;
 };
 
 // ---- routing and grouping (route.cu) --------------------------------------------------------
 // logits[t][e] = x[t] . w_router[e] + b[e] (fp32 accumulation).
 cudaError_t launch_router_logits(const uint16_t* x, const float* w_router, const float* b_router, int T,
                                  int E, int d, float* logits, cudaStream_t st);
-// Top-k + softmax gates per token; if masks != nullptr also writes the per-chunk expert masks
-// (bit t of masks[c][e] <=> token c*32+t chose e).
-cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* gates,
-                        uint32_t* masks, uint32_t* err, cudaStream_t st);
+// Top-k + softmax gates per token.  The logits are sum_s parts[s][T][E] (+ bias[e]) and are
+// written to logits_out if given.  If masks != nullptr also writes the per-chunk expert masks,
+// expert-major: bit t of masks[e * n_chunks + c] <=> token c*32+t chose e.
+cudaError_t launch_topk(const float* parts, int nsplit, const float* bias, float* logits_out, int T, int E, int k,
+                        int32_t* ids, float* gates, uint32_t* masks, uint32_t* err, cudaStream_t st);
+
+// ---- tensor-core router (router_tc.cu) --------------------------------------------------------
+// parts[s][T][E] = x[T][k-range s] . W_r[E][k-range s]^T with W_r split into three bf16 pieces
+// (w3: 2-D map over [3E rows][d], box 64 x 128).  Requires E % 128 == 0 and d % 64 == 0.
+int router_tc_splits(int T, int E, int d, int num_sms);
+cudaError_t launch_router_tc(const CUtensorMap* w3, const uint16_t* x, int T, int E, int d, int nsplit, float* parts,
+                             uint32_t* err, cudaStream_t st);
+cudaError_t launch_split_router(const float* w, uint16_t* w3, size_t n, cudaStream_t st);
 // Per-chunk expert masks from given ids (validates range / duplicates).
 cudaError_t launch_masks_from_ids(const int32_t* ids, int T, int E, int k, uint32_t* masks,
                                   uint32_t* err, cudaStream_t st);
@@ -93,7 +104,7 @@ struct TcArgs {
   uint16_t* y_s = nullptr;
   uint32_t* err = nullptr;
   int T = 0, E = 0, k = 0, d = 0, f = 0, n_shared = 0, f_s = 0;
-  int n_shared_segs = 0;   // ceil(T / kSegRowsMax) when n_shared > 0
+  int n_shared_segs = 0;   // ceil(T / kSegRowsMax) when n_shared > 0 (shared tokens split evenly)
 };
 
 cudaError_t launch_tc_gateup(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st);

@@ -165,39 +165,52 @@ MOE_DEVICE bool rank_before(float va, int ia, float vb, int ib) {
   return ia < ib;
 }
 
-constexpr int kMaxPerLane = 32;  // E <= 1024
+// One block per 32-token chunk, one warp per token (two per warp for E > 384).  Lane l holds the logits of experts
+// l, l + 32, ..., l + 32 (PL - 1); each of the k rounds takes the lane-local best untaken value
+// and a warp arg-max under rank_before.  Masks are stored expert-major: masks[e * n_chunks + c].
+// The logits are the sum of `nsplit` partial matrices parts[s][T][E] (s ascending) plus the
+// optional bias; they are written to logits_out when it is given.
+template <int PL>
+constexpr int topk_threads() { return PL >= 16 ? 512 : 1024; }  // 64 registers/thread at 1024
 
-// One block per 32-token chunk, 8 warps x 4 tokens.
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int T, int E, int k,
-                                                   int32_t* __restrict__ ids, float* __restrict__ gates,
-                                                   uint32_t* __restrict__ masks, uint32_t* err) {
+template <int PL>
+__global__ void __launch_bounds__(topk_threads<PL>()) topk_kernel(const float* __restrict__ parts, int nsplit,
+                                                    const float* __restrict__ bias, float* __restrict__ logits_out,
+                                                    int T, int E, int k, int n_chunks, int32_t* __restrict__ ids,
+                                                    float* __restrict__ gates, uint32_t* __restrict__ masks,
+                                                    uint32_t* err) {
   extern __shared__ uint32_t smask[];  // [E]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
   if (masks)
     for (int e = threadIdx.x; e < E; e += blockDim.x) smask[e] = 0u;
   __syncthreads();
-  const int per_lane = (E + 31) / 32;
-  for (int tl = warp; tl < kChunk; tl += 8) {
+  for (int tl = warp; tl < kChunk; tl += blockDim.x / 32) {
     const int t = c * kChunk + tl;
     if (t >= T) break;
-    const float* row = logits + static_cast<size_t>(t) * E;
-    float v[kMaxPerLane];
+    float v[PL];
 #pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
+    for (int i = 0; i < PL; ++i) {
       const int e = lane + 32 * i;
-      v[i] = (i < per_lane && e < E) ? row[e] : __int_as_float(0x7fc00000);
+      float acc = __int_as_float(0x7fc00000);
+      if (e < E) {
+        acc = parts[static_cast<size_t>(t) * E + e];
+        for (int sp = 1; sp < nsplit; ++sp) acc += parts[(static_cast<size_t>(sp) * T + t) * E + e];
+        if (bias) acc += bias[e];
+        if (logits_out) logits_out[static_cast<size_t>(t) * E + e] = acc;
+      }
+      v[i] = acc;
     }
     uint32_t taken = 0u;
-    float sel_v = 0.f;   // lane j keeps the value chosen in round j
+    float sel_v = 0.f;  // lane j keeps the value chosen in round j
     int sel_i = 0;
     for (int j = 0; j < k; ++j) {
       float bv = __int_as_float(0x7fc00000);
       int bi = 0x7fffffff;
 #pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i) {
+      for (int i = 0; i < PL; ++i) {
         const int e = lane + 32 * i;
-        if (i < per_lane && e < E && !((taken >> i) & 1u) && rank_before(v[i], e, bv, bi)) {
+        if (e < E && !((taken >> i) & 1u) && rank_before(v[i], e, bv, bi)) {
           bv = v[i];
           bi = e;
         }
@@ -219,7 +232,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
     }
     // gates: softmax over the k selected logits, slot 0 holds the maximum
     const float vmax = __shfl_sync(0xffffffffu, sel_v, 0);
-    float ex = (lane < k) ? expf(sel_v - vmax) : 0.f;
+    const float ex = (lane < k) ? expf(sel_v - vmax) : 0.f;
     float sum = ex;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
@@ -233,16 +246,31 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
   }
   if (masks) {
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) masks[static_cast<size_t>(c) * E + e] = smask[e];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) masks[static_cast<size_t>(e) * n_chunks + c] = smask[e];
   }
 }
 
-cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* gates,
-                        uint32_t* masks, uint32_t* err, cudaStream_t st) {
+template <int PL>
+static void launch_topk_pl(const float* parts, int nsplit, const float* bias, float* logits_out, int T, int E, int k,
+                           int n_chunks, int32_t* ids, float* gates, uint32_t* masks, uint32_t* err, cudaStream_t st) {
+  topk_kernel<PL><<<n_chunks, topk_threads<PL>(), masks ? E * sizeof(uint32_t) : 0, st>>>(
+      parts, nsplit, bias, logits_out, T, E, k, n_chunks, ids, gates, masks, err);
+}
+
+cudaError_t launch_topk(const float* parts, int nsplit, const float* bias, float* logits_out, int T, int E, int k,
+                        int32_t* ids, float* gates, uint32_t* masks, uint32_t* err, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
   const int n_chunks = (T + kChunk - 1) / kChunk;
-  topk_kernel<<<n_chunks, 256, masks ? E * sizeof(uint32_t) : 0, st>>>(logits, T, E, k, ids, gates,
-                                                                      masks, err);
+  const int pl = (E + 31) / 32;
+#define MOE_TOPK(PLV) launch_topk_pl<PLV>(parts, nsplit, bias, logits_out, T, E, k, n_chunks, ids, gates, masks, err, st)
+  if (pl <= 1) MOE_TOPK(1);
+  else if (pl <= 2) MOE_TOPK(2);
+  else if (pl <= 4) MOE_TOPK(4);
+  else if (pl <= 8) MOE_TOPK(8);
+  else if (pl <= 12) MOE_TOPK(12);
+  else if (pl <= 16) MOE_TOPK(16);
+  else MOE_TOPK(32);
+#undef MOE_TOPK
   return cudaGetLastError();
 }
 
@@ -259,7 +287,7 @@ MOE_DEVICE bool assignment_valid(const int32_t* __restrict__ ids_row, int j, int
 }
 
 __global__ void __launch_bounds__(256) masks_from_ids_kernel(const int32_t* __restrict__ ids, int T, int E,
-                                                             int k, uint32_t* __restrict__ masks,
+                                                             int k, int n_chunks, uint32_t* __restrict__ masks,
                                                              uint32_t* err) {
   extern __shared__ uint32_t smask[];
   const int c = blockIdx.x;
@@ -282,14 +310,14 @@ __global__ void __launch_bounds__(256) masks_from_ids_kernel(const int32_t* __re
     atomicOr(&smask[e], 1u << tl);
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) masks[static_cast<size_t>(c) * E + e] = smask[e];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) masks[static_cast<size_t>(e) * n_chunks + c] = smask[e];
 }
 
 cudaError_t launch_masks_from_ids(const int32_t* ids, int T, int E, int k, uint32_t* masks,
                                   uint32_t* err, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
   const int n_chunks = (T + kChunk - 1) / kChunk;
-  masks_from_ids_kernel<<<n_chunks, 256, E * sizeof(uint32_t), st>>>(ids, T, E, k, masks, err);
+  masks_from_ids_kernel<<<n_chunks, 256, E * sizeof(uint32_t), st>>>(ids, T, E, k, n_chunks, masks, err);
   return cudaGetLastError();
 }
 
@@ -336,7 +364,7 @@ MOE_DEVICE void write_segments(Seg* segs, int base, int max_segs, int e, int sta
   for (int s = 0; s < ns; ++s) {
     const int rows = q + (s < rem ? 1 : 0);
     if (base + s < max_segs) {
-      segs[base + s] = Seg{e, r, rows, 0};
+      segs[base + s] = Seg{e, r, rows, base, ns, 0, 0, 0};
     } else {
       set_error(err, MOE_DEVERR_SEGMENT);
     }
@@ -344,37 +372,39 @@ MOE_DEVICE void write_segments(Seg* segs, int base, int max_segs, int e, int sta
   }
 }
 
-// Single block of 1024 threads; thread e owns expert e (E <= 1024).
+// Single block of 1024 threads.  Warp w scans experts w, w + 32, ...: 32 consecutive chunk masks
+// of one expert per load (masks are expert-major), popcount, warp prefix sum -> chunk bases.
+// Then thread e scans the expert totals -> offsets, and writes the expert's segments.
 __global__ void __launch_bounds__(1024) group_scan_kernel(const uint32_t* __restrict__ masks, int n_chunks,
                                                           int E, int32_t* __restrict__ chunk_base,
                                                           int32_t* __restrict__ counts,
                                                           int32_t* __restrict__ offsets, Seg* segs,
                                                           int32_t* n_segs, int max_segs, uint32_t* err) {
-  const int e = threadIdx.x;
-  int run = 0;
-  if (e < E) {
-    int c = 0;
-    for (; c + 4 <= n_chunks; c += 4) {
-      const uint32_t m0 = masks[static_cast<size_t>(c) * E + e];
-      const uint32_t m1 = masks[static_cast<size_t>(c + 1) * E + e];
-      const uint32_t m2 = masks[static_cast<size_t>(c + 2) * E + e];
-      const uint32_t m3 = masks[static_cast<size_t>(c + 3) * E + e];
-      chunk_base[static_cast<size_t>(c) * E + e] = run;
-      run += __popc(m0);
-      chunk_base[static_cast<size_t>(c + 1) * E + e] = run;
-      run += __popc(m1);
-      chunk_base[static_cast<size_t>(c + 2) * E + e] = run;
-      run += __popc(m2);
-      chunk_base[static_cast<size_t>(c + 3) * E + e] = run;
-      run += __popc(m3);
+  __shared__ int s_total[1024];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = warp; e < E; e += 32) {
+    const uint32_t* m = masks + static_cast<size_t>(e) * n_chunks;
+    int32_t* cb = chunk_base + static_cast<size_t>(e) * n_chunks;
+    int run = 0;
+    for (int c0 = 0; c0 < n_chunks; c0 += 32) {
+      const int c = c0 + lane;
+      const int n = c < n_chunks ? __popc(m[c]) : 0;
+      int inc = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int up = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += up;
+      }
+      if (c < n_chunks) cb[c] = run + inc - n;
+      run += __shfl_sync(0xffffffffu, inc, 31);
     }
-    for (; c < n_chunks; ++c) {
-      chunk_base[static_cast<size_t>(c) * E + e] = run;
-      run += __popc(masks[static_cast<size_t>(c) * E + e]);
-    }
+    if (lane == 0) s_total[e] = run;
   }
+  __syncthreads();
+  const int e = threadIdx.x;
+  const int run = e < E ? s_total[e] : 0;
   int total;
-  const int off = block_exclusive_scan(e < E ? run : 0, &total);
+  const int off = block_exclusive_scan(run, &total);
   if (e < E) {
     counts[e] = run;
     offsets[e] = off;
@@ -404,6 +434,7 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int32_t* __restrict_
                                                       int k, int32_t* __restrict__ perm,
                                                       int32_t* __restrict__ inv) {
   const int c = blockIdx.x;
+  const int n_chunks = gridDim.x;
   for (int a = threadIdx.x; a < kChunk * k; a += blockDim.x) {
     const int tl = a / k, j = a % k;
     const int t = c * kChunk + tl;
@@ -415,9 +446,9 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int32_t* __restrict_
       inv[ai] = -1;
       continue;
     }
-    const uint32_t m = masks[static_cast<size_t>(c) * E + e];
-    const int rank = __popc(m & ((1u << tl) - 1u));
-    const int r = offsets[e] + chunk_base[static_cast<size_t>(c) * E + e] + rank;
+    const size_t me = static_cast<size_t>(e) * n_chunks + c;
+    const int rank = __popc(masks[me] & ((1u << tl) - 1u));
+    const int r = offsets[e] + chunk_base[me] + rank;
     perm[r] = static_cast<int32_t>(ai);
     inv[ai] = r;
   }

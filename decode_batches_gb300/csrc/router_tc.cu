@@ -1,0 +1,224 @@
+// Router logits on the tensor cores for large T.
+//
+// l[t, e] = x[t] . W_r[e] + b[e] with fp32 router weights.  W_r is split once, at set-up, into
+// three bf16 matrices W_r = W1 + W2 + W3 exactly (W1 = bf16(W_r), W2 = bf16(W_r - W1),
+// W3 = W_r - W1 - W2, which has at most 8 significant bits left).  x is bf16, so every product
+// x * Wp is exact in fp32 and the MMAs accumulate, in fp32 TMEM, the sum an fp32 FMA loop
+// would form -- at bf16 tensor-core rate instead of CUDA-core FMA rate.
+//
+// Tile: 128 experts (M, the A operand, TMA) x up to 128 tokens (N, the B operand, cp.async) x a
+// K range of at most 512.  The tensor core's internal fp32 accumulation loses about 2^-24 of the
+// running sum per MMA step, so chains are kept short: W1 accumulates in one TMEM accumulator
+// (<= 32 steps per K range) and W2 + W3, 2^-8 smaller, in a second one; the epilogue adds the
+// two in IEEE fp32.  Partial sums land in parts[split][t][e] and the top-k kernel adds them in a
+// fixed order (deterministic).
+// The router of the "DeepSeek V4.1F Q4 with native DSpark MTP on M3 Ultra" post (Decode
+// paragraph) is one dispatch; here it is one GEMM launch plus the top-k launch.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace rt {
+
+constexpr int BM = 128;                 // experts per tile
+constexpr int BN = 128;                 // tokens per tile
+constexpr int BK = 64;
+constexpr int kPieces = 3;
+constexpr int kStages = 3;
+constexpr int kABytes = BM * BK * 2;    // one piece
+constexpr int kBBytes = BN * BK * 2;
+constexpr int kStageBytes = kPieces * kABytes + kBBytes;  // 64 KB
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024;
+constexpr int kGather = 128;
+
+__global__ void __launch_bounds__(320, 1)
+    router_tc_kernel(const __grid_constant__ CUtensorMap w3, const uint16_t* __restrict__ x, int T, int E, int d,
+                     int nsplit, float* __restrict__ parts, uint32_t* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e0 = blockIdx.x * BM;
+  const int t0 = blockIdx.y * BN;
+  const int split = blockIdx.z;
+  const int nk = d / BK;
+  const int kc0 = split * nk / nsplit, kc1 = (split + 1) * nk / nsplit;
+  const int rows = min(BN, T - t0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1 + kGather);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) tma_prefetch_map(&w3);
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 2 * BN);  // [0, BN): W1 chain, [BN, 2 BN): W2 + W3 chain
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_last();  // W pieces are re-read by every token tile
+      for (int kc = kc0, g = 0; kc < kc1; ++kc, ++g) {
+        const int slot = g % kStages;
+        const uint32_t use = g / kStages;
+        if (!mbar_wait(&empty[slot], (use & 1u) ^ 1u, abort_flag, err)) break;
+        uint8_t* sa = smem + slot * kStageBytes;
+        mbar_arrive_expect_tx(&full[slot], kPieces * kABytes);
+        for (int p = 0; p < kPieces; ++p) tma_load_2d(sa + p * kABytes, &w3, &full[slot], kc * BK, p * E + e0, pol);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t N = rows <= 16 ? 16u : static_cast<uint32_t>((rows + 15) & ~15);
+      const uint32_t idesc = idesc_bf16_f32(BM, N);
+      bool ok = true;
+      for (int kc = kc0, g = 0; kc < kc1; ++kc, ++g) {
+        const int slot = g % kStages;
+        const uint32_t use = g / kStages;
+        if (!mbar_wait(&full[slot], use & 1u, abort_flag, err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + slot * kStageBytes);
+        const uint64_t bdesc = smem_desc_sw128(sa + kPieces * kABytes);
+#pragma unroll
+        for (int p = 0; p < kPieces; ++p) {
+          const uint64_t adesc = smem_desc_sw128(sa + p * kABytes);
+#pragma unroll
+          for (int ks = 0; ks < BK / 16; ++ks) {
+            const bool first = kc == kc0 && ks == 0 && p != 2;  // p = 2 adds onto the p = 1 chain
+            mma_f16_ss(p == 0 ? tmem : tmem + BN, adesc + 2 * ks, bdesc + 2 * ks, idesc, first ? 0u : 1u);
+          }
+        }
+        mma_commit(&empty[slot]);
+      }
+      mma_commit(acc_full);  // also drains every MMA before the epilogue / dealloc
+      if (!ok) *abort_flag = 1;
+    }
+  } else if (warp < 6) {
+    const int q = warp & 3;
+    if (mbar_wait(acc_full, 0, abort_flag, err)) {
+      tc_fence_after();
+      const int e = e0 + 32 * q + lane;
+      float* out = parts + (static_cast<size_t>(split) * T + t0) * E + e;
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16);
+      for (int c0 = 0; c0 < rows; c0 += 16) {
+        uint32_t r[16], r2[16];
+        tmem_ld_32x32b_x16(tbase + c0, r);
+        tmem_ld_32x32b_x16(tbase + BN + c0, r2);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          if (c0 + c < rows) out[static_cast<size_t>(c0 + c) * E] = __uint_as_float(r[c]) + __uint_as_float(r2[c]);
+      }
+    }
+  } else {
+    // token rows t0 .. t0 + rows of x, 16-byte cp.async into the 128-byte-swizzled B tile; 8
+    // consecutive threads copy the 8 chunks of one row (thread p: chunk p % 8, rows p / 8 + 16 i)
+    const int p = threadIdx.x - 192;
+    const int ch = p & 7, r0 = p >> 3;
+    int g = 0;
+    bool ok = true;
+    for (int kc = kc0; kc < kc1; ++kc, ++g) {
+      const int slot = g % kStages;
+      const uint32_t use = g / kStages;
+      if (!mbar_wait(&empty[slot], (use & 1u) ^ 1u, abort_flag, err)) {
+        ok = false;
+        break;
+      }
+      const uint32_t sb = smem_u32(smem + slot * kStageBytes + kPieces * kABytes);
+#pragma unroll
+      for (int i = 0; i < BN / 16; ++i) {
+        const int n = r0 + 16 * i;
+        if (n < rows)
+          cp_async_16(sb + n * 128 + ((ch ^ (n & 7)) << 4), x + static_cast<size_t>(t0 + n) * d + kc * BK + ch * 8);
+      }
+      cp_async_commit();
+      if (g >= 1) {
+        cp_async_wait<1>();
+        fence_proxy_async_smem();
+        mbar_arrive(&full[(g - 1) % kStages]);
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    if (ok && g >= 1 && !*abort_flag) mbar_arrive(&full[(g - 1) % kStages]);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 2 * BN);
+  }
+}
+
+}  // namespace rt
+
+// K splits: at least ceil(d / 512) (short accumulation chains), more while the grid is below one
+// CTA per SM, at most one split per 64-wide K chunk.
+int router_tc_splits(int T, int E, int d, int num_sms) {
+  const int tiles = (E / rt::BM) * ((T + rt::BN - 1) / rt::BN);
+  const int nk = d / rt::BK;
+  int s = tiles > 0 ? num_sms / tiles : 1;
+  const int s_min = (nk + 7) / 8;
+  if (s < s_min) s = s_min;
+  if (s > nk) s = nk;
+  if (s < 1) s = 1;
+  return s;
+}
+
+static bool g_rt_attr = false;
+
+cudaError_t launch_router_tc(const CUtensorMap* w3, const uint16_t* x, int T, int E, int d, int nsplit, float* parts,
+                             uint32_t* err, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  if (!g_rt_attr) {
+    cudaError_t e = cudaFuncSetAttribute(rt::router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         rt::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    g_rt_attr = true;
+  }
+  dim3 grid(E / rt::BM, (T + rt::BN - 1) / rt::BN, nsplit);
+  rt::router_tc_kernel<<<grid, 320, rt::kSmemBytes, st>>>(*w3, x, T, E, d, nsplit, parts, err);
+  return cudaGetLastError();
+}
+
+// W_r (fp32 [E][d]) -> three bf16 matrices [3][E][d] with W1 + W2 + W3 == W_r exactly.
+__global__ void split_router_kernel(const float* __restrict__ w, uint16_t* __restrict__ w3, size_t n) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float v = w[i];
+    const uint16_t h1 = f32_to_bf16_bits_rn(v);
+    const float r1 = v - bf16_bits_to_f32(h1);
+    const uint16_t h2 = f32_to_bf16_bits_rn(r1);
+    const float r2 = r1 - bf16_bits_to_f32(h2);
+    w3[i] = h1;
+    w3[n + i] = h2;
+    w3[2 * n + i] = f32_to_bf16_bits_rn(r2);
+  }
+}
+
+cudaError_t launch_split_router(const float* w, uint16_t* w3, size_t n, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  split_router_kernel<<<1024, 256, 0, st>>>(w, w3, n);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
