@@ -127,6 +127,11 @@ MOE_DEVICE void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, in
 MOE_DEVICE void cp_async_16(uint32_t dst_smem, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
 }
+// Same with an L2 cache-eviction policy (e.g. evict_last for activations re-read by many CTAs).
+MOE_DEVICE void cp_async_16_hint(uint32_t dst_smem, const void* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src), "l"(policy)
+               : "memory");
+}
 MOE_DEVICE void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 MOE_DEVICE void cp_async_wait() {

@@ -295,6 +295,7 @@ __global__ void __launch_bounds__(kGateUp ? 320 : 192, 1)
     // lanes); thread p handles chunk p % 8 of rows p / 8 + 16 i, i = 0..7.
     const int p = threadIdx.x - 192;  // 0..127
     const int ch = p & 7, r0 = p >> 3;
+    const uint64_t pol_x = l2_policy_evict_last();  // each x row is gathered once per weight tile
     uint32_t g = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
@@ -320,7 +321,7 @@ __global__ void __launch_bounds__(kGateUp ? 320 : 192, 1)
 #pragma unroll
         for (int i = 0; i < kSegRowsMax / 16; ++i) {
           const int n = r0 + 16 * i;
-          if (src[i]) cp_async_16(sb + n * 128 + ((ch ^ (n & 7)) << 4), src[i] + kk * BK);
+          if (src[i]) cp_async_16_hint(sb + n * 128 + ((ch ^ (n & 7)) << 4), src[i] + kk * BK, pol_x);
         }
         cp_async_commit();
         if (g >= kLag) {

@@ -188,18 +188,31 @@ __global__ void __launch_bounds__(topk_threads<PL>()) topk_kernel(const float* _
   for (int tl = warp; tl < kChunk; tl += blockDim.x / 32) {
     const int t = c * kChunk + tl;
     if (t >= T) break;
+    // all loads of one partial matrix are issued together, then added (split order fixed)
     float v[PL];
 #pragma unroll
     for (int i = 0; i < PL; ++i) {
       const int e = lane + 32 * i;
-      float acc = __int_as_float(0x7fc00000);
-      if (e < E) {
-        acc = parts[static_cast<size_t>(t) * E + e];
-        for (int sp = 1; sp < nsplit; ++sp) acc += parts[(static_cast<size_t>(sp) * T + t) * E + e];
-        if (bias) acc += bias[e];
-        if (logits_out) logits_out[static_cast<size_t>(t) * E + e] = acc;
+      v[i] = e < E ? parts[static_cast<size_t>(t) * E + e] : __int_as_float(0x7fc00000);
+    }
+    for (int sp = 1; sp < nsplit; ++sp) {
+      const float* ps = parts + (static_cast<size_t>(sp) * T + t) * E;
+      float w[PL];
+#pragma unroll
+      for (int i = 0; i < PL; ++i) {
+        const int e = lane + 32 * i;
+        w[i] = e < E ? ps[e] : 0.f;
       }
-      v[i] = acc;
+#pragma unroll
+      for (int i = 0; i < PL; ++i) v[i] += w[i];
+    }
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) {
+        if (bias) v[i] += bias[e];
+        if (logits_out) logits_out[static_cast<size_t>(t) * E + e] = v[i];
+      }
     }
     uint32_t taken = 0u;
     float sel_v = 0.f;  // lane j keeps the value chosen in round j
@@ -374,47 +387,69 @@ MOE_DEVICE void write_segments(Seg* segs, int base, int max_segs, int e, int sta
 
 // Single block of 1024 threads.  Warp w scans experts w, w + 32, ...: 32 consecutive chunk masks
 // of one expert per load (masks are expert-major), popcount, warp prefix sum -> chunk bases.
-// Then thread e scans the expert totals -> offsets, and writes the expert's segments.
+// Loads are issued in batches of kBatch (expert, 32-chunk group) items before any is used, so
+// the warp waits for memory once per batch instead of once per item.  Then thread e scans the
+// expert totals -> offsets, and writes the expert's segments.
 __global__ void __launch_bounds__(1024) group_scan_kernel(const uint32_t* __restrict__ masks, int n_chunks,
                                                           int E, int32_t* __restrict__ chunk_base,
                                                           int32_t* __restrict__ counts,
                                                           int32_t* __restrict__ offsets, Seg* segs,
                                                           int32_t* n_segs, int max_segs, uint32_t* err) {
+  constexpr int kBatch = 16;
   __shared__ int s_total[1024];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int e = warp; e < E; e += 32) {
-    const uint32_t* m = masks + static_cast<size_t>(e) * n_chunks;
-    int32_t* cb = chunk_base + static_cast<size_t>(e) * n_chunks;
-    int run = 0;
-    for (int c0 = 0; c0 < n_chunks; c0 += 32) {
-      const int c = c0 + lane;
-      const int n = c < n_chunks ? __popc(m[c]) : 0;
-      int inc = n;
+  const int groups = (n_chunks + 31) / 32;                 // 32-chunk groups per expert
+  const int my_experts = E > warp ? (E - warp + 31) / 32 : 0;
+  const int items = my_experts * groups;                   // item i: expert warp + 32 (i / groups), group i % groups
+  int run = 0;
+  for (int b0 = 0; b0 < items; b0 += kBatch) {
+    int pc[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = b0 + j;
+      pc[j] = 0;
+      if (i < items) {
+        const int e = warp + 32 * (i / groups);
+        const int c = (i % groups) * 32 + lane;
+        if (c < n_chunks) pc[j] = __popc(masks[static_cast<size_t>(e) * n_chunks + c]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = b0 + j;
+      if (i >= items) break;
+      const int e = warp + 32 * (i / groups);
+      const int g = i % groups;
+      if (g == 0) run = 0;
+      int inc = pc[j];
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int up = __shfl_up_sync(0xffffffffu, inc, o);
         if (lane >= o) inc += up;
       }
-      if (c < n_chunks) cb[c] = run + inc - n;
+      const int c = g * 32 + lane;
+      if (c < n_chunks) chunk_base[static_cast<size_t>(e) * n_chunks + c] = run + inc - pc[j];
       run += __shfl_sync(0xffffffffu, inc, 31);
+      if (g == groups - 1 && lane == 0) s_total[e] = run;
     }
-    if (lane == 0) s_total[e] = run;
   }
+  if (groups == 0)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_total[e] = 0;
   __syncthreads();
   const int e = threadIdx.x;
-  const int run = e < E ? s_total[e] : 0;
+  const int tot_e = e < E ? s_total[e] : 0;
   int total;
-  const int off = block_exclusive_scan(run, &total);
+  const int off = block_exclusive_scan(tot_e, &total);
   if (e < E) {
-    counts[e] = run;
+    counts[e] = tot_e;
     offsets[e] = off;
   }
   if (e == 0) offsets[E] = total;
   if (segs) {
     int seg_total;
-    const int ns = e < E ? num_segments(run) : 0;
+    const int ns = e < E ? num_segments(tot_e) : 0;
     const int sbase = block_exclusive_scan(ns, &seg_total);
-    if (e < E) write_segments(segs, sbase, max_segs, e, off, run, err);
+    if (e < E) write_segments(segs, sbase, max_segs, e, off, tot_e, err);
     if (e == 0) *n_segs = min(seg_total, max_segs);
   }
 }
