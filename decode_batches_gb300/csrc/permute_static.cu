@@ -1,0 +1,67 @@
+// Allocation-free grouping entry point.
+//
+// moe_permute needs scratch memory (per-chunk expert masks and chunk bases), which normally
+// lives in the workspace the caller allocated for a plan.  Some callers cannot allocate device
+// memory at all: engines whose memory planner owns every byte of the device and forbids a
+// component from allocating outside its pool, and code that runs while a stream is being
+// captured into a CUDA graph or on a latency-critical path, where cudaMalloc is either not
+// permitted or would synchronise the device.  moe_permute_static serves them: its scratch is a
+// fixed, file-scope device array that exists as soon as the library is loaded on a device.
+//
+// The array is kStaticWords 32-bit words for the masks plus the same for the chunk bases
+// (2 MiB in all).  Every GPU that loads the library holds it until the process exits.  All calls
+// on a device share it: calls that can overlap on the GPU (different streams without ordering)
+// race on it.  Each call rewrites every scratch word it reads, so nothing needs clearing.
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+constexpr size_t kStaticWords = size_t(1) << 18;  // per array: n_chunks * E <= 262144
+
+static __device__ __align__(256) uint32_t g_static_scratch[2 * kStaticWords];
+
+// Device address of g_static_scratch, looked up once per device with that device current.
+static std::mutex g_static_mu;
+static void* g_static_ptr[64] = {};
+
+static cudaError_t static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return e;
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace moe
+
+extern "C" moe_status moe_permute_static(int E, int k, const int32_t* ids, int T, int32_t* counts, int32_t* offsets,
+                                         int32_t* perm, int32_t* inv_perm, moe_stream_t stream) {
+  using namespace moe;
+  if (E < 1 || E > 1024 || k < 1 || k > 32 || k > E || T < 0) return MOE_ERR_INVALID_ARG;
+  if (!counts || !offsets || !perm || !inv_perm || (T > 0 && !ids)) return MOE_ERR_INVALID_ARG;
+  const size_t n_chunks = (static_cast<size_t>(T) + kChunk - 1) / kChunk;
+  if (n_chunks * static_cast<size_t>(E) > kStaticWords) return MOE_ERR_WORKSPACE;
+  void* base = nullptr;
+  if (static_scratch(&base) != cudaSuccess) return MOE_ERR_CUDA;
+  uint32_t* masks = static_cast<uint32_t*>(base);
+  int32_t* chunk_base = reinterpret_cast<int32_t*>(masks + kStaticWords);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (T > 0 && launch_masks_from_ids(ids, T, E, k, masks, nullptr, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_group_scan(masks, static_cast<int>(n_chunks), E, chunk_base, counts, offsets, nullptr, nullptr, 0,
+                        nullptr, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (T > 0 && launch_scatter(ids, masks, chunk_base, offsets, T, E, k, perm, inv_perm, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}

@@ -173,6 +173,25 @@ moe_status moe_permute(moe_plan* plan, const int32_t* ids, int T, int32_t* count
                        int32_t* offsets, int32_t* perm, int32_t* inv_perm, moe_stream_t stream);
 
 /*
+ * moe_permute without a plan and without any device allocation.  The pages have no counterpart
+ * to this call; it exists for callers that cannot allocate device memory: engines whose memory
+ * planner owns the whole device and forbids components from allocating outside its pool, and
+ * code running during CUDA-graph stream capture or on a latency-critical path, where cudaMalloc
+ * is not permitted or would synchronise the device.  Same inputs and outputs as moe_permute
+ * (ids int32 [T][k] -> counts [E], offsets [E+1], perm and inv_perm [T*k], all device
+ * pointers; invalid or repeated ids are dropped with inv_perm = -1, but there is no error word).
+ * Scratch is a fixed 2 MiB device array inside the library, present on every GPU that loads it
+ * until the process exits; ceil(T / 32) * E must not exceed 262144 (T <= 32768 at E = 256),
+ * else MOE_ERR_WORKSPACE and nothing is enqueued.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  All calls share the array: two calls that may run at the same time on the GPU
+ * (unordered streams) race; calls ordered on one stream do not.  Every scratch word a call
+ * reads is rewritten by that call, so no clearing is needed between calls.
+ */
+moe_status moe_permute_static(int E, int k, const int32_t* ids, int T, int32_t* counts,
+                              int32_t* offsets, int32_t* perm, int32_t* inv_perm, moe_stream_t stream);
+
+/*
  * Expert FFNs on grouped rows (testing entry point for the grouped GEMMs):
  *   y[r] = FFN_e(x[perm[r] / k]) for r in [offsets[e], offsets[e+1]),  fp16 [T*k][d_model],
  *   shared_y[t] = sum_s FFN_shared_s(x[t]) fp16 [T][d_model] (may be NULL if n_shared == 0).
