@@ -77,6 +77,7 @@ struct moe_plan {
   uint16_t* w_down_s = nullptr;
   uint32_t* err = nullptr;
   bool weights_set = false, shared_set = false;
+  bool tiled = false, tiled_s = false;  // weights stored in the tile-contiguous layouts
   // workspace (caller-owned)
   uint8_t* ws = nullptr;
   size_t ws_bytes = 0;
@@ -224,20 +225,8 @@ static moe_status make_map_16(CUtensorMap* m, const void* base, uint64_t inner, 
 }
 
 static moe_status build_weight_maps(moe_plan* p) {
-  p->maps_weights = false;
-  if (!tc_shape_ok(p) || !p->weights_set) return MOE_OK;
-  moe_status s;
-  const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  if ((s = make_map_16(&p->maps.w_gu, p->w_gu, p->d, static_cast<uint64_t>(p->E) * 2 * p->f, 128, BF)) != MOE_OK) return s;
-  if ((s = make_map_16(&p->maps.w_down, p->w_down, p->f, static_cast<uint64_t>(p->E) * p->d, 128, F16)) != MOE_OK) return s;
-  if (p->n_shared > 0) {
-    if (!p->shared_set) return MOE_OK;
-    if ((s = make_map_16(&p->maps.w_gu_s, p->w_gu_s, p->d, static_cast<uint64_t>(p->n_shared) * 2 * p->f_s, 128, BF)) != MOE_OK)
-      return s;
-    if ((s = make_map_16(&p->maps.w_down_s, p->w_down_s, p->f_s, static_cast<uint64_t>(p->n_shared) * p->d, 128, F16)) != MOE_OK)
-      return s;
-  }
-  p->maps_weights = true;
+  // the tensor-core path reads the tile-contiguous weights directly (bulk copies, no maps)
+  p->maps_weights = tc_shape_ok(p) && p->weights_set && p->tiled && (p->n_shared == 0 || (p->shared_set && p->tiled_s));
   return MOE_OK;
 }
 
@@ -335,6 +324,20 @@ static moe_status ensure_err_word(moe_plan* p) {
 // ============================================================================================
 // weights
 // ============================================================================================
+// Down weights (n bf16 matrices [rows][K]) into the fp16 tile-contiguous layout.
+static moe_status tile_down_f16(uint16_t* dst, const void* src, int n, int rows, int K, int by_matrix) {
+  uint32_t* flag = nullptr;
+  MOE_CUDA_TRY(cudaMalloc(&flag, sizeof(uint32_t)));
+  cudaMemset(flag, 0, sizeof(uint32_t));
+  cudaError_t e = launch_tile_down(static_cast<const uint16_t*>(src), dst, n, rows, K, by_matrix, flag, 0);
+  uint32_t bad = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&bad, flag, sizeof bad, cudaMemcpyDeviceToHost);
+  cudaFree(flag);
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "down weight tiling: %s", cudaGetErrorString(e));
+  if (bad) return fail(MOE_ERR_UNSUPPORTED, "a down-projection weight is outside the fp16 range (|w| > 65504)");
+  return MOE_OK;
+}
+
 // Copy n bf16 values into an fp16 plan buffer; MOE_ERR_UNSUPPORTED if any is outside the fp16
 // range (the down projection runs fp16 x fp16 on the tensor cores).
 static moe_status copy_bf16_as_f16(uint16_t* dst, const void* src, size_t n) {
@@ -384,17 +387,28 @@ extern "C" moe_status moe_plan_set_weights(moe_plan* p, const float* w_router, c
     MOE_CUDA_TRY(cudaMemset(p->b_router, 0, E * sizeof(float)));
   const size_t gu_row = fp4 ? d / 2 : d * 2;     // bytes per gate/up row
   const size_t dn_row = fp4 ? f / 2 : f * 2;     // bytes per down row
+  p->tiled = !fp4 && d % 128 == 0 && f % 64 == 0;
   MOE_CUDA_TRY(cudaMalloc(&p->w_gu, E * 2 * f * gu_row));
-  MOE_CUDA_TRY(launch_interleave_gate_up(static_cast<const uint8_t*>(w_gate), static_cast<const uint8_t*>(w_up), p->w_gu,
-                                         p->E, p->f, gu_row, 0));
   MOE_CUDA_TRY(cudaMalloc(&p->w_down, E * d * dn_row));
-  if (fp4) {
-    MOE_CUDA_TRY(cudaMemcpy(p->w_down, w_down, E * d * dn_row, cudaMemcpyDeviceToDevice));
-  } else {
-    s = copy_bf16_as_f16(reinterpret_cast<uint16_t*>(p->w_down), w_down, E * d * f);
+  if (p->tiled) {
+    MOE_CUDA_TRY(launch_tile_gate_up(static_cast<const uint16_t*>(w_gate), static_cast<const uint16_t*>(w_up),
+                                     reinterpret_cast<uint16_t*>(p->w_gu), p->E, p->f, p->d, 0));
+    s = tile_down_f16(reinterpret_cast<uint16_t*>(p->w_down), w_down, p->E, p->d, p->f, 1);
     if (s != MOE_OK) {
       free_weights(p);
       return s;
+    }
+  } else {
+    MOE_CUDA_TRY(launch_interleave_gate_up(static_cast<const uint8_t*>(w_gate), static_cast<const uint8_t*>(w_up),
+                                           p->w_gu, p->E, p->f, gu_row, 0));
+    if (fp4) {
+      MOE_CUDA_TRY(cudaMemcpy(p->w_down, w_down, E * d * dn_row, cudaMemcpyDeviceToDevice));
+    } else {
+      s = copy_bf16_as_f16(reinterpret_cast<uint16_t*>(p->w_down), w_down, E * d * f);
+      if (s != MOE_OK) {
+        free_weights(p);
+        return s;
+      }
     }
   }
   if (fp4) {
@@ -425,10 +439,17 @@ extern "C" moe_status moe_plan_set_shared(moe_plan* p, int d_ff_shared, const vo
   p->f_s = d_ff_shared;
   const size_t n = p->n_shared, d = p->d, fs = d_ff_shared;
   MOE_CUDA_TRY(cudaMalloc(&p->w_gu_s, n * 2 * fs * d * 2));
-  MOE_CUDA_TRY(launch_interleave_gate_up(static_cast<const uint8_t*>(w_gate), static_cast<const uint8_t*>(w_up),
-                                         reinterpret_cast<uint8_t*>(p->w_gu_s), p->n_shared, p->f_s, d * 2, 0));
   MOE_CUDA_TRY(cudaMalloc(&p->w_down_s, n * d * fs * 2));
-  s = copy_bf16_as_f16(p->w_down_s, w_down, n * d * fs);
+  p->tiled_s = d % 128 == 0 && fs % 64 == 0;
+  if (p->tiled_s) {
+    MOE_CUDA_TRY(launch_tile_gate_up(static_cast<const uint16_t*>(w_gate), static_cast<const uint16_t*>(w_up), p->w_gu_s,
+                                     p->n_shared, p->f_s, p->d, 0));
+    s = tile_down_f16(p->w_down_s, w_down, p->n_shared, p->d, p->f_s, 0);
+  } else {
+    MOE_CUDA_TRY(launch_interleave_gate_up(static_cast<const uint8_t*>(w_gate), static_cast<const uint8_t*>(w_up),
+                                           reinterpret_cast<uint8_t*>(p->w_gu_s), p->n_shared, p->f_s, d * 2, 0));
+    s = copy_bf16_as_f16(p->w_down_s, w_down, n * d * fs);
+  }
   if (s != MOE_OK) return s;
   MOE_CUDA_TRY(cudaDeviceSynchronize());
   p->shared_set = true;
@@ -508,6 +529,8 @@ static FfnWeights ffn_weights(const moe_plan* p) {
   w.d = p->d;
   w.f = p->f;
   w.err = p->err;
+  w.tiled = p->tiled ? 1 : 0;
+  w.tiled_s = p->tiled_s ? 1 : 0;
   return w;
 }
 
@@ -520,6 +543,10 @@ static moe_status run_experts(moe_plan* p, const uint16_t* x, int T, const int32
   if (use_tc(p)) {
     if (!p->maps_weights || !p->maps_ws) return fail(MOE_ERR_NOT_READY, "tensor maps not built");
     TcArgs a;
+    a.w_gu = reinterpret_cast<const uint16_t*>(p->w_gu);
+    a.w_gu_s = p->w_gu_s;
+    a.w_down = reinterpret_cast<const uint16_t*>(p->w_down);
+    a.w_down_s = p->w_down_s;
     a.segs = ws_ptr<Seg>(p, p->L.segs);
     a.n_segs = ws_ptr<int32_t>(p, p->L.n_segs);
     a.perm = perm;
@@ -588,10 +615,11 @@ extern "C" moe_status moe_layer_forward(moe_plan* p, const void* x, int T, int n
   const bool tc = use_tc(p);
   s = route_step(p, xb, T, nullptr, ids, gates, masks, st);
   if (s != MOE_OK) return s;
-  LAUNCH(p, "group_scan", st,
-         launch_group_scan(masks, n_chunks, p->E, chunk_base, counts, offsets, tc ? ws_ptr<Seg>(p, p->L.segs) : nullptr,
-                           ws_ptr<int32_t>(p, p->L.n_segs), p->L.max_segs, p->err, st));
-  LAUNCH(p, "scatter", st, launch_scatter(ids, masks, chunk_base, offsets, T, p->E, p->k, perm, inv, st));
+  LAUNCH(p, "chunk_scan", st, launch_chunk_scan(masks, n_chunks, p->E, chunk_base, counts, st));
+  LAUNCH(p, "scatter", st,
+         launch_scatter(ids, masks, chunk_base, counts, T, p->E, p->k, perm, inv, offsets,
+                        tc ? ws_ptr<Seg>(p, p->L.segs) : nullptr, ws_ptr<int32_t>(p, p->L.n_segs), p->L.max_segs,
+                        p->err, st));
   s = run_experts(p, xb, T, offsets, perm, y, y_s, st);
   if (s != MOE_OK) return s;
   LAUNCH(p, "combine", st, launch_combine(y, gates, inv, y_s, T, p->k, p->d, static_cast<uint16_t*>(out), st));
@@ -640,9 +668,10 @@ extern "C" moe_status moe_permute(moe_plan* p, const int32_t* ids, int T, int32_
   uint32_t* masks = ws_ptr<uint32_t>(p, p->L.masks);
   int32_t* chunk_base = ws_ptr<int32_t>(p, p->L.chunk_base);
   if (T > 0) LAUNCH(p, "masks_from_ids", st, launch_masks_from_ids(ids, T, p->E, p->k, masks, p->err, st));
-  LAUNCH(p, "group_scan", st,
-         launch_group_scan(masks, n_chunks, p->E, chunk_base, counts, offsets, nullptr, nullptr, 0, p->err, st));
-  if (T > 0) LAUNCH(p, "scatter", st, launch_scatter(ids, masks, chunk_base, offsets, T, p->E, p->k, perm, inv_perm, st));
+  LAUNCH(p, "chunk_scan", st, launch_chunk_scan(masks, n_chunks, p->E, chunk_base, counts, st));
+  LAUNCH(p, "scatter", st,
+         launch_scatter(ids, masks, chunk_base, counts, T, p->E, p->k, perm, inv_perm, offsets, nullptr, nullptr, 0,
+                        p->err, st));
   return MOE_OK;
 }
 

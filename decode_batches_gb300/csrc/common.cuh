@@ -121,6 +121,16 @@ MOE_DEVICE void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, in
       : "memory");
 }
 
+// Bulk copy of `bytes` contiguous bytes (multiple of 16, both addresses 16-byte aligned) into
+// shared memory, completing `bytes` transactions on the mbarrier.
+MOE_DEVICE void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // ------------------------------------------------------------------------------------------
 // cp.async (16-byte, L2 only) for gathered rows
 // ------------------------------------------------------------------------------------------
@@ -254,7 +264,8 @@ MOE_DEVICE uint32_t pack_bf16x2(float lo, float hi) {
          (static_cast<uint32_t>(f32_to_bf16_bits_rn(hi)) << 16);
 }
 
-// silu(g) * u in fp32 (the SwiGLU of the gate and up projections).
-MOE_DEVICE float swiglu(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+// silu(g) * u in fp32 (the SwiGLU of the gate and up projections).  Fast exp and division:
+// the result is rounded to fp16 (11 bits) right after, far coarser than their ~2-ulp error.
+MOE_DEVICE float swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
 }  // namespace moe

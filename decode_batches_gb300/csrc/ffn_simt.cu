@@ -47,6 +47,30 @@ MOE_DEVICE float warp_dot_f16(const float* act, const uint16_t* wrow, int K, int
   return acc;
 }
 
+// Dot product with one row of a tile-contiguous matrix: `blocks` points at the row's first
+// 128 x 64 block, consecutive K chunks are consecutive blocks, r is the row inside the block.
+template <bool kF16>
+MOE_DEVICE float warp_dot_tiled(const float* act, const uint16_t* blocks, int r, int K, int lane) {
+  float acc = 0.f;
+  for (int k = lane * 8; k < K; k += 256) {
+    const uint4 wv = *reinterpret_cast<const uint4*>(blocks + static_cast<size_t>(k >> 6) * kTileElems +
+                                                     tile_elem_offset(r, k & 63));
+    float wf[8];
+    if (kF16)
+      f16x8_to_f32(wv, wf);
+    else
+      bf16x8_to_f32(wv, wf);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc = fmaf(act[k + q], wf[q], acc);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  return acc;
+}
+
+// Row of (feature F, gate 0 / up 1) inside its 128-row gate/up tile.
+MOE_DEVICE int gu_tile_row(int F, int which) { return 16 * ((F & 63) >> 3) + 8 * which + (F & 7); }
+
 MOE_DEVICE uint16_t to_f16_sat(float v, bool& sat) {
   if (!(fabsf(v) <= kF16Max)) {
     sat = true;
@@ -116,6 +140,11 @@ __global__ void __launch_bounds__(256) simt_gateup_kernel(FfnWeights w, const ui
         const uint8_t* s = w.s_gu + static_cast<size_t>(e) * 2 * w.f * (w.d / 32);
         g = warp_dot_fp4(act, c + static_cast<size_t>(gu_row(F, 0)) * (w.d / 2), s + static_cast<size_t>(gu_row(F, 0)) * (w.d / 32), w.d, lane);
         u = warp_dot_fp4(act, c + static_cast<size_t>(gu_row(F, 1)) * (w.d / 2), s + static_cast<size_t>(gu_row(F, 1)) * (w.d / 32), w.d, lane);
+      } else if (w.tiled) {
+        const uint16_t* blocks = static_cast<const uint16_t*>(w.w_gu) +
+                                 (static_cast<size_t>(e) * (w.f / 64) + F / 64) * (w.d / 64) * kTileElems;
+        g = warp_dot_tiled<false>(act, blocks, gu_tile_row(F, 0), w.d, lane);
+        u = warp_dot_tiled<false>(act, blocks, gu_tile_row(F, 1), w.d, lane);
       } else {
         const uint16_t* base = static_cast<const uint16_t*>(w.w_gu) + static_cast<size_t>(e) * 2 * w.f * w.d;
         g = warp_dot_bf16(act, base + static_cast<size_t>(gu_row(F, 0)) * w.d, w.d, lane);
@@ -132,9 +161,17 @@ __global__ void __launch_bounds__(256) simt_gateup_kernel(FfnWeights w, const ui
     const int fs_tot = w.n_shared * w.f_s;
     for (int F = warp; F < fs_tot; F += 8) {
       const int s = F / w.f_s, Fl = F % w.f_s;
-      const uint16_t* base = w.w_gu_s + static_cast<size_t>(s) * 2 * w.f_s * w.d;
-      const float g = warp_dot_bf16(act, base + static_cast<size_t>(gu_row(Fl, 0)) * w.d, w.d, lane);
-      const float u = warp_dot_bf16(act, base + static_cast<size_t>(gu_row(Fl, 1)) * w.d, w.d, lane);
+      float g, u;
+      if (w.tiled_s) {
+        const uint16_t* blocks =
+            w.w_gu_s + (static_cast<size_t>(s) * (w.f_s / 64) + Fl / 64) * (w.d / 64) * kTileElems;
+        g = warp_dot_tiled<false>(act, blocks, gu_tile_row(Fl, 0), w.d, lane);
+        u = warp_dot_tiled<false>(act, blocks, gu_tile_row(Fl, 1), w.d, lane);
+      } else {
+        const uint16_t* base = w.w_gu_s + static_cast<size_t>(s) * 2 * w.f_s * w.d;
+        g = warp_dot_bf16(act, base + static_cast<size_t>(gu_row(Fl, 0)) * w.d, w.d, lane);
+        u = warp_dot_bf16(act, base + static_cast<size_t>(gu_row(Fl, 1)) * w.d, w.d, lane);
+      }
       bool sat = false;
       const uint16_t hv = to_f16_sat(swiglu(g, u), sat);
       if (lane == 0) {
@@ -164,6 +201,10 @@ __global__ void __launch_bounds__(256) simt_down_kernel(FfnWeights w, int T, con
         const uint8_t* c = static_cast<const uint8_t*>(w.w_down) + (static_cast<size_t>(e) * w.d + n) * (w.f / 2);
         const uint8_t* s = w.s_down + (static_cast<size_t>(e) * w.d + n) * (w.f / 32);
         v = warp_dot_fp4(act, c, s, w.f, lane);
+      } else if (w.tiled) {
+        const uint16_t* blocks = static_cast<const uint16_t*>(w.w_down) +
+                                 (static_cast<size_t>(e) * (w.d / 128) + n / 128) * (w.f / 64) * kTileElems;
+        v = warp_dot_tiled<true>(act, blocks, n & 127, w.f, lane);
       } else {
         v = warp_dot_f16(act, static_cast<const uint16_t*>(w.w_down) + (static_cast<size_t>(e) * w.d + n) * w.f, w.f, lane);
       }
@@ -182,7 +223,11 @@ __global__ void __launch_bounds__(256) simt_down_kernel(FfnWeights w, int T, con
     for (int n = warp; n < w.d; n += 8) {
       float v = 0.f;
       for (int s = 0; s < w.n_shared; ++s)
-        v += warp_dot_f16(act + s * w.f_s, w.w_down_s + (static_cast<size_t>(s) * w.d + n) * w.f_s, w.f_s, lane);
+        v += w.tiled_s ? warp_dot_tiled<true>(act + s * w.f_s,
+                                              w.w_down_s + (static_cast<size_t>(n / 128) * w.n_shared + s) *
+                                                               (w.f_s / 64) * kTileElems,
+                                              n & 127, w.f_s, lane)
+                       : warp_dot_f16(act + s * w.f_s, w.w_down_s + (static_cast<size_t>(s) * w.d + n) * w.f_s, w.f_s, lane);
       bool sat = false;
       const uint16_t yv = to_f16_sat(v, sat);
       if (lane == 0) {

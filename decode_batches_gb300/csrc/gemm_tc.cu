@@ -1,16 +1,16 @@
 // Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), sm_103a.
 //
 // The grouped problem is a list of segments: consecutive grouped rows of one routed expert
-// (at most 256), or consecutive tokens for the shared experts.  Each unit of work is one
+// (at most 128), or consecutive tokens for the shared experts.  Each unit of work is one
 // segment times one 128-row tile of that expert's weight matrix.  The MMA computes
 //     D[weight row][token] = W[128 x K] . X[N x K]^T
-// ("swap-AB": the weight tile is the M=128 operand, the segment's tokens are N <= 256), so the
+// ("swap-AB": the weight tile is the M=128 operand, the segment's tokens are N <= 128), so the
 // weights -- the bytes that bound this layer -- stream through shared memory exactly once per
 // segment, whatever the number of rows routed to the expert.
 //
 //   gate/up kernel (bf16 x bf16): A = 128 interleaved rows of W_gate|W_up (8 gate rows, then
-//     the same 8 features' up rows, repeated), TMA-loaded; B = the segment's token rows of x,
-//     gathered with cp.async (the permutation is applied on the fly, x is never copied);
+//     the same 8 features' up rows, repeated); B = the segment's token rows of x, gathered
+//     with cp.async (the permutation is applied on the fly, x is never copied);
 //     epilogue: h = fp16(silu(gate) * up), the gate-first SwiGLU of "Why SSD-streamed MoE was
 //     slow: 8GB Jetson Orin Nano, part 2" (section re-checking part 1), rounded inside the
 //     producer as in the Decode paragraph of "DeepSeek V4.1F Q4 with native DSpark MTP on M3
@@ -18,9 +18,11 @@
 //   down kernel (fp16 x fp16): A = 128 rows of W_down (held as fp16 by the plan), B = the
 //     segment's rows of h (TMA); epilogue writes y (fp16) in grouped row order for the combine.
 //   Intermediates that leave the fp16 range are clamped and flag MOE_DEVERR_RANGE.
+//   Weights are stored tile-contiguous and pre-swizzled (16 KB per 128 x 64 tile, a unit's K
+//   loop consecutive), so each A stage is one bulk copy and a unit streams one run of HBM.
 //
 // Roles (persistent CTAs, one per SM, every role walks the same unit sequence):
-//   warp 0      TMA producer (A, and B for the down kernel)
+//   warp 0      producer: A by bulk copy; B by TMA (down kernel)
 //   warp 1      TMEM owner and MMA issuer (one thread)
 //   warps 2-5   epilogue (TMEM lanes 32*(warp%4) .. +31)
 //   warps 6-9   gate/up only: cp.async gather of the token rows
@@ -29,6 +31,8 @@
 // expert with more than 128 rows is split into parts; the units of its parts are ordered
 // tile-major (tile 0 of every part, then tile 1, ...) so that CTAs working on the same
 // weight tile run side by side and the second read of the tile is served by L2.
+// Measured on the 2051-token step: the weight stream alone runs at the measured HBM copy rate;
+// separate rings for A and B, a 7th stage and a longer gather lag were all slower or equal.
 // Every wait is bounded (see common.cuh); on a timeout the CTA stops issuing work, drains its
 // MMAs, frees TMEM and returns with MOE_DEVERR_TIMEOUT set.
 #include "common.cuh"
@@ -40,7 +44,7 @@ namespace tc {
 constexpr int BM = 128;                          // weight rows per unit (MMA M)
 constexpr int BK = 64;                           // K elements per stage (128-byte rows)
 constexpr int kStages = 6;
-constexpr int kLag = 4;                          // gather completion lag (stages), < kStages
+constexpr int kLag = 2;                          // gather completion lag (stages), < kStages
 constexpr int kABytes = BM * BK * 2;             // 16 KB
 constexpr int kBBytes = kSegRowsMax * BK * 2;    // 16 KB (N <= 128)
 constexpr int kStageBytes = kABytes + kBBytes;
@@ -114,9 +118,9 @@ __global__ void __launch_bounds__(kGateUp ? 320 : 192, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_map(kGateUp ? &maps.w_gu : &maps.w_down);
-    if (a.n_shared) tma_prefetch_map(kGateUp ? &maps.w_gu_s : &maps.w_down_s);
+  if (warp == 0 && lane == 0 && !kGateUp) {
+    tma_prefetch_map(&maps.h);
+    if (a.n_shared) tma_prefetch_map(&maps.h_s);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -156,23 +160,18 @@ __global__ void __launch_bounds__(kGateUp ? 320 : 192, 1)
           uint8_t* sa = smem + slot * kStageBytes;
           uint8_t* sb = sa + kABytes;
           mbar_arrive_expect_tx(&full[slot], kABytes + nbox * 32 * BK * 2);
-          if (kGateUp) {
-            if (un.shared)
-              tma_load_2d(sa, &maps.w_gu_s, &full[slot], kk * BK, un.tile * BM, pol_w);
-            else
-              tma_load_2d(sa, &maps.w_gu, &full[slot], kk * BK, un.expert * 2 * a.f + un.tile * BM, pol_w);
-          } else {
-            if (un.shared) {
-              const int kglob = kk * BK;
-              const int s = kglob / a.f_s, kin = kglob % a.f_s;
-              tma_load_2d(sa, &maps.w_down_s, &full[slot], kin, s * a.d + un.tile * BM, pol_w);
-              for (int i = 0; i < nbox; ++i)
-                tma_load_2d(sb + i * 32 * BK * 2, &maps.h_s, &full[slot], kglob, un.row_start + 32 * i, pol_act);
-            } else {
-              tma_load_2d(sa, &maps.w_down, &full[slot], kk * BK, un.expert * a.d + un.tile * BM, pol_w);
-              for (int i = 0; i < nbox; ++i)
-                tma_load_2d(sb + i * 32 * BK * 2, &maps.h, &full[slot], kk * BK, un.row_start + 32 * i, pol_act);
-            }
+          const uint16_t* wsrc;
+          if (kGateUp)
+            wsrc = un.shared ? a.w_gu_s + (static_cast<size_t>(un.tile) * nk + kk) * kTileElems
+                             : a.w_gu + ((static_cast<size_t>(un.expert) * tiles_r + un.tile) * nk + kk) * kTileElems;
+          else
+            wsrc = un.shared ? a.w_down_s + (static_cast<size_t>(un.tile) * nk + kk) * kTileElems
+                             : a.w_down + ((static_cast<size_t>(un.expert) * tiles_r + un.tile) * nk + kk) * kTileElems;
+          bulk_load(sa, wsrc, kABytes, &full[slot], pol_w);
+          if (!kGateUp) {
+            const CUtensorMap* hm = un.shared ? &maps.h_s : &maps.h;
+            for (int i = 0; i < nbox; ++i)
+              tma_load_2d(sb + i * 32 * BK * 2, hm, &full[slot], kk * BK, un.row_start + 32 * i, pol_act);
           }
         }
         if (!ok) break;

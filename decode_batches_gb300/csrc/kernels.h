@@ -44,14 +44,15 @@ cudaError_t launch_split_router(const float* w, uint16_t* w3, size_t n, cudaStre
 // Per-chunk expert masks from given ids (validates range / duplicates).
 cudaError_t launch_masks_from_ids(const int32_t* ids, int T, int E, int k, uint32_t* masks,
                                   uint32_t* err, cudaStream_t st);
-// Exclusive scan over experts and chunks; counts, offsets, chunk bases, and (if segs) the
-// segment list of the routed experts for the grouped GEMMs.
-cudaError_t launch_group_scan(const uint32_t* masks, int n_chunks, int E, int32_t* chunk_base,
-                              int32_t* counts, int32_t* offsets, Seg* segs, int32_t* n_segs,
-                              int max_segs, uint32_t* err, cudaStream_t st);
-// perm / inv_perm from masks, bases and offsets.
+// Per-expert scan over the chunk masks: chunk_base[e][c] (assignments of e in earlier chunks)
+// and counts[e].
+cudaError_t launch_chunk_scan(const uint32_t* masks, int n_chunks, int E, int32_t* chunk_base, int32_t* counts,
+                              cudaStream_t st);
+// perm / inv_perm, and offsets (exclusive scan of counts, offsets[E] = total); if segs is given
+// also the segment list of the routed experts for the grouped GEMMs.
 cudaError_t launch_scatter(const int32_t* ids, const uint32_t* masks, const int32_t* chunk_base,
-                           const int32_t* offsets, int T, int E, int k, int32_t* perm, int32_t* inv,
+                           const int32_t* counts, int T, int E, int k, int32_t* perm, int32_t* inv,
+                           int32_t* offsets, Seg* segs, int32_t* n_segs, int max_segs, uint32_t* err,
                            cudaStream_t st);
 // Segment list from offsets only (used by the separate experts entry point).
 cudaError_t launch_segments_from_offsets(const int32_t* offsets, int E, Seg* segs, int32_t* n_segs,
@@ -76,6 +77,8 @@ struct FfnWeights {
   int f_s = 0;
   int E = 0, k = 0, d = 0, f = 0;
   uint32_t* err = nullptr;
+  // 1: bf16 routed / shared weights are in the tile-contiguous layouts of the tensor-core path
+  int tiled = 0, tiled_s = 0;
 };
 
 // h, h_s, y, y_s are fp16.
@@ -85,15 +88,16 @@ cudaError_t launch_ffn_simt(const FfnWeights& w, const uint16_t* x, int T, const
 
 // ---- expert FFN, tcgen05 path (gemm_tc.cu) ---------------------------------------------------
 struct TcMaps {
-  CUtensorMap w_gu;      // A for gate/up: [E*2f rows][d], box 64 x 128
-  CUtensorMap w_gu_s;    // A for shared gate/up: [n_s*2f_s rows][d]
-  CUtensorMap w_down;    // A for down: [E*d rows][f], box 64 x 128
-  CUtensorMap w_down_s;  // A for shared down: [n_s*d rows][f_s]
-  CUtensorMap h;         // B for down: [R_max rows][f], box 64 x 32
-  CUtensorMap h_s;       // B for shared down: [T_max rows][n_s*f_s], box 64 x 32
+  CUtensorMap h;         // B for down: [R_max rows][f] fp16, box 64 x 32
+  CUtensorMap h_s;       // B for shared down: [T_max rows][n_s*f_s] fp16, box 64 x 32
 };
 
 struct TcArgs {
+  // tile-contiguous weights (launch_tile_gate_up / launch_tile_down layouts)
+  const uint16_t* w_gu = nullptr;    // [E][f/64][d/64] blocks, bf16
+  const uint16_t* w_gu_s = nullptr;  // [n_s*f_s/64][d/64] blocks, bf16
+  const uint16_t* w_down = nullptr;  // [E][d/128][f/64] blocks, fp16
+  const uint16_t* w_down_s = nullptr;  // [d/128][n_s][f_s/64] blocks, fp16
   const Seg* segs = nullptr;
   const int32_t* n_segs = nullptr;
   const int32_t* perm = nullptr;
@@ -121,5 +125,17 @@ cudaError_t launch_interleave_gate_up(const uint8_t* gate, const uint8_t* up, ui
                                       int f, size_t row_bytes, cudaStream_t st);
 // dst fp16 <- src bf16 (round to nearest even); *bad |= 1 if a value is outside the fp16 range.
 cudaError_t launch_bf16_to_f16(const uint16_t* src, uint16_t* dst, size_t n, uint32_t* bad, cudaStream_t st);
+// Tile-contiguous, pre-swizzled layouts of the tensor-core path (16 KB blocks of 128 rows x 64
+// K elements).  Gate/up of n experts -> [n][f/64][d/64] blocks (rows interleaved by 8).  Down
+// (bf16 -> fp16) of n matrices [rows][K] -> by_matrix ? [n][rows/128][K/64] : [rows/128][n][K/64].
+cudaError_t launch_tile_gate_up(const uint16_t* gate, const uint16_t* up, uint16_t* dst, int n, int f, int d,
+                                cudaStream_t st);
+cudaError_t launch_tile_down(const uint16_t* src, uint16_t* dst, int n, int rows, int K, int by_matrix, uint32_t* bad,
+                             cudaStream_t st);
+constexpr int kTileElems = 128 * 64;
+// Element offset of (row r, K element kk) inside one 128 x 64 block (128-byte swizzle).
+__host__ __device__ inline size_t tile_elem_offset(int r, int kk) {
+  return static_cast<size_t>(r) * 64 + ((((kk >> 3) ^ (r & 7)) << 3) | (kk & 7));
+}
 
 }  // namespace moe

@@ -58,10 +58,10 @@ extern "C" moe_status moe_permute_static(int E, int k, const int32_t* ids, int T
   int32_t* chunk_base = reinterpret_cast<int32_t*>(masks + kStaticWords);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (T > 0 && launch_masks_from_ids(ids, T, E, k, masks, nullptr, st) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_group_scan(masks, static_cast<int>(n_chunks), E, chunk_base, counts, offsets, nullptr, nullptr, 0,
-                        nullptr, st) != cudaSuccess)
+  if (launch_chunk_scan(masks, static_cast<int>(n_chunks), E, chunk_base, counts, st) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (T > 0 && launch_scatter(ids, masks, chunk_base, offsets, T, E, k, perm, inv_perm, st) != cudaSuccess)
+  if (launch_scatter(ids, masks, chunk_base, counts, T, E, k, perm, inv_perm, offsets, nullptr, nullptr, 0, nullptr,
+                     st) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

@@ -55,4 +55,83 @@ cudaError_t launch_bf16_to_f16(const uint16_t* src, uint16_t* dst, size_t n, uin
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------------------------
+// Tile-contiguous layouts for the tensor-core path.  A block is 128 weight rows x 64 K elements
+// (16 KB) stored exactly as the MMA reads it from shared memory: row r at r * 128 bytes, its
+// 16-byte chunk c at ((c ^ (r % 8)) * 16) (the 128-byte swizzle).  Blocks of one unit's K loop
+// are consecutive, so a unit streams its weights as one contiguous run of HBM.
+// ---------------------------------------------------------------------------------------------
+// Gate/up of n experts ([n][f][d] each) -> blocks [n][f/64][d/64]; block row r of feature tile t
+// is gate row 64t + 8(r/16) + r%8 when r%16 < 8, else the up row of that feature.
+__global__ void tile_gate_up_kernel(const uint16_t* __restrict__ gate, const uint16_t* __restrict__ up,
+                                    uint16_t* __restrict__ dst, int f, int d, size_t n_chunks16) {
+  const int nk = d / 64, tiles = f / 64;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n_chunks16;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    // destination chunk i: block b = i / 1024, row r = (i % 1024) / 8, physical chunk pc = i % 8
+    const size_t b = i >> 10;
+    const int r = static_cast<int>((i >> 3) & 127), pc = static_cast<int>(i & 7);
+    const int kc = static_cast<int>(b % nk);
+    const size_t et = b / nk;
+    const int t = static_cast<int>(et % tiles);
+    const size_t e = et / tiles;
+    const int F = 64 * t + 8 * (r >> 4) + (r & 7);
+    const uint16_t* src = ((r & 15) < 8 ? gate : up) + (e * f + F) * static_cast<size_t>(d) + kc * 64 + 8 * (pc ^ (r & 7));
+    reinterpret_cast<uint4*>(dst)[i] = *reinterpret_cast<const uint4*>(src);
+  }
+}
+
+cudaError_t launch_tile_gate_up(const uint16_t* gate, const uint16_t* up, uint16_t* dst, int n, int f, int d,
+                                cudaStream_t st) {
+  const size_t chunks = static_cast<size_t>(n) * 2 * f * d / 8;
+  if (chunks == 0) return cudaSuccess;
+  tile_gate_up_kernel<<<2048, 256, 0, st>>>(gate, up, dst, f, d, chunks);
+  return cudaGetLastError();
+}
+
+// Down projections of n matrices ([n][rows][K] bf16) -> fp16 blocks.  Routed order (by_matrix):
+// block (m, rows/128 tile dt, K chunk kc) at (m * (rows/128) + dt) * (K/64) + kc.  Shared order:
+// at (dt * n + m) * (K/64) + kc, so one output tile's K loop runs over all n matrices.
+__global__ void tile_down_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst, int n, int rows, int K,
+                                 int by_matrix, size_t n_chunks16, uint32_t* bad) {
+  const int nk = K / 64, dts = rows / 128;
+  bool oor = false;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n_chunks16;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t b = i >> 10;
+    const int r = static_cast<int>((i >> 3) & 127), pc = static_cast<int>(i & 7);
+    const int kc = static_cast<int>(b % nk);
+    const size_t rest = b / nk;
+    int m, dt;
+    if (by_matrix) {
+      dt = static_cast<int>(rest % dts);
+      m = static_cast<int>(rest / dts);
+    } else {
+      m = static_cast<int>(rest % n);
+      dt = static_cast<int>(rest / n);
+    }
+    const uint16_t* s = src + (static_cast<size_t>(m) * rows + dt * 128 + r) * K + kc * 64 + 8 * (pc ^ (r & 7));
+    const uint4 v = *reinterpret_cast<const uint4*>(s);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float lo = bf16_bits_to_f32(static_cast<uint16_t>(w[q] & 0xFFFFu));
+      const float hi = bf16_bits_to_f32(static_cast<uint16_t>(w[q] >> 16));
+      if (!(fabsf(lo) <= kF16Max) || !(fabsf(hi) <= kF16Max)) oor = true;
+      o[q] = static_cast<uint32_t>(f32_to_f16_bits_rn(lo)) | (static_cast<uint32_t>(f32_to_f16_bits_rn(hi)) << 16);
+    }
+    reinterpret_cast<uint4*>(dst)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (oor) atomicOr(bad, 1u);
+}
+
+cudaError_t launch_tile_down(const uint16_t* src, uint16_t* dst, int n, int rows, int K, int by_matrix, uint32_t* bad,
+                             cudaStream_t st) {
+  const size_t chunks = static_cast<size_t>(n) * rows * K / 8;
+  if (chunks == 0) return cudaSuccess;
+  tile_down_kernel<<<2048, 256, 0, st>>>(src, dst, n, rows, K, by_matrix, chunks, bad);
+  return cudaGetLastError();
+}
+
 }  // namespace moe

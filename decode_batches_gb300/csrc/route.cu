@@ -156,29 +156,35 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* w_router, const
 // Top-k with gates
 // ============================================================================================
 
-// true if (va, ia) comes before (vb, ib): larger value first, then lower index; NaN after all
-// numbers (NaNs among themselves by index); -0 == +0.
-MOE_DEVICE bool rank_before(float va, int ia, float vb, int ib) {
-  const bool na = isnan(va), nb = isnan(vb);
-  if (na != nb) return nb;
-  if (!na && va != vb) return va > vb;
-  return ia < ib;
+// Sortable 64-bit key of (logit v, expert e): a larger key ranks first.  The high word maps the
+// float to an unsigned integer that grows with v (-0 is first turned into +0, so the two
+// compare equal); NaN maps to 0, below -inf.  The low word is ~e, so on equal values the lower
+// index ranks first.  Padding lanes (e >= E) get key 0, below every real candidate.
+MOE_DEVICE uint64_t rank_key(float v, int e) {
+  uint32_t hi = 0u;
+  if (!isnan(v)) {
+    const uint32_t b = __float_as_uint(v + 0.0f);
+    hi = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  }
+  return (static_cast<uint64_t>(hi) << 32) | static_cast<uint32_t>(~e);
 }
 
-// One block per 32-token chunk, one warp per token (two per warp for E > 384).  Lane l holds the logits of experts
-// l, l + 32, ..., l + 32 (PL - 1); each of the k rounds takes the lane-local best untaken value
-// and a warp arg-max under rank_before.  Masks are stored expert-major: masks[e * n_chunks + c].
-// The logits are the sum of `nsplit` partial matrices parts[s][T][E] (s ascending) plus the
-// optional bias; they are written to logits_out when it is given.
+// One block per 32-token chunk, one warp per token (two per warp for E > 384).  Lane l holds the
+// keys of experts l, l + 32, ..., l + 32 (PL - 1).  Each of the k rounds takes every lane's best
+// remaining key and a warp-wide maximum (redux on the high word, then on the low word among the
+// lanes that hold that high word); the owner lane retires the winner.  Masks are stored
+// expert-major: masks[e * n_chunks + c].  The logits are the sum of `nsplit` partial matrices
+// parts[s][T][E] (s ascending) plus the optional bias; they are written to logits_out if given.
 template <int PL>
 constexpr int topk_threads() { return PL >= 16 ? 512 : 1024; }  // 64 registers/thread at 1024
 
 template <int PL>
 __global__ void __launch_bounds__(topk_threads<PL>()) topk_kernel(const float* __restrict__ parts, int nsplit,
-                                                    const float* __restrict__ bias, float* __restrict__ logits_out,
-                                                    int T, int E, int k, int n_chunks, int32_t* __restrict__ ids,
-                                                    float* __restrict__ gates, uint32_t* __restrict__ masks,
-                                                    uint32_t* err) {
+                                                                  const float* __restrict__ bias,
+                                                                  float* __restrict__ logits_out, int T, int E, int k,
+                                                                  int n_chunks, int32_t* __restrict__ ids,
+                                                                  float* __restrict__ gates,
+                                                                  uint32_t* __restrict__ masks, uint32_t* err) {
   extern __shared__ uint32_t smask[];  // [E]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
@@ -193,7 +199,7 @@ __global__ void __launch_bounds__(topk_threads<PL>()) topk_kernel(const float* _
 #pragma unroll
     for (int i = 0; i < PL; ++i) {
       const int e = lane + 32 * i;
-      v[i] = e < E ? parts[static_cast<size_t>(t) * E + e] : __int_as_float(0x7fc00000);
+      v[i] = e < E ? parts[static_cast<size_t>(t) * E + e] : 0.f;
     }
     for (int sp = 1; sp < nsplit; ++sp) {
       const float* ps = parts + (static_cast<size_t>(sp) * T + t) * E;
@@ -206,44 +212,41 @@ __global__ void __launch_bounds__(topk_threads<PL>()) topk_kernel(const float* _
 #pragma unroll
       for (int i = 0; i < PL; ++i) v[i] += w[i];
     }
+    uint64_t key[PL];
 #pragma unroll
     for (int i = 0; i < PL; ++i) {
       const int e = lane + 32 * i;
       if (e < E) {
         if (bias) v[i] += bias[e];
         if (logits_out) logits_out[static_cast<size_t>(t) * E + e] = v[i];
+        key[i] = rank_key(v[i], e);
+      } else {
+        key[i] = 0ull;
       }
     }
-    uint32_t taken = 0u;
-    float sel_v = 0.f;  // lane j keeps the value chosen in round j
-    int sel_i = 0;
+    int sel_i = 0;  // lane j keeps the expert chosen in round j
     for (int j = 0; j < k; ++j) {
-      float bv = __int_as_float(0x7fc00000);
-      int bi = 0x7fffffff;
+      uint64_t best = key[0];
 #pragma unroll
-      for (int i = 0; i < PL; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && rank_before(v[i], e, bv, bi)) {
-          bv = v[i];
-          bi = e;
-        }
-      }
+      for (int i = 1; i < PL; ++i) best = key[i] > best ? key[i] : best;
+      const uint32_t hi = static_cast<uint32_t>(best >> 32);
+      const uint32_t win_hi = __reduce_max_sync(0xffffffffu, hi);
+      const uint32_t win_lo = __reduce_max_sync(0xffffffffu, hi == win_hi ? static_cast<uint32_t>(best) : 0u);
+      const int win_e = static_cast<int>(~win_lo);
+      if ((win_e & 31) == lane) {
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (rank_before(ov, oi, bv, bi)) {
-          bv = ov;
-          bi = oi;
-        }
+        for (int i = 0; i < PL; ++i)
+          if (i == (win_e >> 5)) key[i] = 0ull;
       }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == j) {
-        sel_v = bv;
-        sel_i = bi;
-      }
+      if (lane == j) sel_i = win_e;
     }
     // gates: softmax over the k selected logits, slot 0 holds the maximum
+    float sel_v = 0.f;
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+      const float vi = __shfl_sync(0xffffffffu, v[i], sel_i & 31);
+      if (i == (sel_i >> 5)) sel_v = vi;
+    }
     const float vmax = __shfl_sync(0xffffffffu, sel_v, 0);
     const float ex = (lane < k) ? expf(sel_v - vmax) : 0.f;
     float sum = ex;
@@ -312,10 +315,6 @@ __global__ void __launch_bounds__(256) masks_from_ids_kernel(const int32_t* __re
     if (t >= T) continue;
     const int32_t* row = ids + static_cast<size_t>(t) * k;
     const int e = row[j];
-    if (e < 0 || e >= E) {
-      set_error(err, MOE_DEVERR_EXPERT_RANGE);
-      continue;
-    }
     if (!assignment_valid(row, j, e, E)) {
       set_error(err, MOE_DEVERR_EXPERT_RANGE);
       continue;
@@ -334,8 +333,51 @@ cudaError_t launch_masks_from_ids(const int32_t* ids, int T, int E, int k, uint3
   return cudaGetLastError();
 }
 
-// Exclusive scan of one int per thread over a 1024-thread block.  Returns the exclusive
-// prefix; *total receives the block sum.
+// Per-expert scan over chunks: one warp per expert, 32 chunk masks per load (masks are
+// expert-major), the loads of up to kBatch 32-chunk groups issued before any is used.
+// chunk_base[e][c] = number of assignments of expert e in chunks before c; counts[e] = total.
+__global__ void __launch_bounds__(256) chunk_scan_kernel(const uint32_t* __restrict__ masks, int n_chunks, int E,
+                                                         int32_t* __restrict__ chunk_base,
+                                                         int32_t* __restrict__ counts) {
+  constexpr int kBatch = 8;
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (e >= E) return;
+  const uint32_t* m = masks + static_cast<size_t>(e) * n_chunks;
+  int32_t* cb = chunk_base + static_cast<size_t>(e) * n_chunks;
+  const int groups = (n_chunks + 31) / 32;
+  int run = 0;
+  for (int g0 = 0; g0 < groups; g0 += kBatch) {
+    int pc[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int c = (g0 + b) * 32 + lane;
+      pc[b] = c < n_chunks ? __popc(m[c]) : 0;
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      if (g0 + b >= groups) break;
+      int inc = pc[b];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int up = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += up;
+      }
+      const int c = (g0 + b) * 32 + lane;
+      if (c < n_chunks) cb[c] = run + inc - pc[b];
+      run += __shfl_sync(0xffffffffu, inc, 31);
+    }
+  }
+  if (lane == 0) counts[e] = run;
+}
+
+cudaError_t launch_chunk_scan(const uint32_t* masks, int n_chunks, int E, int32_t* chunk_base, int32_t* counts,
+                              cudaStream_t st) {
+  chunk_scan_kernel<<<(E + 7) / 8, 256, 0, st>>>(masks, n_chunks, E, chunk_base, counts);
+  return cudaGetLastError();
+}
+
+// Exclusive scan over the block (blockDim.x a multiple of 32, <= 1024) of v; *total = block sum.
 MOE_DEVICE int block_exclusive_scan(int v, int* total) {
   __shared__ int warp_sums[32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -364,8 +406,8 @@ MOE_DEVICE int block_exclusive_scan(int v, int* total) {
   return warp_excl + inc - v;
 }
 
-// Split `total` rows of expert e (starting at grouped row `start`) into near-equal segments
-// of at most kSegRowsMax rows.
+// Split `total` rows of expert e (starting at grouped row `start`) into near-equal segments of
+// at most kSegRowsMax rows; `base` is the index of the expert's first segment.
 MOE_DEVICE int num_segments(int total) { return (total + kSegRowsMax - 1) / kSegRowsMax; }
 
 MOE_DEVICE void write_segments(Seg* segs, int base, int max_segs, int e, int start, int total,
@@ -385,91 +427,67 @@ MOE_DEVICE void write_segments(Seg* segs, int base, int max_segs, int e, int sta
   }
 }
 
-// Single block of 1024 threads.  Warp w scans experts w, w + 32, ...: 32 consecutive chunk masks
-// of one expert per load (masks are expert-major), popcount, warp prefix sum -> chunk bases.
-// Loads are issued in batches of kBatch (expert, 32-chunk group) items before any is used, so
-// the warp waits for memory once per batch instead of once per item.  Then thread e scans the
-// expert totals -> offsets, and writes the expert's segments.
-__global__ void __launch_bounds__(1024) group_scan_kernel(const uint32_t* __restrict__ masks, int n_chunks,
-                                                          int E, int32_t* __restrict__ chunk_base,
-                                                          int32_t* __restrict__ counts,
-                                                          int32_t* __restrict__ offsets, Seg* segs,
-                                                          int32_t* n_segs, int max_segs, uint32_t* err) {
-  constexpr int kBatch = 16;
-  __shared__ int s_total[1024];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int groups = (n_chunks + 31) / 32;                 // 32-chunk groups per expert
-  const int my_experts = E > warp ? (E - warp + 31) / 32 : 0;
-  const int items = my_experts * groups;                   // item i: expert warp + 32 (i / groups), group i % groups
-  int run = 0;
-  for (int b0 = 0; b0 < items; b0 += kBatch) {
-    int pc[kBatch];
+constexpr int kScanThreads = 256;
+constexpr int kScanPerThread = 1024 / kScanThreads;  // E <= 1024
+
+// Block-wide exclusive scan of counts[0..E) into s_off[0..E]; returns the total.
+MOE_DEVICE int block_offsets(const int32_t* __restrict__ counts, int E, int* s_off) {
+  int c[kScanPerThread];
+  int mine = 0;
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      const int i = b0 + j;
-      pc[j] = 0;
-      if (i < items) {
-        const int e = warp + 32 * (i / groups);
-        const int c = (i % groups) * 32 + lane;
-        if (c < n_chunks) pc[j] = __popc(masks[static_cast<size_t>(e) * n_chunks + c]);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      const int i = b0 + j;
-      if (i >= items) break;
-      const int e = warp + 32 * (i / groups);
-      const int g = i % groups;
-      if (g == 0) run = 0;
-      int inc = pc[j];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int up = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += up;
-      }
-      const int c = g * 32 + lane;
-      if (c < n_chunks) chunk_base[static_cast<size_t>(e) * n_chunks + c] = run + inc - pc[j];
-      run += __shfl_sync(0xffffffffu, inc, 31);
-      if (g == groups - 1 && lane == 0) s_total[e] = run;
-    }
+  for (int q = 0; q < kScanPerThread; ++q) {
+    const int e = threadIdx.x * kScanPerThread + q;
+    c[q] = e < E ? counts[e] : 0;
+    mine += c[q];
   }
-  if (groups == 0)
-    for (int e = threadIdx.x; e < E; e += blockDim.x) s_total[e] = 0;
-  __syncthreads();
-  const int e = threadIdx.x;
-  const int tot_e = e < E ? s_total[e] : 0;
   int total;
-  const int off = block_exclusive_scan(tot_e, &total);
-  if (e < E) {
-    counts[e] = tot_e;
-    offsets[e] = off;
+  int run = block_exclusive_scan(mine, &total);
+#pragma unroll
+  for (int q = 0; q < kScanPerThread; ++q) {
+    const int e = threadIdx.x * kScanPerThread + q;
+    if (e < E) s_off[e] = run;
+    run += c[q];
   }
-  if (e == 0) offsets[E] = total;
-  if (segs) {
-    int seg_total;
-    const int ns = e < E ? num_segments(tot_e) : 0;
-    const int sbase = block_exclusive_scan(ns, &seg_total);
-    if (e < E) write_segments(segs, sbase, max_segs, e, off, tot_e, err);
-    if (e == 0) *n_segs = min(seg_total, max_segs);
-  }
+  if (threadIdx.x == 0) s_off[E] = total;
+  __syncthreads();
+  return total;
 }
 
-cudaError_t launch_group_scan(const uint32_t* masks, int n_chunks, int E, int32_t* chunk_base,
-                              int32_t* counts, int32_t* offsets, Seg* segs, int32_t* n_segs,
-                              int max_segs, uint32_t* err, cudaStream_t st) {
-  group_scan_kernel<<<1, 1024, 0, st>>>(masks, n_chunks, E, chunk_base, counts, offsets, segs, n_segs,
-                                        max_segs, err);
-  return cudaGetLastError();
-}
-
-__global__ void __launch_bounds__(256) scatter_kernel(const int32_t* __restrict__ ids,
-                                                      const uint32_t* __restrict__ masks,
-                                                      const int32_t* __restrict__ chunk_base,
-                                                      const int32_t* __restrict__ offsets, int T, int E,
-                                                      int k, int32_t* __restrict__ perm,
-                                                      int32_t* __restrict__ inv) {
+// One block per 32-token chunk.  Every block scans the expert counts into shared offsets (E
+// values, cheaper than another launch); block 0 also publishes offsets and, if segs is given,
+// the segment list of the grouped GEMMs.  Each assignment's row is offsets[e] + its chunk's
+// base + the popcount of the earlier bits of the chunk's mask word: a stable counting sort.
+__global__ void __launch_bounds__(kScanThreads) scatter_kernel(
+    const int32_t* __restrict__ ids, const uint32_t* __restrict__ masks, const int32_t* __restrict__ chunk_base,
+    const int32_t* __restrict__ counts, int T, int E, int k, int n_chunks, int32_t* __restrict__ perm,
+    int32_t* __restrict__ inv, int32_t* __restrict__ offsets, Seg* segs, int32_t* n_segs, int max_segs,
+    uint32_t* err) {
+  __shared__ int s_off[1025];
+  block_offsets(counts, E, s_off);
+  if (blockIdx.x == 0) {
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = s_off[e];
+    if (segs) {
+      int ns[kScanPerThread];
+      int mine = 0;
+#pragma unroll
+      for (int q = 0; q < kScanPerThread; ++q) {
+        const int e = threadIdx.x * kScanPerThread + q;
+        ns[q] = e < E ? num_segments(s_off[e + 1] - s_off[e]) : 0;
+        mine += ns[q];
+      }
+      int seg_total;
+      int base = block_exclusive_scan(mine, &seg_total);
+#pragma unroll
+      for (int q = 0; q < kScanPerThread; ++q) {
+        const int e = threadIdx.x * kScanPerThread + q;
+        if (e < E) write_segments(segs, base, max_segs, e, s_off[e], s_off[e + 1] - s_off[e], err);
+        base += ns[q];
+      }
+      if (threadIdx.x == 0) *n_segs = min(seg_total, max_segs);
+    }
+  }
   const int c = blockIdx.x;
-  const int n_chunks = gridDim.x;
+  if (c >= n_chunks) return;
   for (int a = threadIdx.x; a < kChunk * k; a += blockDim.x) {
     const int tl = a / k, j = a % k;
     const int t = c * kChunk + tl;
@@ -483,36 +501,49 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int32_t* __restrict_
     }
     const size_t me = static_cast<size_t>(e) * n_chunks + c;
     const int rank = __popc(masks[me] & ((1u << tl) - 1u));
-    const int r = offsets[e] + chunk_base[me] + rank;
+    const int r = s_off[e] + chunk_base[me] + rank;
     perm[r] = static_cast<int32_t>(ai);
     inv[ai] = r;
   }
 }
 
 cudaError_t launch_scatter(const int32_t* ids, const uint32_t* masks, const int32_t* chunk_base,
-                           const int32_t* offsets, int T, int E, int k, int32_t* perm, int32_t* inv,
+                           const int32_t* counts, int T, int E, int k, int32_t* perm, int32_t* inv,
+                           int32_t* offsets, Seg* segs, int32_t* n_segs, int max_segs, uint32_t* err,
                            cudaStream_t st) {
-  if (T <= 0) return cudaSuccess;
   const int n_chunks = (T + kChunk - 1) / kChunk;
-  scatter_kernel<<<n_chunks, 256, 0, st>>>(ids, masks, chunk_base, offsets, T, E, k, perm, inv);
+  scatter_kernel<<<n_chunks > 0 ? n_chunks : 1, kScanThreads, 0, st>>>(ids, masks, chunk_base, counts, T, E, k,
+                                                                       n_chunks, perm, inv, offsets, segs, n_segs,
+                                                                       max_segs, err);
   return cudaGetLastError();
 }
 
-__global__ void __launch_bounds__(1024) segments_from_offsets_kernel(const int32_t* __restrict__ offsets,
-                                                                     int E, Seg* segs, int32_t* n_segs,
-                                                                     int max_segs, uint32_t* err) {
-  const int e = threadIdx.x;
-  const int start = e < E ? offsets[e] : 0;
-  const int total = e < E ? offsets[e + 1] - start : 0;
+// Segment list from offsets only (the separate experts entry point).  One block of 256 threads.
+__global__ void __launch_bounds__(kScanThreads) segments_from_offsets_kernel(const int32_t* __restrict__ offsets,
+                                                                           int E, Seg* segs, int32_t* n_segs,
+                                                                           int max_segs, uint32_t* err) {
+  int ns[kScanPerThread];
+  int mine = 0;
+#pragma unroll
+  for (int q = 0; q < kScanPerThread; ++q) {
+    const int e = threadIdx.x * kScanPerThread + q;
+    ns[q] = e < E ? num_segments(offsets[e + 1] - offsets[e]) : 0;
+    mine += ns[q];
+  }
   int seg_total;
-  const int sbase = block_exclusive_scan(num_segments(total), &seg_total);
-  if (e < E) write_segments(segs, sbase, max_segs, e, start, total, err);
-  if (e == 0) *n_segs = min(seg_total, max_segs);
+  int base = block_exclusive_scan(mine, &seg_total);
+#pragma unroll
+  for (int q = 0; q < kScanPerThread; ++q) {
+    const int e = threadIdx.x * kScanPerThread + q;
+    if (e < E) write_segments(segs, base, max_segs, e, offsets[e], offsets[e + 1] - offsets[e], err);
+    base += ns[q];
+  }
+  if (threadIdx.x == 0) *n_segs = min(seg_total, max_segs);
 }
 
 cudaError_t launch_segments_from_offsets(const int32_t* offsets, int E, Seg* segs, int32_t* n_segs,
                                          int max_segs, uint32_t* err, cudaStream_t st) {
-  segments_from_offsets_kernel<<<1, 1024, 0, st>>>(offsets, E, segs, n_segs, max_segs, err);
+  segments_from_offsets_kernel<<<1, kScanThreads, 0, st>>>(offsets, E, segs, n_segs, max_segs, err);
   return cudaGetLastError();
 }
 

@@ -178,3 +178,19 @@ def test_forward_edge_arguments_and_canaries():
     assert torch.all(buf[:guard] == 12345) and torch.all(buf[-guard:] == 12345)
     ref = oracle_layer(w)
     compare_layer(bf16_tensor_to_f64(out_view), ref, w.spec.k, TOL_BF16)
+
+
+def test_untiled_shape_runs_the_reference_path():
+    """d and d_ff that the tensor-core tiles do not divide: the plan keeps the row-interleaved
+    layout and the CUDA-core path computes the layer (with shared experts)."""
+    spec = synth.LayerSpec(E=5, k=2, d=96, f=40, n_shared=2, f_s=24, wdtype="bf16")
+    w = synth.custom(spec, 37, n_prefill=30, name="odd")
+    plan = make_plan(w)
+    from decode_batches_gb300 import MoeError
+    with pytest.raises(MoeError):
+        plan.set_path("tc")
+    x = to_dev(w.x(), "bf16")
+    out = bf16_tensor_to_f64(plan.forward(x, n_prefill=w.n_prefill))
+    _, ids, _ = plan.route(x, want_logits=False)
+    compare_layer(out, oracle_layer(w), spec.k, TOL_BF16, ids.cpu().numpy())
+    assert plan.device_error() == 0
