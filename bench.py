@@ -307,8 +307,12 @@ def run_gpu(args):
     clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv") if os.path.isdir(
         os.path.join(ROOT, "gpurun_out")) else None)
     clocks.start()
-    ms, kernels, _ = time_forward(plan, x, w.n_prefill, args.steps, args.warmup, world, timing=True)
+    # timed region: K steps, nothing recorded between the layer's kernels
+    ms, _, _ = time_forward(plan, x, w.n_prefill, args.steps, args.warmup, world)
     clk = clocks.stop()
+    # per-kernel durations: a second timed region with CUDA events around every launch (the
+    # events serialise the launches, so this region is not the one `value` comes from)
+    _, kernels, _ = time_forward(plan, x, w.n_prefill, max(20, args.steps // 4), 3, world, timing=True)
     launches_per_step = plan.last_launch_count()
 
     tokens_per_s = world * T / (ms * 1e-3)
@@ -342,8 +346,8 @@ def run_gpu(args):
         xq = dev(wq.x()).view(torch.bfloat16)
         cq = routing_counts(plan, xq)
         bq = layer_bytes_flops(wq, cq)
-        msq, kq, _ = time_forward(plan, xq, wq.n_prefill, max(20, min(args.steps, 400)), max(3, args.warmup), world,
-                                  timing=True)
+        msq, _, _ = time_forward(plan, xq, wq.n_prefill, max(20, min(args.steps, 400)), max(3, args.warmup), world)
+        _, kq, _ = time_forward(plan, xq, wq.n_prefill, max(20, min(args.steps, 100)), 3, world, timing=True)
         tq = max(bq["bytes"] / (hbm * 1e9), bq["flops"] / (tflops * 1e12))
         sweep.append({"quantum": q, "T": wq.T, "tokens_per_s": round(world * wq.T / (msq * 1e-3), 1),
                       "ms_per_step": round(msq, 5), "touched_experts": bq["touched"],

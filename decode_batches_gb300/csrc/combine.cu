@@ -14,6 +14,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
                                                       uint16_t* __restrict__ out) {
   __shared__ int s_row[32];
   __shared__ float s_g[32];
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x;
   if (threadIdx.x < k) {
     s_row[threadIdx.x] = inv[static_cast<size_t>(t) * k + threadIdx.x];
@@ -55,8 +57,7 @@ cudaError_t launch_combine(const uint16_t* y, const float* gates, const int32_t*
   int threads = d / 8;
   if (threads > 256) threads = 256;
   threads = (threads + 31) / 32 * 32;
-  combine_kernel<<<T, threads, 0, st>>>(y, gates, inv, shared_y, T, k, d, out);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(T), dim3(threads), 0, st, y, gates, inv, shared_y, T, k, d, out);
 }
 
 }  // namespace moe

@@ -12,6 +12,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/moe.h"
 
 #define MOE_DEVICE __device__ __forceinline__
@@ -36,6 +38,33 @@ MOE_DEVICE uint64_t global_timer_ns() {
 
 MOE_DEVICE void set_error(uint32_t* err, uint32_t bits) {
   if (err) atomicOr(err, bits);
+}
+
+// ------------------------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of a layer step is launched with programmatic
+// stream serialization: it may start while its predecessor in the stream is still running,
+// runs its shared-memory / TMEM prologue, then waits in pdl_wait() -- before its first global
+// memory access -- until the predecessor has completed and its writes are visible.  pdl_trigger()
+// at kernel entry lets the successor launch early.  Without the launch attribute both are no-ops.
+// ------------------------------------------------------------------------------------------
+MOE_DEVICE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MOE_DEVICE void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Host side: launch `kern` with the programmatic-stream-serialization attribute.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // ------------------------------------------------------------------------------------------

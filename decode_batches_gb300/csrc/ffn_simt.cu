@@ -119,6 +119,8 @@ __global__ void __launch_bounds__(256) simt_gateup_kernel(FfnWeights w, const ui
                                                           const int32_t* __restrict__ perm,
                                                           uint16_t* __restrict__ h, uint16_t* __restrict__ h_s) {
   extern __shared__ float act[];  // [d]
+  pdl_trigger();
+  pdl_wait();
   const int R = T * w.k;
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -187,6 +189,8 @@ __global__ void __launch_bounds__(256) simt_down_kernel(FfnWeights w, int T, con
                                                         const uint16_t* __restrict__ h_s,
                                                         uint16_t* __restrict__ y, uint16_t* __restrict__ y_s) {
   extern __shared__ float act[];  // [max(f, n_s * f_s)]
+  pdl_trigger();
+  pdl_wait();
   const int R = T * w.k;
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -243,12 +247,12 @@ cudaError_t launch_ffn_simt(const FfnWeights& w, const uint16_t* x, int T, const
                             uint16_t* y_s, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
   const int blocks = T * w.k + (w.n_shared > 0 ? T : 0);
-  simt_gateup_kernel<<<blocks, 256, w.d * sizeof(float), st>>>(w, x, T, offsets, perm, h, h_s);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(simt_gateup_kernel, dim3(blocks), dim3(256), w.d * sizeof(float), st, w, x, T, offsets,
+                             perm, h, h_s);
   if (e != cudaSuccess) return e;
   const int kmax = w.f > w.n_shared * w.f_s ? w.f : w.n_shared * w.f_s;
-  simt_down_kernel<<<blocks, 256, kmax * sizeof(float), st>>>(w, T, offsets, h, h_s, y, y_s);
-  return cudaGetLastError();
+  return launch_pdl(simt_down_kernel, dim3(blocks), dim3(256), kmax * sizeof(float), st, w, T, offsets,
+                    static_cast<const uint16_t*>(h), static_cast<const uint16_t*>(h_s), y, y_s);
 }
 
 }  // namespace moe

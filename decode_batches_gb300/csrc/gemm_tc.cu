@@ -130,6 +130,8 @@ __global__ void __launch_bounds__(kGateUp ? 320 : 192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+  pdl_wait();  // the predecessor's outputs (segments, perm, h) are visible from here on
 
   const int tiles_r = kGateUp ? a.f / 64 : a.d / BM;
   const int tiles_s = kGateUp ? (a.n_shared * a.f_s) / 64 : a.d / BM;
@@ -359,8 +361,7 @@ static cudaError_t launch_tc(const TcMaps* maps, const TcArgs& a, int num_sms, c
     if (e != cudaSuccess) return e;
     g_tc_attr_set[kGateUp] = true;
   }
-  kern<<<num_sms, kGateUp ? 320 : 192, tc::kSmemBytes, st>>>(*maps, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(num_sms), dim3(kGateUp ? 320 : 192), tc::kSmemBytes, st, *maps, a);
 }
 
 cudaError_t launch_tc_gateup(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st) {

@@ -31,6 +31,8 @@ __global__ void __launch_bounds__(256) router_logits_small_kernel(const uint16_t
                                                                   const float* __restrict__ br, int T,
                                                                   int E, int d,
                                                                   float* __restrict__ logits) {
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * 8 + warp;
   const int t0 = blockIdx.y * kTokTile;
@@ -82,6 +84,8 @@ __global__ void __launch_bounds__(256) router_logits_tiled_kernel(const uint16_t
                                                                   int E, int d,
                                                                   float* __restrict__ logits) {
   constexpr int BM = 64, BN = 64, BK = 32;
+  pdl_trigger();
+  pdl_wait();
   __shared__ float xs[BK][BM + 4];
   __shared__ float ws[BK][BN + 4];
   const int tid = threadIdx.x;
@@ -144,12 +148,11 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* w_router, const
   if (T <= 0) return cudaSuccess;
   if (T <= 128) {
     dim3 grid((E + 7) / 8, (T + 15) / 16);
-    router_logits_small_kernel<16><<<grid, 256, 0, st>>>(x, w_router, b_router, T, E, d, logits);
+    return launch_pdl(router_logits_small_kernel<16>, grid, dim3(256), 0, st, x, w_router, b_router, T, E, d, logits);
   } else {
     dim3 grid((T + 63) / 64, (E + 63) / 64);
-    router_logits_tiled_kernel<<<grid, 256, 0, st>>>(x, w_router, b_router, T, E, d, logits);
+    return launch_pdl(router_logits_tiled_kernel, grid, dim3(256), 0, st, x, w_router, b_router, T, E, d, logits);
   }
-  return cudaGetLastError();
 }
 
 // ============================================================================================
@@ -186,6 +189,8 @@ __global__ void __launch_bounds__(topk_threads<PL>()) topk_kernel(const float* _
                                                                   float* __restrict__ gates,
                                                                   uint32_t* __restrict__ masks, uint32_t* err) {
   extern __shared__ uint32_t smask[];  // [E]
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
   if (masks)
@@ -267,10 +272,11 @@ __global__ void __launch_bounds__(topk_threads<PL>()) topk_kernel(const float* _
 }
 
 template <int PL>
-static void launch_topk_pl(const float* parts, int nsplit, const float* bias, float* logits_out, int T, int E, int k,
-                           int n_chunks, int32_t* ids, float* gates, uint32_t* masks, uint32_t* err, cudaStream_t st) {
-  topk_kernel<PL><<<n_chunks, topk_threads<PL>(), masks ? E * sizeof(uint32_t) : 0, st>>>(
-      parts, nsplit, bias, logits_out, T, E, k, n_chunks, ids, gates, masks, err);
+static cudaError_t launch_topk_pl(const float* parts, int nsplit, const float* bias, float* logits_out, int T, int E,
+                                  int k, int n_chunks, int32_t* ids, float* gates, uint32_t* masks, uint32_t* err,
+                                  cudaStream_t st) {
+  return launch_pdl(topk_kernel<PL>, dim3(n_chunks), dim3(topk_threads<PL>()), masks ? E * sizeof(uint32_t) : 0, st,
+                    parts, nsplit, bias, logits_out, T, E, k, n_chunks, ids, gates, masks, err);
 }
 
 cudaError_t launch_topk(const float* parts, int nsplit, const float* bias, float* logits_out, int T, int E, int k,
@@ -279,15 +285,14 @@ cudaError_t launch_topk(const float* parts, int nsplit, const float* bias, float
   const int n_chunks = (T + kChunk - 1) / kChunk;
   const int pl = (E + 31) / 32;
 #define MOE_TOPK(PLV) launch_topk_pl<PLV>(parts, nsplit, bias, logits_out, T, E, k, n_chunks, ids, gates, masks, err, st)
-  if (pl <= 1) MOE_TOPK(1);
-  else if (pl <= 2) MOE_TOPK(2);
-  else if (pl <= 4) MOE_TOPK(4);
-  else if (pl <= 8) MOE_TOPK(8);
-  else if (pl <= 12) MOE_TOPK(12);
-  else if (pl <= 16) MOE_TOPK(16);
-  else MOE_TOPK(32);
+  if (pl <= 1) return MOE_TOPK(1);
+  if (pl <= 2) return MOE_TOPK(2);
+  if (pl <= 4) return MOE_TOPK(4);
+  if (pl <= 8) return MOE_TOPK(8);
+  if (pl <= 12) return MOE_TOPK(12);
+  if (pl <= 16) return MOE_TOPK(16);
+  return MOE_TOPK(32);
 #undef MOE_TOPK
-  return cudaGetLastError();
 }
 
 // ============================================================================================
@@ -306,6 +311,8 @@ __global__ void __launch_bounds__(256) masks_from_ids_kernel(const int32_t* __re
                                                              int k, int n_chunks, uint32_t* __restrict__ masks,
                                                              uint32_t* err) {
   extern __shared__ uint32_t smask[];
+  pdl_trigger();
+  pdl_wait();
   const int c = blockIdx.x;
   for (int e = threadIdx.x; e < E; e += blockDim.x) smask[e] = 0u;
   __syncthreads();
@@ -329,8 +336,8 @@ cudaError_t launch_masks_from_ids(const int32_t* ids, int T, int E, int k, uint3
                                   uint32_t* err, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
   const int n_chunks = (T + kChunk - 1) / kChunk;
-  masks_from_ids_kernel<<<n_chunks, 256, E * sizeof(uint32_t), st>>>(ids, T, E, k, n_chunks, masks, err);
-  return cudaGetLastError();
+  return launch_pdl(masks_from_ids_kernel, dim3(n_chunks), dim3(256), E * sizeof(uint32_t), st, ids, T, E, k, n_chunks,
+                    masks, err);
 }
 
 // Per-expert scan over chunks: one warp per expert, 32 chunk masks per load (masks are
@@ -340,6 +347,8 @@ __global__ void __launch_bounds__(256) chunk_scan_kernel(const uint32_t* __restr
                                                          int32_t* __restrict__ chunk_base,
                                                          int32_t* __restrict__ counts) {
   constexpr int kBatch = 8;
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (e >= E) return;
@@ -373,8 +382,7 @@ __global__ void __launch_bounds__(256) chunk_scan_kernel(const uint32_t* __restr
 
 cudaError_t launch_chunk_scan(const uint32_t* masks, int n_chunks, int E, int32_t* chunk_base, int32_t* counts,
                               cudaStream_t st) {
-  chunk_scan_kernel<<<(E + 7) / 8, 256, 0, st>>>(masks, n_chunks, E, chunk_base, counts);
-  return cudaGetLastError();
+  return launch_pdl(chunk_scan_kernel, dim3((E + 7) / 8), dim3(256), 0, st, masks, n_chunks, E, chunk_base, counts);
 }
 
 // Exclusive scan over the block (blockDim.x a multiple of 32, <= 1024) of v; *total = block sum.
@@ -463,6 +471,8 @@ __global__ void __launch_bounds__(kScanThreads) scatter_kernel(
     int32_t* __restrict__ inv, int32_t* __restrict__ offsets, Seg* segs, int32_t* n_segs, int max_segs,
     uint32_t* err) {
   __shared__ int s_off[1025];
+  pdl_trigger();
+  pdl_wait();
   block_offsets(counts, E, s_off);
   if (blockIdx.x == 0) {
     for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = s_off[e];
@@ -512,16 +522,16 @@ cudaError_t launch_scatter(const int32_t* ids, const uint32_t* masks, const int3
                            int32_t* offsets, Seg* segs, int32_t* n_segs, int max_segs, uint32_t* err,
                            cudaStream_t st) {
   const int n_chunks = (T + kChunk - 1) / kChunk;
-  scatter_kernel<<<n_chunks > 0 ? n_chunks : 1, kScanThreads, 0, st>>>(ids, masks, chunk_base, counts, T, E, k,
-                                                                       n_chunks, perm, inv, offsets, segs, n_segs,
-                                                                       max_segs, err);
-  return cudaGetLastError();
+  return launch_pdl(scatter_kernel, dim3(n_chunks > 0 ? n_chunks : 1), dim3(kScanThreads), 0, st, ids, masks, chunk_base,
+                    counts, T, E, k, n_chunks, perm, inv, offsets, segs, n_segs, max_segs, err);
 }
 
 // Segment list from offsets only (the separate experts entry point).  One block of 256 threads.
 __global__ void __launch_bounds__(kScanThreads) segments_from_offsets_kernel(const int32_t* __restrict__ offsets,
                                                                            int E, Seg* segs, int32_t* n_segs,
                                                                            int max_segs, uint32_t* err) {
+  pdl_trigger();
+  pdl_wait();
   int ns[kScanPerThread];
   int mine = 0;
 #pragma unroll
@@ -543,8 +553,8 @@ __global__ void __launch_bounds__(kScanThreads) segments_from_offsets_kernel(con
 
 cudaError_t launch_segments_from_offsets(const int32_t* offsets, int E, Seg* segs, int32_t* n_segs,
                                          int max_segs, uint32_t* err, cudaStream_t st) {
-  segments_from_offsets_kernel<<<1, kScanThreads, 0, st>>>(offsets, E, segs, n_segs, max_segs, err);
-  return cudaGetLastError();
+  return launch_pdl(segments_from_offsets_kernel, dim3(1), dim3(kScanThreads), 0, st, offsets, E, segs, n_segs, max_segs,
+                    err);
 }
 
 }  // namespace moe

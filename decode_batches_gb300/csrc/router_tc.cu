@@ -68,6 +68,8 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+  pdl_wait();  // x and the previous step's readers of `parts` are done from here on
 
   if (warp == 0) {
     if (lane == 0) {
@@ -197,8 +199,7 @@ cudaError_t launch_router_tc(const CUtensorMap* w3, const uint16_t* x, int T, in
     g_rt_attr = true;
   }
   dim3 grid(E / rt::BM, (T + rt::BN - 1) / rt::BN, nsplit);
-  rt::router_tc_kernel<<<grid, 320, rt::kSmemBytes, st>>>(*w3, x, T, E, d, nsplit, parts, err);
-  return cudaGetLastError();
+  return launch_pdl(rt::router_tc_kernel, grid, dim3(320), rt::kSmemBytes, st, *w3, x, T, E, d, nsplit, parts, err);
 }
 
 // W_r (fp32 [E][d]) -> three bf16 matrices [3][E][d] with W1 + W2 + W3 == W_r exactly.
