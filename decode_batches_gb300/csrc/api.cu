@@ -46,7 +46,7 @@ namespace {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t logits, parts, ids, gates, masks, chunk_base, counts, offsets, perm, inv, segs, n_segs, h, h_s, y, y_s;
+  size_t logits, parts, ids, gates, masks, chunk_base, counts, offsets, perm, inv, segs, n_segs, h, h_s, y, y_s, x16;
   size_t total;
   int max_segs;
 };
@@ -78,6 +78,8 @@ struct moe_plan {
   uint32_t* err = nullptr;
   bool weights_set = false, shared_set = false;
   bool tiled = false, tiled_s = false;  // weights stored in the tile-contiguous layouts
+  bool fp4_tiled = false;  // 4-bit routed weights in the tile-contiguous layout
+  bool fp4_tc = false;     // ... and every scale in the fp16-exact range: tensor-core path allowed
   // workspace (caller-owned)
   uint8_t* ws = nullptr;
   size_t ws_bytes = 0;
@@ -130,6 +132,7 @@ static WsLayout layout_for(const moe_plan* p, int T_max) {
   L.h_s = take(T * static_cast<size_t>(p->n_shared) * p->f_s * 2);
   L.y = take(R * p->d * 2);
   L.y_s = take(T * p->d * 2);
+  L.x16 = take(p->wdtype == MOE_W_MXFP4 ? T * p->d * 2 : 0);
   L.total = o;
   return L;
 }
@@ -139,9 +142,12 @@ static Tp* ws_ptr(moe_plan* p, size_t off) {
   return reinterpret_cast<Tp*>(p->ws + off);
 }
 
+// The tensor-core path: bf16 routed weights with d % 128 == 0 and d_ff % 64 == 0, or 4-bit
+// routed weights in the tiled layout whose scales all allow exact fp16 dequantisation; shared
+// experts need d_ff_shared % 64 == 0.
 static bool tc_shape_ok(const moe_plan* p) {
-  return p->wdtype == MOE_W_BF16 && p->d % 128 == 0 && p->f % 64 == 0 &&
-         (p->n_shared == 0 || p->f_s % 64 == 0);
+  const bool routed = p->wdtype == MOE_W_BF16 ? (p->d % 128 == 0 && p->f % 64 == 0) : p->fp4_tc;
+  return routed && (p->n_shared == 0 || p->f_s % 64 == 0);
 }
 
 static bool use_tc(const moe_plan* p) {
@@ -226,7 +232,8 @@ static moe_status make_map_16(CUtensorMap* m, const void* base, uint64_t inner, 
 
 static moe_status build_weight_maps(moe_plan* p) {
   // the tensor-core path reads the tile-contiguous weights directly (bulk copies, no maps)
-  p->maps_weights = tc_shape_ok(p) && p->weights_set && p->tiled && (p->n_shared == 0 || (p->shared_set && p->tiled_s));
+  const bool routed = p->wdtype == MOE_W_BF16 ? p->tiled : p->fp4_tc;
+  p->maps_weights = tc_shape_ok(p) && p->weights_set && routed && (p->n_shared == 0 || (p->shared_set && p->tiled_s));
   return MOE_OK;
 }
 
@@ -388,6 +395,33 @@ extern "C" moe_status moe_plan_set_weights(moe_plan* p, const float* w_router, c
   const size_t gu_row = fp4 ? d / 2 : d * 2;     // bytes per gate/up row
   const size_t dn_row = fp4 ? f / 2 : f * 2;     // bytes per down row
   p->tiled = !fp4 && d % 128 == 0 && f % 64 == 0;
+  p->fp4_tiled = fp4 && d % 128 == 0 && f % 64 == 0;
+  p->fp4_tc = false;
+  if (p->fp4_tiled) {
+    // codes and scales go together into kFp4BlockBytes blocks; no separate scale arrays
+    const size_t gu_blocks = E * (f / 64) * (d / 64), dn_blocks = E * (d / 128) * (f / 64);
+    MOE_CUDA_TRY(cudaMalloc(&p->w_gu, gu_blocks * kFp4BlockBytes));
+    MOE_CUDA_TRY(cudaMalloc(&p->w_down, dn_blocks * kFp4BlockBytes));
+    uint32_t* flag = nullptr;
+    MOE_CUDA_TRY(cudaMalloc(&flag, sizeof(uint32_t)));
+    cudaMemset(flag, 0, sizeof(uint32_t));
+    cudaError_t e = launch_tile_fp4(static_cast<const uint8_t*>(w_gate), s_gate, static_cast<const uint8_t*>(w_up), s_up,
+                                    p->w_gu, p->E, p->f, p->d, 1, flag, 0);
+    if (e == cudaSuccess)
+      e = launch_tile_fp4(static_cast<const uint8_t*>(w_down), s_down, nullptr, nullptr, p->w_down, p->E, p->d, p->f, 0,
+                          flag, 0);
+    uint32_t oor = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(&oor, flag, sizeof oor, cudaMemcpyDeviceToHost);
+    cudaFree(flag);
+    if (e != cudaSuccess) {
+      free_weights(p);
+      return fail(MOE_ERR_CUDA, "4-bit weight tiling: %s", cudaGetErrorString(e));
+    }
+    p->fp4_tc = oor == 0;  // otherwise the CUDA-core path runs the same layout
+    MOE_CUDA_TRY(cudaDeviceSynchronize());
+    p->weights_set = true;
+    return build_weight_maps(p);
+  }
   MOE_CUDA_TRY(cudaMalloc(&p->w_gu, E * 2 * f * gu_row));
   MOE_CUDA_TRY(cudaMalloc(&p->w_down, E * d * dn_row));
   if (p->tiled) {
@@ -531,6 +565,7 @@ static FfnWeights ffn_weights(const moe_plan* p) {
   w.err = p->err;
   w.tiled = p->tiled ? 1 : 0;
   w.tiled_s = p->tiled_s ? 1 : 0;
+  w.fp4_tiled = p->fp4_tiled ? 1 : 0;
   return w;
 }
 
@@ -564,8 +599,24 @@ static moe_status run_experts(moe_plan* p, const uint16_t* x, int T, const int32
     a.n_shared = p->n_shared;
     a.f_s = p->f_s;
     a.n_shared_segs = p->n_shared > 0 ? (T + kSegRowsMax - 1) / kSegRowsMax : 0;
-    LAUNCH(p, "tc_gateup", st, launch_tc_gateup(&p->maps, a, p->num_sms, st));
-    LAUNCH(p, "tc_down", st, launch_tc_down(&p->maps, a, p->num_sms, st));
+    if (p->wdtype == MOE_W_MXFP4) {
+      // routed experts on the 4-bit kernels (fp16 activations), shared experts on the 16-bit
+      // kernels restricted to their units
+      uint16_t* x16 = ws_ptr<uint16_t>(p, p->L.x16);
+      a.q_gu = p->w_gu;
+      a.q_down = p->w_down;
+      a.x16 = x16;
+      LAUNCH(p, "x_to_f16", st, launch_x_to_f16(x, x16, static_cast<size_t>(T) * p->d, p->err, st));
+      LAUNCH(p, "fp4_gateup", st, launch_fp4_gateup(&p->maps, a, p->num_sms, st));
+      TcArgs sh = a;
+      sh.routed = 0;
+      if (p->n_shared > 0) LAUNCH(p, "tc_gateup_shared", st, launch_tc_gateup(&p->maps, sh, p->num_sms, st));
+      LAUNCH(p, "fp4_down", st, launch_fp4_down(&p->maps, a, p->num_sms, st));
+      if (p->n_shared > 0) LAUNCH(p, "tc_down_shared", st, launch_tc_down(&p->maps, sh, p->num_sms, st));
+    } else {
+      LAUNCH(p, "tc_gateup", st, launch_tc_gateup(&p->maps, a, p->num_sms, st));
+      LAUNCH(p, "tc_down", st, launch_tc_down(&p->maps, a, p->num_sms, st));
+    }
   } else {
     FfnWeights w = ffn_weights(p);
     LAUNCH(p, "simt_ffn", st, launch_ffn_simt(w, x, T, offsets, perm, h, h_s, y, y_s, st));

@@ -103,6 +103,28 @@ MOE_DEVICE float warp_dot_fp4(const float* act, const uint8_t* crow, const uint8
   return acc;
 }
 
+// Same with a row of the 4-bit tile-contiguous layout: `blocks` is the row's first block (K
+// chunk 0), r its row inside the blocks; 32-element scale block b lives in chunk b / 2, half b % 2.
+MOE_DEVICE float warp_dot_fp4_tiled(const float* act, const uint8_t* blocks, int r, int K, int lane) {
+  float acc = 0.f;
+  for (int b = lane; b < K / 32; b += 32) {
+    const uint8_t* blk = blocks + static_cast<size_t>(b >> 1) * kFp4BlockBytes;
+    const uint4 cv = *reinterpret_cast<const uint4*>(blk + (b & 1) * 2048 + r * 16);
+    const float scale = ldexpf(1.0f, static_cast<int>(blk[4096 + 2 * r + (b & 1)]) - 127);
+    const uint32_t w[4] = {cv.x, cv.y, cv.z, cv.w};
+    float part = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+#pragma unroll
+      for (int n = 0; n < 8; ++n) part = fmaf(act[b * 32 + q * 8 + n], c_e2m1[(w[q] >> (4 * n)) & 0xF], part);
+    }
+    acc = fmaf(part, scale, acc);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  return acc;
+}
+
 // Expert of grouped row r: the e with offsets[e] <= r < offsets[e+1] (binary search).
 MOE_DEVICE int expert_of_row(const int32_t* offsets, int E, int r) {
   int lo = 0, hi = E - 1;
@@ -137,7 +159,12 @@ __global__ void __launch_bounds__(256) simt_gateup_kernel(FfnWeights w, const ui
   if (e >= 0) {
     for (int F = warp; F < w.f; F += 8) {
       float g, u;
-      if (w.fp4) {
+      if (w.fp4 && w.fp4_tiled) {
+        const uint8_t* blocks = static_cast<const uint8_t*>(w.w_gu) +
+                                (static_cast<size_t>(e) * (w.f / 64) + F / 64) * (w.d / 64) * kFp4BlockBytes;
+        g = warp_dot_fp4_tiled(act, blocks, gu_tile_row(F, 0), w.d, lane);
+        u = warp_dot_fp4_tiled(act, blocks, gu_tile_row(F, 1), w.d, lane);
+      } else if (w.fp4) {
         const uint8_t* c = static_cast<const uint8_t*>(w.w_gu) + static_cast<size_t>(e) * 2 * w.f * (w.d / 2);
         const uint8_t* s = w.s_gu + static_cast<size_t>(e) * 2 * w.f * (w.d / 32);
         g = warp_dot_fp4(act, c + static_cast<size_t>(gu_row(F, 0)) * (w.d / 2), s + static_cast<size_t>(gu_row(F, 0)) * (w.d / 32), w.d, lane);
@@ -201,7 +228,11 @@ __global__ void __launch_bounds__(256) simt_down_kernel(FfnWeights w, int T, con
     __syncthreads();
     for (int n = warp; n < w.d; n += 8) {
       float v;
-      if (w.fp4) {
+      if (w.fp4 && w.fp4_tiled) {
+        const uint8_t* blocks = static_cast<const uint8_t*>(w.w_down) +
+                                (static_cast<size_t>(e) * (w.d / 128) + n / 128) * (w.f / 64) * kFp4BlockBytes;
+        v = warp_dot_fp4_tiled(act, blocks, n & 127, w.f, lane);
+      } else if (w.fp4) {
         const uint8_t* c = static_cast<const uint8_t*>(w.w_down) + (static_cast<size_t>(e) * w.d + n) * (w.f / 2);
         const uint8_t* s = w.s_down + (static_cast<size_t>(e) * w.d + n) * (w.f / 32);
         v = warp_dot_fp4(act, c, s, w.f, lane);

@@ -1,0 +1,449 @@
+// Grouped expert GEMMs with block-scaled 4-bit weights on the tensor cores (sm_103a).
+//
+// Same grouped problem, units and epilogues as gemm_tc.cu (swap-AB: 128 weight rows as M, the
+// segment's tokens as N <= 128), for routed experts whose weights are e2m1 codes with one e8m0
+// scale per 32 K elements (OCP MX v1.0; the "moe-prefill-quantum" page's hardware check and
+// the Jetson page's model are MXFP4).  The weights are dequantised in the kernel:
+//
+//   raw 4-bit blocks (4352 B per 128 x 64 tile chunk) --bulk copy--> shared memory
+//   --4 dequant warps, one TMEM lane quarter each: cvt.rn.f16x2.e2m1x2, times the block scale
+//     (one HMUL2, exact in fp16 for the scale range checked at set-up)--> TMEM (tcgen05.st)
+//   --tcgen05.mma kind::f16 with A read from TMEM, B (fp16 token / hidden rows) from shared
+//     memory--> fp32 accumulator in TMEM --> the same SwiGLU / down epilogues.
+//
+// The dequantised tile never touches shared memory: shared-memory traffic per weight byte stays
+// close to the 16-bit kernel's, and the weights -- 4.25 bits each -- stream from HBM once.
+// Activations are fp16 (x converted once per step; h is fp16 already), matching the fp16 A.
+//
+// Roles: warp 0 raw producer; warp 1 TMEM owner and MMA issuer; warps 2-5 epilogue; gate/up:
+// warps 6-9 gather the fp16 token rows (cp.async), warps 10-13 dequantise; down: warp 6 loads
+// rows of h by TMA, warps 7-10 dequantise.  Every wait is bounded (common.cuh).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace fq {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kStagesRaw = 8;                    // 4-bit blocks in shared memory
+constexpr int kStagesA = 4;                      // dequantised A tiles in TMEM
+constexpr int kStagesB = 6;                      // activation rows in shared memory
+constexpr int kLag = 2;                          // gather completion lag (stages), < kStagesB
+constexpr int kBBytes = kSegRowsMax * BK * 2;    // 16 KB
+constexpr int kAccCols = kSegRowsMax;            // 128 fp32 columns per accumulator
+constexpr int kACols = BK / 2;                   // 32 columns (fp16 pairs) per A stage
+constexpr int kAStart = 2 * kAccCols;            // A stages after the two accumulators
+constexpr int kTmemCols = 512;                   // 256 accumulator + 128 A columns, rounded up
+constexpr int kSmemBytes = kStagesB * kBBytes + kStagesRaw * kFp4BlockBytes + 1024 + 1024;
+constexpr int kGatherThreads = 128;
+
+MOE_DEVICE int pad16(int rows) { return rows <= 16 ? 16 : ((rows + 15) & ~15); }
+
+struct Unit {
+  int expert, row_start, rows, tile;
+};
+
+// Routed units only; the parts of one expert are tile-major (see gemm_tc.cu).
+MOE_DEVICE Unit decode_unit(int u, const Seg* segs, int tiles) {
+  const Seg any = segs[u / tiles];
+  const int o = u - any.first * tiles;
+  const Seg s = segs[any.first + o % any.nparts];
+  return Unit{s.expert, s.row_start, s.rows, o / any.nparts};
+}
+
+// e8m0 scale byte -> fp16 2^(s-127) for s in [kFp4ScaleMin, kFp4ScaleMax] (subnormal below 2^-14).
+MOE_DEVICE uint32_t scale_half2(uint32_t s) {
+  const int e = static_cast<int>(s) - 127;
+  const uint32_t h = e >= -14 ? static_cast<uint32_t>(e + 15) << 10 : 1u << (e + 24);
+  return h | (h << 16);
+}
+
+// 16 code bytes (32 e2m1 values, element 2i in the low nibble of byte i) -> 16 fp16x2 words times
+// the scale: word j holds elements (2j, 2j+1) in its (low, high) halves.
+MOE_DEVICE void dequant16(const uint4 c, uint32_t sc2, uint32_t* w) {
+  const uint32_t src[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t h0, h1, h2, h3;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+        : "r"(src[i]));
+    const uint32_t hv[4] = {h0, h1, h2, h3};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t o;
+      asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o) : "r"(hv[q]), "r"(sc2));
+      w[4 * i + q] = o;
+    }
+  }
+}
+
+MOE_DEVICE void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+MOE_DEVICE void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16.
+MOE_DEVICE void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+template <bool kGateUp>
+__global__ void __launch_bounds__(kGateUp ? 448 : 352, 1)
+    fp4_ffn_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
+  constexpr int kDqWarp = kGateUp ? 10 : 7;  // first dequant warp
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring_b = smem;                                  // kStagesB x 16 KB, 1024-aligned
+  uint8_t* ring_raw = smem + kStagesB * kBBytes;           // kStagesRaw x 4352 B
+  uint64_t* raw_full = reinterpret_cast<uint64_t*>(ring_raw + kStagesRaw * kFp4BlockBytes);
+  uint64_t* raw_empty = raw_full + kStagesRaw;
+  uint64_t* a_full = raw_empty + kStagesRaw;
+  uint64_t* a_empty = a_full + kStagesA;
+  uint64_t* b_full = a_empty + kStagesA;
+  uint64_t* b_empty = b_full + kStagesB;
+  uint64_t* acc_full = b_empty + kStagesB;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStagesRaw; ++s) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], 4);
+    }
+    for (int s = 0; s < kStagesA; ++s) {
+      mbar_init(&a_full[s], 4);
+      mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < kStagesB; ++s) {
+      mbar_init(&b_full[s], kGateUp ? kGatherThreads : 1);
+      mbar_init(&b_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (!kGateUp && warp == 6 && lane == 0) tma_prefetch_map(&maps.h);
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+  pdl_wait();
+
+  const int tiles = kGateUp ? a.f / 64 : a.d / BM;
+  const int nk = kGateUp ? a.d / BK : a.f / BK;
+  const int total_units = (*a.n_segs) * tiles;
+  const uint8_t* wq = kGateUp ? a.q_gu : a.q_down;
+
+  if (warp == 0) {
+    // ---------------- raw 4-bit blocks: one bulk copy per stage ----------------
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first();
+      uint32_t g = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
+        const Unit un = decode_unit(u, a.segs, tiles);
+        const uint8_t* w0 = wq + (static_cast<size_t>(un.expert) * tiles + un.tile) * nk * kFp4BlockBytes;
+        for (int kk = 0; kk < nk; ++kk, ++g) {
+          const int slot = g % kStagesRaw;
+          if (!mbar_wait(&raw_empty[slot], ((g / kStagesRaw) & 1u) ^ 1u, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&raw_full[slot], kFp4BlockBytes);
+          bulk_load(ring_raw + slot * kFp4BlockBytes, w0 + static_cast<size_t>(kk) * kFp4BlockBytes, kFp4BlockBytes,
+                    &raw_full[slot], pol_w);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (A from TMEM) ----------------
+    if (lane == 0) {
+      uint32_t g = 0, j = 0;
+      for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x, ++j) {
+        const Unit un = decode_unit(u, a.segs, tiles);
+        const uint32_t N = static_cast<uint32_t>(pad16(un.rows));
+        const uint32_t buf = j & 1u, use_acc = j >> 1;
+        if (!mbar_wait(&acc_empty[buf], (use_acc & 1u) ^ 1u, abort_flag, a.err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + buf * kAccCols;
+        const uint32_t idesc = idesc_f16_f32(BM, N);
+        bool ok = true;
+        for (int kk = 0; kk < nk; ++kk, ++g) {
+          const int sa = g % kStagesA, sb = g % kStagesB;
+          if (!mbar_wait(&a_full[sa], (g / kStagesA) & 1u, abort_flag, a.err) ||
+              !mbar_wait(&b_full[sb], (g / kStagesB) & 1u, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_tmem = tmem + kAStart + sa * kACols;
+          const uint64_t bdesc = smem_desc_sw128(smem_u32(ring_b + sb * kBBytes));
+#pragma unroll
+          for (int ks = 0; ks < BK / 16; ++ks)  // K = 16 per MMA: 8 TMEM columns of A, +32 B of B
+            mma_f16_ts(d_tmem, a_tmem + 8 * ks, bdesc + 2 * ks, idesc, (kk | ks) != 0);
+          mma_commit(&a_empty[sa]);
+          mma_commit(&b_empty[sb]);
+        }
+        if (!ok) break;
+        mma_commit(&acc_full[buf]);
+      }
+      mma_commit(drain);
+      mbar_wait(drain, 0, nullptr, a.err);
+    }
+  } else if (warp < 6) {
+    // ---------------- epilogue (as in gemm_tc.cu) ----------------
+    const int q = warp & 3;
+    uint32_t j = 0;
+    for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x, ++j) {
+      const Unit un = decode_unit(u, a.segs, tiles);
+      const uint32_t buf = j & 1u, use_acc = j >> 1;
+      if (!mbar_wait(&acc_full[buf], use_acc & 1u, abort_flag, a.err)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * kAccCols;
+      const int L = 32 * q + lane;
+      bool sat = false;
+      if (kGateUp) {
+        const int w16 = L & 15;
+        const bool is_gate = w16 < 8;
+        const int feat = un.tile * 64 + 8 * (L >> 4) + (w16 & 7);
+        for (int c0 = 0; c0 < un.rows; c0 += 16) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(tbase + c0, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const uint32_t send = is_gate ? r[2 * jj + 1] : r[2 * jj];
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 8);
+            const int col = c0 + 2 * jj + (is_gate ? 0 : 1);
+            const float gv = __uint_as_float(is_gate ? r[2 * jj] : recv);
+            const float uv = __uint_as_float(is_gate ? recv : r[2 * jj + 1]);
+            if (col < un.rows) {
+              float hv = swiglu(gv, uv);
+              if (!(fabsf(hv) <= kF16Max)) {
+                sat = true;
+                hv = fminf(fmaxf(hv, -kF16Max), kF16Max);
+              }
+              a.h[static_cast<size_t>(un.row_start + col) * a.f + feat] = f32_to_f16_bits_rn(hv);
+            }
+          }
+        }
+      } else {
+        const int feat = un.tile * BM + L;
+        for (int c0 = 0; c0 < un.rows; c0 += 16) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(tbase + c0, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            if (c0 + c < un.rows) {
+              float v = __uint_as_float(r[c]);
+              if (!(fabsf(v) <= kF16Max)) {
+                sat = true;
+                v = fminf(fmaxf(v, -kF16Max), kF16Max);
+              }
+              a.y[static_cast<size_t>(un.row_start + c0 + c) * a.d + feat] = f32_to_f16_bits_rn(v);
+            }
+          }
+        }
+      }
+      if (__any_sync(0xffffffffu, sat) && lane == 0) set_error(a.err, MOE_DEVERR_RANGE);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+  } else if (warp >= kDqWarp) {
+    // ---------------- dequantisation into TMEM ----------------
+    const int q = warp & 3;   // TMEM lane quarter
+    const int r = 32 * q + lane;  // weight row of the tile owned by this thread
+    uint32_t g = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
+      for (int kk = 0; kk < nk; ++kk, ++g) {
+        const int sr = g % kStagesRaw, sa = g % kStagesA;
+        if (!mbar_wait(&raw_full[sr], (g / kStagesRaw) & 1u, abort_flag, a.err) ||
+            !mbar_wait(&a_empty[sa], ((g / kStagesA) & 1u) ^ 1u, abort_flag, a.err)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* blk = ring_raw + sr * kFp4BlockBytes;
+        const uint4 c0 = *reinterpret_cast<const uint4*>(blk + r * 16);
+        const uint4 c1 = *reinterpret_cast<const uint4*>(blk + 2048 + r * 16);
+        const uint32_t sc = *reinterpret_cast<const uint16_t*>(blk + 4096 + 2 * r);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&raw_empty[sr]);  // raw bytes are in registers now
+        uint32_t w[32];
+        dequant16(c0, scale_half2(sc & 0xFFu), w);
+        dequant16(c1, scale_half2(sc >> 8), w + 16);
+        tmem_st_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + kAStart + sa * kACols, w);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[sa]);
+      }
+    }
+  } else if (!kGateUp) {
+    // ---------------- B producer (down): rows of h by TMA ----------------
+    if (warp == 6 && lane == 0) {
+      const uint64_t pol_act = l2_policy_evict_last();
+      uint32_t g = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
+        const Unit un = decode_unit(u, a.segs, tiles);
+        const int nbox = (pad16(un.rows) + 31) / 32;
+        for (int kk = 0; kk < nk; ++kk, ++g) {
+          const int slot = g % kStagesB;
+          if (!mbar_wait(&b_empty[slot], ((g / kStagesB) & 1u) ^ 1u, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&b_full[slot], nbox * 32 * BK * 2);
+          for (int i = 0; i < nbox; ++i)
+            tma_load_2d(ring_b + slot * kBBytes + i * 32 * BK * 2, &maps.h, &b_full[slot], kk * BK,
+                        un.row_start + 32 * i, pol_act);
+        }
+      }
+    }
+  } else {
+    // ---------------- B producer (gate/up): fp16 token rows gathered with cp.async ----------
+    const int p = threadIdx.x - 192;  // 0..127
+    const int ch = p & 7, r0 = p >> 3;
+    const uint64_t pol_x = l2_policy_evict_last();
+    uint32_t g = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
+      const Unit un = decode_unit(u, a.segs, tiles);
+      const uint16_t* src[kSegRowsMax / 16];
+#pragma unroll
+      for (int i = 0; i < kSegRowsMax / 16; ++i) {
+        const int n = r0 + 16 * i;
+        src[i] = nullptr;
+        if (n < un.rows) src[i] = a.x16 + static_cast<size_t>(a.perm[un.row_start + n] / a.k) * a.d + ch * 8;
+      }
+      for (int kk = 0; kk < nk; ++kk, ++g) {
+        const int slot = g % kStagesB;
+        if (!mbar_wait(&b_empty[slot], ((g / kStagesB) & 1u) ^ 1u, abort_flag, a.err)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sb = smem_u32(ring_b + slot * kBBytes);
+#pragma unroll
+        for (int i = 0; i < kSegRowsMax / 16; ++i) {
+          const int n = r0 + 16 * i;
+          if (src[i]) cp_async_16_hint(sb + n * 128 + ((ch ^ (n & 7)) << 4), src[i] + kk * BK, pol_x);
+        }
+        cp_async_commit();
+        if (g >= kLag) {
+          cp_async_wait<kLag>();
+          fence_proxy_async_smem();
+          mbar_arrive(&b_full[(g - kLag) % kStagesB]);
+        }
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    if (ok && !*abort_flag) {
+      const uint32_t first = g >= kLag ? g - kLag : 0;
+      for (uint32_t s = first; s < g; ++s) mbar_arrive(&b_full[s % kStagesB]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace fq
+
+static bool g_fq_attr[2] = {false, false};
+
+template <bool kGateUp>
+static cudaError_t launch_fq(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st) {
+  auto kern = fq::fp4_ffn_kernel<kGateUp>;
+  if (!g_fq_attr[kGateUp]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, fq::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    g_fq_attr[kGateUp] = true;
+  }
+  return launch_pdl(kern, dim3(num_sms), dim3(kGateUp ? 448 : 352), fq::kSmemBytes, st, *maps, a);
+}
+
+cudaError_t launch_fp4_gateup(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st) {
+  return launch_fq<true>(maps, a, num_sms, st);
+}
+
+cudaError_t launch_fp4_down(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st) {
+  return launch_fq<false>(maps, a, num_sms, st);
+}
+
+// x (bf16) -> fp16 for the 4-bit path's B operand; exact for 2^-17 <= |x| <= 65504 (and 0),
+// larger magnitudes are clamped and flag MOE_DEVERR_RANGE.
+__global__ void __launch_bounds__(256) x_to_f16_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ x16,
+                                                       size_t n8, uint32_t* err) {
+  pdl_trigger();
+  pdl_wait();
+  bool sat = false;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const uint4 v = reinterpret_cast<const uint4*>(x)[i];
+    float f[8];
+    bf16x8_to_f32(v, f);
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float lo = f[2 * q], hi = f[2 * q + 1];
+      if (!(fabsf(lo) <= kF16Max) || !(fabsf(hi) <= kF16Max)) {
+        sat = true;
+        lo = fminf(fmaxf(lo, -kF16Max), kF16Max);
+        hi = fminf(fmaxf(hi, -kF16Max), kF16Max);
+      }
+      o[q] = static_cast<uint32_t>(f32_to_f16_bits_rn(lo)) | (static_cast<uint32_t>(f32_to_f16_bits_rn(hi)) << 16);
+    }
+    reinterpret_cast<uint4*>(x16)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (sat) set_error(err, MOE_DEVERR_RANGE);
+}
+
+cudaError_t launch_x_to_f16(const uint16_t* x, uint16_t* x16, size_t n, uint32_t* err, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  const size_t n8 = n / 8;
+  const int blocks = static_cast<int>(n8 / 256 + 1 < 1024 ? n8 / 256 + 1 : 1024);
+  return launch_pdl(x_to_f16_kernel, dim3(blocks), dim3(256), 0, st, x, x16, n8, err);
+}
+
+}  // namespace moe

@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kGateUp ? 320 : 192, 1)
   const int tiles_r = kGateUp ? a.f / 64 : a.d / BM;
   const int tiles_s = kGateUp ? (a.n_shared * a.f_s) / 64 : a.d / BM;
   const int n_shared_units = a.n_shared ? a.n_shared_segs * tiles_s : 0;
-  const int n_routed_units = (*a.n_segs) * tiles_r;
+  const int n_routed_units = a.routed ? (*a.n_segs) * tiles_r : 0;
   const int total_units = n_shared_units + n_routed_units;
   const int nk_r = kGateUp ? a.d / BK : a.f / BK;
   const int nk_s = kGateUp ? a.d / BK : (a.n_shared * a.f_s) / BK;

@@ -77,8 +77,9 @@ struct FfnWeights {
   int f_s = 0;
   int E = 0, k = 0, d = 0, f = 0;
   uint32_t* err = nullptr;
-  // 1: bf16 routed / shared weights are in the tile-contiguous layouts of the tensor-core path
-  int tiled = 0, tiled_s = 0;
+  // 1: bf16 routed / shared weights are in the tile-contiguous layouts of the tensor-core path;
+  // fp4_tiled: 4-bit routed weights in the launch_tile_fp4 layout (scales inside the blocks)
+  int tiled = 0, tiled_s = 0, fp4_tiled = 0;
 };
 
 // h, h_s, y, y_s are fp16.
@@ -98,6 +99,11 @@ struct TcArgs {
   const uint16_t* w_gu_s = nullptr;  // [n_s*f_s/64][d/64] blocks, bf16
   const uint16_t* w_down = nullptr;  // [E][d/128][f/64] blocks, fp16
   const uint16_t* w_down_s = nullptr;  // [d/128][n_s][f_s/64] blocks, fp16
+  // 4-bit routed weights (launch_tile_fp4 layout) for the fp4 kernels
+  const uint8_t* q_gu = nullptr;     // [E][f/64][d/64] blocks of kFp4BlockBytes
+  const uint8_t* q_down = nullptr;   // [E][d/128][f/64] blocks
+  const uint16_t* x16 = nullptr;     // fp16 copy of x (4-bit path's B operand)
+  int routed = 1;                    // 0: the 16-bit kernels run the shared-expert units only
   const Seg* segs = nullptr;
   const int32_t* n_segs = nullptr;
   const int32_t* perm = nullptr;
@@ -113,6 +119,13 @@ struct TcArgs {
 
 cudaError_t launch_tc_gateup(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_tc_down(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st);
+
+// ---- expert FFN with 4-bit routed weights, tcgen05 (gemm_fp4.cu) -----------------------------
+// Routed units only (shared experts go through the 16-bit kernels with routed = 0).
+cudaError_t launch_fp4_gateup(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_fp4_down(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st);
+// x16 = fp16(x), n elements (multiple of 8); out-of-range values clamp and flag MOE_DEVERR_RANGE.
+cudaError_t launch_x_to_f16(const uint16_t* x, uint16_t* x16, size_t n, uint32_t* err, cudaStream_t st);
 
 // ---- combine (combine.cu): y and shared_y fp16, out bf16 ----------------------------------------
 cudaError_t launch_combine(const uint16_t* y, const float* gates, const int32_t* inv,
@@ -133,6 +146,15 @@ cudaError_t launch_tile_gate_up(const uint16_t* gate, const uint16_t* up, uint16
 cudaError_t launch_tile_down(const uint16_t* src, uint16_t* dst, int n, int rows, int K, int by_matrix, uint32_t* bad,
                              cudaStream_t st);
 constexpr int kTileElems = 128 * 64;
+// 4-bit tile-contiguous blocks (launch_tile_fp4): 128 rows x 64 K elements, codes then scales.
+constexpr int kFp4BlockBytes = 4096 + 256;
+// e8m0 scale bytes for which e2m1 x 2^(s-127) is exact in fp16 (subnormals included): the
+// tensor-core 4-bit path dequantises into fp16.
+constexpr int kFp4ScaleMin = 104;
+constexpr int kFp4ScaleMax = 140;
+cudaError_t launch_tile_fp4(const uint8_t* codes_a, const uint8_t* scales_a, const uint8_t* codes_b,
+                            const uint8_t* scales_b, uint8_t* dst, int n, int rows, int K, int gate_up,
+                            uint32_t* scale_oor, cudaStream_t st);
 // Element offset of (row r, K element kk) inside one 128 x 64 block (128-byte swizzle).
 __host__ __device__ inline size_t tile_elem_offset(int r, int kk) {
   return static_cast<size_t>(r) * 64 + ((((kk >> 3) ^ (r & 7)) << 3) | (kk & 7));

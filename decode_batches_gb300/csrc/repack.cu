@@ -134,4 +134,66 @@ cudaError_t launch_tile_down(const uint16_t* src, uint16_t* dst, int n, int rows
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------------------------
+// 4-bit weights: one block per (matrix, 128-row tile, 64-K chunk), kFp4BlockBytes = 4352 bytes:
+//   [0, 2048)     codes of K elements 0..31 of the chunk, row r at r * 16
+//   [2048, 4096)  codes of K elements 32..63, row r at 2048 + r * 16
+//   [4096, 4352)  e8m0 scales, row r at 4096 + 2 r (+0: elements 0..31, +1: 32..63)
+// so that a thread owning one row reads its 16-byte halves without bank conflicts.  Gate/up rows
+// are interleaved by 8 as in the 16-bit layout.  *scale_oor gets 1 if a scale byte lies outside
+// [kFp4ScaleMin, kFp4ScaleMax], where the fp16 dequantisation would not be exact.
+// ---------------------------------------------------------------------------------------------
+__global__ void tile_fp4_kernel(const uint8_t* __restrict__ codes_a, const uint8_t* __restrict__ scales_a,
+                                const uint8_t* __restrict__ codes_b, const uint8_t* __restrict__ scales_b,
+                                uint8_t* __restrict__ dst, int rows, int K, int gate_up, size_t n_rows_total,
+                                uint32_t* scale_oor) {
+  const int nk = K / 64;
+  const int tiles = gate_up ? rows / 64 : rows / 128;  // gate/up: 64 features per tile
+  bool oor = false;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n_rows_total;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    // work item i: block b = i / 128, row r = i % 128
+    const size_t b = i >> 7;
+    const int r = static_cast<int>(i & 127);
+    const int kc = static_cast<int>(b % nk);
+    const size_t mt = b / nk;
+    const int t = static_cast<int>(mt % tiles);
+    const size_t m = mt / tiles;
+    const uint8_t* codes;
+    const uint8_t* scales;
+    size_t src_row;
+    if (gate_up) {
+      const int F = 64 * t + 8 * (r >> 4) + (r & 7);
+      const bool up = (r & 15) >= 8;
+      codes = up ? codes_b : codes_a;
+      scales = up ? scales_b : scales_a;
+      src_row = m * rows + F;
+    } else {
+      codes = codes_a;
+      scales = scales_a;
+      src_row = m * rows + 128 * t + r;
+    }
+    const uint8_t* c = codes + src_row * (K / 2) + kc * 32;
+    const uint8_t* sc = scales + src_row * (K / 32) + kc * 2;
+    uint8_t* blk = dst + b * kFp4BlockBytes;
+    *reinterpret_cast<uint4*>(blk + r * 16) = *reinterpret_cast<const uint4*>(c);
+    *reinterpret_cast<uint4*>(blk + 2048 + r * 16) = *reinterpret_cast<const uint4*>(c + 16);
+    blk[4096 + 2 * r] = sc[0];
+    blk[4096 + 2 * r + 1] = sc[1];
+    if (sc[0] < kFp4ScaleMin || sc[0] > kFp4ScaleMax || sc[1] < kFp4ScaleMin || sc[1] > kFp4ScaleMax) oor = true;
+  }
+  if (oor) atomicOr(scale_oor, 1u);
+}
+
+cudaError_t launch_tile_fp4(const uint8_t* codes_a, const uint8_t* scales_a, const uint8_t* codes_b,
+                            const uint8_t* scales_b, uint8_t* dst, int n, int rows, int K, int gate_up,
+                            uint32_t* scale_oor, cudaStream_t st) {
+  // gate/up: n experts x (2 * rows) interleaved rows; down: n matrices x rows rows
+  const size_t total_rows = static_cast<size_t>(n) * (gate_up ? 2 * rows : rows) * (K / 64);
+  if (total_rows == 0) return cudaSuccess;
+  tile_fp4_kernel<<<2048, 256, 0, st>>>(codes_a, scales_a, codes_b, scales_b, dst, rows, K, gate_up, total_rows,
+                                        scale_oor);
+  return cudaGetLastError();
+}
+
 }  // namespace moe

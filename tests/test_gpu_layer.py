@@ -35,7 +35,7 @@ def plan_for(spec):
 
 
 def paths_for(spec):
-    return ["simt", "tc"] if spec.wdtype == "bf16" else ["simt"]
+    return ["simt", "tc"]
 
 
 def _cases(lst):
@@ -194,3 +194,49 @@ def test_untiled_shape_runs_the_reference_path():
     _, ids, _ = plan.route(x, want_logits=False)
     compare_layer(out, oracle_layer(w), spec.k, TOL_BF16, ids.cpu().numpy())
     assert plan.device_error() == 0
+
+
+FP4_SMALL = synth.LayerSpec(E=16, k=4, d=256, f=128, n_shared=1, f_s=128, wdtype="mxfp4")
+
+
+@pytest.mark.parametrize("path", ["simt", "tc"])
+@pytest.mark.parametrize("T", [1, 77, 300])
+def test_fp4_small_layer_both_paths(T, path):
+    """4-bit routed weights (dequantised in-kernel) with a bf16 shared expert, every token."""
+    w = synth.custom(FP4_SMALL, T, n_prefill=T - 1, name=f"fp4small{T}")
+    plan = make_plan(w)
+    plan.set_path(path)
+    x = to_dev(w.x(), "bf16")
+    out = bf16_tensor_to_f64(plan.forward(x, n_prefill=w.n_prefill))
+    _, ids, _ = plan.route(x, want_logits=False)
+    ref = oracle_layer(w)
+    compare_layer(out, ref, FP4_SMALL.k, TOL_FP4, ids.cpu().numpy())
+    y, ys = plan.experts(x, to_dev(ref["offsets"]), to_dev(ref["perm"]))
+    rms = np.sqrt(np.mean(ref["y_perm"] ** 2))
+    assert np.abs(y.double().cpu().numpy() - ref["y_perm"]).max() <= TOL_FP4 * rms
+    assert plan.device_error() == 0
+
+
+def test_fp4_scales_outside_fp16_range_use_the_reference_path():
+    """A scale whose e2m1 multiples are not exact in fp16 keeps the tensor-core path off; the
+    CUDA-core path reads the same tiled layout and still matches the oracle."""
+    from decode_batches_gb300 import MoeError, MoePlan
+    w = synth.custom(FP4_SMALL, 40, n_prefill=40, name="fp4oor")
+    ex = w.experts()
+    gs = ex.gate_scale.copy()
+    gs[3, 5, 2] = 100            # 2^-27: below the fp16-exact range
+    ex.gate_scale = gs
+    s = w.spec
+    plan = MoePlan(s.E, s.k, s.d, s.f, s.n_shared, s.wdtype)
+    plan.set_weights(to_dev(w.router_weight()), None, to_dev(ex.gate), to_dev(ex.up), to_dev(ex.down),
+                     to_dev(gs), to_dev(ex.up_scale), to_dev(ex.down_scale))
+    sh = w.shared()
+    plan.set_shared(s.f_s, to_dev(sh[0], "bf16"), to_dev(sh[1], "bf16"), to_dev(sh[2], "bf16"))
+    plan.allocate_workspace(w.T)
+    with pytest.raises(MoeError):
+        plan.set_path("tc")
+    x = to_dev(w.x(), "bf16")
+    out = bf16_tensor_to_f64(plan.forward(x, n_prefill=w.n_prefill))
+    ref = oracle.moe_layer(w.x(), w.router_weight(), None, s.k,
+                           oracle.DecodedExperts(ex.gate, ex.up, ex.down, gs, ex.up_scale, ex.down_scale), sh)
+    compare_layer(out, ref, s.k, TOL_FP4)
