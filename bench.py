@@ -159,6 +159,28 @@ def layer_bytes_flops(w: synth.Workload, counts: np.ndarray) -> dict:
             "weight_bytes": touched * expert + shared}
 
 
+def kernel_alg_bytes(name: str, w: synth.Workload, counts: np.ndarray):
+    """Algorithmic bytes of one launch of the named kernel (compulsory reads + writes)."""
+    s = w.spec
+    touched = int((counts > 0).sum())
+    wb = 2.0 if s.wdtype == "bf16" else 0.5 + 1.0 / 32.0
+    R = w.T * s.k
+    h_r, h_s = R * s.f * 2.0, w.T * s.n_shared * s.f_s * 2.0
+    y_r, y_s = R * s.d * 2.0, (w.T * s.d * 2.0 if s.n_shared else 0.0)
+    sh_gu, sh_dn = 2.0 * s.d * s.f_s * 2.0 * s.n_shared, s.d * s.f_s * 2.0 * s.n_shared
+    x = w.T * s.d * 2.0
+    table = {
+        "tc_gateup": touched * 2.0 * s.d * s.f * wb + sh_gu + x + h_r + h_s,
+        "tc_down": touched * s.d * s.f * wb + sh_dn + h_r + h_s + y_r + y_s,
+        "fp4_gateup": touched * 2.0 * s.d * s.f * wb + x + h_r,
+        "fp4_down": touched * s.d * s.f * wb + h_r + y_r,
+        "tc_gateup_shared": sh_gu + x + h_s,
+        "tc_down_shared": sh_dn + h_s + y_s,
+        "combine": y_r + y_s + x + R * 8.0,
+    }
+    return table.get(name)
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_batches_gb300", "csrc")
@@ -323,12 +345,9 @@ def run_gpu(args):
     if dom:
         name, (n, tot_ms) = dom
         per_launch_s = tot_ms / n * 1e-3
-        if name == "tc_gateup":
-            alg, bound = bf["gateup_bytes"], "hbm"
-        elif name == "tc_down":
-            alg, bound = bf["down_bytes"], "hbm"
-        else:
-            alg, bound = bf["bytes"], "hbm"
+        alg, bound = kernel_alg_bytes(name, w, counts), "hbm"
+        if alg is None:
+            alg = bf["bytes"]
         achieved = alg / per_launch_s / 1e9
         tr = committed_traffic(name)
         roofline = {"bound": bound, "kernel": name, "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
@@ -354,6 +373,22 @@ def run_gpu(args):
                       "roofline_frac": round(tq / (msq * 1e-3), 4),
                       "bound": "hbm" if bq["bytes"] / (hbm * 1e9) >= bq["flops"] / (tflops * 1e12) else "tensor",
                       "kernel_us": {k: round(v[1] / v[0] * 1e3, 2) for k, v in kq.items()}})
+
+    extra = {}
+    if not args.no_extra and args.workload == "mixed":
+        # the other configurations of the layer: 4-token decode on the same plan; the 4-bit Zipf
+        # step and the 6-row verify batch on a 384-expert 4-bit plan
+        extra["decode_T4"] = measure_workload(plan, synth.workload("decode", seed=rank_seed(0, rank) if world > 1 else 0),
+                                              hbm, tflops, world, args)
+        del plan
+        torch.cuda.empty_cache()
+        fp4_plan = upload_plan(synth.workload("fp4_zipf", seed=0), 2051)
+        extra["fp4_zipf_T2051"] = measure_workload(fp4_plan, synth.workload("fp4_zipf", seed=rank_seed(0, rank) if world > 1 else 0),
+                                                   hbm, tflops, world, args)
+        extra["verify_8x6_T48"] = measure_workload(fp4_plan, synth.workload("verify", seed=rank_seed(0, rank) if world > 1 else 0),
+                                                   hbm, tflops, world, args, committed=(48, 8))
+        del fp4_plan
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -385,6 +420,7 @@ def run_gpu(args):
         "launches_per_step": launches_per_step,
         "clocks": clk,
         "sweep": sweep,
+        "workloads": extra,
         "cpu_baseline": cpu,
     }
     if rank == 0:
@@ -393,6 +429,27 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.barrier()
         dist.destroy_process_group()
+
+
+def measure_workload(plan, w: synth.Workload, hbm: float, tflops: float, world: int, args, committed=None) -> dict:
+    """tokens/s, roofline and per-kernel times of one more workload on an uploaded plan."""
+    import torch
+    x = torch.from_numpy(np.ascontiguousarray(w.x())).cuda().view(torch.bfloat16)
+    counts = routing_counts(plan, x)
+    b = layer_bytes_flops(w, counts)
+    steps = max(50, min(args.steps, 1000))
+    ms, _, _ = time_forward(plan, x, w.n_prefill, steps, max(3, args.warmup), world)
+    _, k, _ = time_forward(plan, x, w.n_prefill, max(20, steps // 4), 3, world, timing=True)
+    t_hbm, t_tc = b["bytes"] / (hbm * 1e9), b["flops"] / (tflops * 1e12)
+    out = {"workload": workload_desc(w), "T": w.T, "tokens_per_s": round(world * w.T / (ms * 1e-3), 1),
+           "ms_per_step": round(ms, 5), "touched_experts": b["touched"], "alg_bytes": b["bytes"], "flops": b["flops"],
+           "bound": "hbm" if t_hbm >= t_tc else "tensor", "roofline_frac": round(max(t_hbm, t_tc) / (ms * 1e-3), 4),
+           "hbm_frac": round(b["bytes"] / (ms * 1e-3) / (hbm * 1e9), 4), "launches_per_step": plan.last_launch_count(),
+           "kernel_us": {n: round(v[1] / v[0] * 1e3, 2) for n, v in k.items()}}
+    if committed:
+        # weight bytes streamed per committed token: every verify row accepted / one per sequence
+        out["weight_bytes_per_committed_token"] = {f"{c}_committed": round(b["weight_bytes"] / c, 1) for c in committed}
+    return out
 
 
 def workload_desc(w: synth.Workload) -> str:
@@ -486,6 +543,7 @@ def main(argv=None):
     ap.add_argument("--quantum", type=int, default=2048)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the decode, 4-bit and verify workloads")
     ap.add_argument("--cpu-sample", type=int, default=256)
     ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--sample", type=int, default=256, help=argparse.SUPPRESS)
