@@ -120,6 +120,38 @@ MOE_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_fl
   }
 }
 
+// Non-blocking probe of the phase with the given parity (mbarrier.test_wait).  Issue it early
+// and consume the result late: the probe's latency then overlaps other work.
+MOE_DEVICE bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// The same wait for a whole converged warp: every lane waits, the result is warp-uniform.
+MOE_DEVICE bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint32_t* err) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, err));
+}
+
+// One lane of a converged warp (the same lane every time the full warp calls it).  Role loops
+// that issue tcgen05.mma / TMA run converged and issue under elect_one(): the operands then stay
+// warp-uniform, and a single MMA issues in a few tens of cycles instead of a few hundred.
+MOE_DEVICE bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ------------------------------------------------------------------------------------------
 // TMA (tensor maps live in kernel parameter space: __grid_constant__ const CUtensorMap)
 // ------------------------------------------------------------------------------------------

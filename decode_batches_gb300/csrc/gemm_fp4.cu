@@ -16,8 +16,12 @@
 // Activations are fp16 (x converted once per step; h is fp16 already), matching the fp16 A.
 //
 // Roles: warp 0 raw producer; warp 1 TMEM owner and MMA issuer; warps 2-5 epilogue; gate/up:
-// warps 6-9 gather the fp16 token rows (cp.async), warps 10-13 dequantise; down: warp 6 loads
-// rows of h by TMA, warps 7-10 dequantise.  Every wait is bounded (common.cuh).
+// warps 6-13 gather the fp16 token rows (cp.async), warps 14-21 dequantise; down: warp 6 loads
+// rows of h by TMA, warps 7-14 dequantise.  The dequant warps form two quartets (one warp per
+// TMEM lane quarter each) that take alternate stages.  A stage is 128 deep in K (two 4-bit
+// blocks, two 64-wide swizzled B slices, 8 MMAs), so the single-thread MMA issue -- one barrier
+// wait and one commit per stage -- keeps ahead of the weight stream.  Producer and MMA loops run
+// converged and issue under elect_one().  Every wait is bounded (common.cuh).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -25,18 +29,26 @@ namespace moe {
 namespace fq {
 
 constexpr int BM = 128;
-constexpr int BK = 64;
-constexpr int kStagesRaw = 8;                    // 4-bit blocks in shared memory
-constexpr int kStagesA = 4;                      // dequantised A tiles in TMEM
-constexpr int kStagesB = 6;                      // activation rows in shared memory
-constexpr int kLag = 2;                          // gather completion lag (stages), < kStagesB
-constexpr int kBBytes = kSegRowsMax * BK * 2;    // 16 KB
+constexpr int kSubK = 64;                        // one 128-byte-swizzled K slice / one 4-bit block
+constexpr int kSubs = 2;                         // K slices per pipeline stage (K = 128)
+constexpr int kStages = 4;                       // A (TMEM) + B (shared memory) stages, one ring
+constexpr int kStagesRaw = 8;                    // 4-bit stages in shared memory (~70 KB in flight)
+constexpr int kDqSets = 2;                       // dequant quartets; quartet s takes stages g % 2 == s
+constexpr int kSubBytes = kSegRowsMax * kSubK * 2;         // 16 KB: one K slice of up to 128 rows
+constexpr int kBBytes = kSubs * kSubBytes;                 // 32 KB per stage
+constexpr int kRawBytes = kSubs * kFp4BlockBytes;          // 8704 B per stage
 constexpr int kAccCols = kSegRowsMax;            // 128 fp32 columns per accumulator
-constexpr int kACols = BK / 2;                   // 32 columns (fp16 pairs) per A stage
+constexpr int kACols = kSubs * kSubK / 2;        // 64 columns (fp16 pairs) per A stage
 constexpr int kAStart = 2 * kAccCols;            // A stages after the two accumulators
-constexpr int kTmemCols = 512;                   // 256 accumulator + 128 A columns, rounded up
-constexpr int kSmemBytes = kStagesB * kBBytes + kStagesRaw * kFp4BlockBytes + 1024 + 1024;
-constexpr int kGatherThreads = 128;
+constexpr int kTmemCols = 512;                   // 256 accumulator + 256 A columns
+constexpr int kGatherPerSlot = 2;                // gate/up B producers per ring slot
+constexpr int kGatherWarps = kGatherPerSlot * kStages;
+constexpr int kTokBytes = kGatherWarps * kSegRowsMax * 4;  // per gather warp: token of each row
+constexpr int kSmemBytes = kStages * kBBytes + kStagesRaw * kRawBytes + 1024 + 1024 + kTokBytes;
+
+static_assert(kStagesRaw % kDqSets == 0 && kStages % kDqSets == 0, "stage rings must split evenly between quartets");
+static_assert(kAStart + kStages * kACols <= kTmemCols, "TMEM columns");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 MOE_DEVICE int pad16(int rows) { return rows <= 16 ? 16 : ((rows + 15) & ~15); }
 
@@ -107,25 +119,31 @@ MOE_DEVICE void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uin
       : "memory");
 }
 
+// Pipeline.  Stage g covers K slices [2g, 2g + 2) of the unit (the last stage of an odd K/64
+// has one).  Rings:
+//   raw[g % kStagesRaw]  4-bit blocks, filled by one bulk copy, freed by the quartet that read them
+//   A/B[g % kStages]     dequantised weights in TMEM + activation rows in shared memory; full when
+//                        the quartet (4 arrivals) and the B producer (the slot's gather warp, or
+//                        one arrive.expect_tx for TMA) are done, empty when the MMAs reading it finish.
+// The MMA warp thus waits on one barrier and commits once per 128 K.
 template <bool kGateUp>
-__global__ void __launch_bounds__(kGateUp ? 448 : 352, 1)
+__global__ void __launch_bounds__(kGateUp ? 704 : 480, 1)
     fp4_ffn_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
-  constexpr int kDqWarp = kGateUp ? 10 : 7;  // first dequant warp
+  constexpr int kDqWarp = kGateUp ? 6 + kGatherWarps : 7;  // first dequant warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ring_b = smem;                                  // kStagesB x 16 KB, 1024-aligned
-  uint8_t* ring_raw = smem + kStagesB * kBBytes;           // kStagesRaw x 4352 B
-  uint64_t* raw_full = reinterpret_cast<uint64_t*>(ring_raw + kStagesRaw * kFp4BlockBytes);
+  uint8_t* ring_b = smem;                                  // kStages x 32 KB, 1024-aligned
+  uint8_t* ring_raw = smem + kStages * kBBytes;            // kStagesRaw x 8704 B
+  uint64_t* raw_full = reinterpret_cast<uint64_t*>(ring_raw + kStagesRaw * kRawBytes);
   uint64_t* raw_empty = raw_full + kStagesRaw;
-  uint64_t* a_full = raw_empty + kStagesRaw;
-  uint64_t* a_empty = a_full + kStagesA;
-  uint64_t* b_full = a_empty + kStagesA;
-  uint64_t* b_empty = b_full + kStagesB;
-  uint64_t* acc_full = b_empty + kStagesB;
+  uint64_t* full = raw_empty + kStagesRaw;
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int32_t* tok_tab = reinterpret_cast<int32_t*>(ring_raw + kStagesRaw * kRawBytes + 1024);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -133,13 +151,9 @@ __global__ void __launch_bounds__(kGateUp ? 448 : 352, 1)
       mbar_init(&raw_full[s], 1);
       mbar_init(&raw_empty[s], 4);
     }
-    for (int s = 0; s < kStagesA; ++s) {
-      mbar_init(&a_full[s], 4);
-      mbar_init(&a_empty[s], 1);
-    }
-    for (int s = 0; s < kStagesB; ++s) {
-      mbar_init(&b_full[s], kGateUp ? kGatherThreads : 1);
-      mbar_init(&b_empty[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 4 + (kGateUp ? kGatherPerSlot : 1));  // dequant quartet + B producer(s)
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -162,66 +176,70 @@ __global__ void __launch_bounds__(kGateUp ? 448 : 352, 1)
   pdl_wait();
 
   const int tiles = kGateUp ? a.f / 64 : a.d / BM;
-  const int nk = kGateUp ? a.d / BK : a.f / BK;
+  const int nsub = (kGateUp ? a.d : a.f) / kSubK;          // K slices (4-bit blocks) per unit
+  const int nst = (nsub + kSubs - 1) / kSubs;              // stages per unit
   const int total_units = (*a.n_segs) * tiles;
   const uint8_t* wq = kGateUp ? a.q_gu : a.q_down;
 
   if (warp == 0) {
-    // ---------------- raw 4-bit blocks: one bulk copy per stage ----------------
-    if (lane == 0) {
-      const uint64_t pol_w = l2_policy_evict_first();
-      uint32_t g = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
-        const Unit un = decode_unit(u, a.segs, tiles);
-        const uint8_t* w0 = wq + (static_cast<size_t>(un.expert) * tiles + un.tile) * nk * kFp4BlockBytes;
-        for (int kk = 0; kk < nk; ++kk, ++g) {
-          const int slot = g % kStagesRaw;
-          if (!mbar_wait(&raw_empty[slot], ((g / kStagesRaw) & 1u) ^ 1u, abort_flag, a.err)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&raw_full[slot], kFp4BlockBytes);
-          bulk_load(ring_raw + slot * kFp4BlockBytes, w0 + static_cast<size_t>(kk) * kFp4BlockBytes, kFp4BlockBytes,
+    // ---------------- raw 4-bit blocks: one bulk copy per stage (the blocks are adjacent) -----
+    const uint64_t pol_w = l2_policy_evict_first();
+    uint32_t g = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+      const Unit un = decode_unit(u, a.segs, tiles);
+      const uint8_t* w0 = wq + (static_cast<size_t>(un.expert) * tiles + un.tile) * nsub * kFp4BlockBytes;
+      for (int kk = 0; kk < nst; ++kk, ++g) {
+        const int slot = g % kStagesRaw;
+        const uint32_t bytes = static_cast<uint32_t>(min(kSubs, nsub - kSubs * kk)) * kFp4BlockBytes;
+        if (!(ok = mbar_wait_warp(&raw_empty[slot], ((g / kStagesRaw) & 1u) ^ 1u, abort_flag, a.err))) break;
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&raw_full[slot], bytes);
+          bulk_load(ring_raw + slot * kRawBytes, w0 + static_cast<size_t>(kSubs * kk) * kFp4BlockBytes, bytes,
                     &raw_full[slot], pol_w);
         }
+        __syncwarp();
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer (A from TMEM) ----------------
-    if (lane == 0) {
-      uint32_t g = 0, j = 0;
-      for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x, ++j) {
-        const Unit un = decode_unit(u, a.segs, tiles);
-        const uint32_t N = static_cast<uint32_t>(pad16(un.rows));
-        const uint32_t buf = j & 1u, use_acc = j >> 1;
-        if (!mbar_wait(&acc_empty[buf], (use_acc & 1u) ^ 1u, abort_flag, a.err)) break;
+    // ---------------- MMA issuer (A from TMEM): the warp waits, one elected lane issues -------
+    uint32_t g = 0, j = 0;
+    bool ok = true, ready = false;  // ready: full[g % kStages] already seen complete for stage g
+    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++j) {
+      const Unit un = decode_unit(u, a.segs, tiles);
+      const uint32_t N = static_cast<uint32_t>(pad16(un.rows));
+      const uint32_t buf = j & 1u, use_acc = j >> 1;
+      if (!(ok = mbar_wait_warp(&acc_empty[buf], (use_acc & 1u) ^ 1u, abort_flag, a.err))) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + buf * kAccCols;
+      const uint32_t idesc = idesc_f16_f32(BM, N);
+      for (int kk = 0; kk < nst; ++kk, ++g) {
+        const int s = g % kStages;
+        if (!ready && !(ok = mbar_wait_warp(&full[s], (g / kStages) & 1u, abort_flag, a.err))) break;
+        const uint32_t gn = g + 1;  // probe the next stage now, use the answer next iteration
+        const bool next = mbar_test(&full[gn % kStages], (gn / kStages) & 1u);
         tc_fence_after();
-        const uint32_t d_tmem = tmem + buf * kAccCols;
-        const uint32_t idesc = idesc_f16_f32(BM, N);
-        bool ok = true;
-        for (int kk = 0; kk < nk; ++kk, ++g) {
-          const int sa = g % kStagesA, sb = g % kStagesB;
-          if (!mbar_wait(&a_full[sa], (g / kStagesA) & 1u, abort_flag, a.err) ||
-              !mbar_wait(&b_full[sb], (g / kStagesB) & 1u, abort_flag, a.err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_tmem = tmem + kAStart + sa * kACols;
-          const uint64_t bdesc = smem_desc_sw128(smem_u32(ring_b + sb * kBBytes));
+        const uint32_t a_tmem = tmem + kAStart + s * kACols;
+        const uint64_t bdesc = smem_desc_sw128(smem_u32(ring_b + s * kBBytes));
+        const int subs = min(kSubs, nsub - kSubs * kk);
+        if (elect_one()) {
+          for (int j2 = 0; j2 < subs; ++j2) {
 #pragma unroll
-          for (int ks = 0; ks < BK / 16; ++ks)  // K = 16 per MMA: 8 TMEM columns of A, +32 B of B
-            mma_f16_ts(d_tmem, a_tmem + 8 * ks, bdesc + 2 * ks, idesc, (kk | ks) != 0);
-          mma_commit(&a_empty[sa]);
-          mma_commit(&b_empty[sb]);
+            for (int ks = 0; ks < kSubK / 16; ++ks)  // K = 16 per MMA: 8 TMEM columns of A, +32 B of B
+              mma_f16_ts(d_tmem, a_tmem + 32 * j2 + 8 * ks, bdesc + (kSubBytes >> 4) * j2 + 2 * ks, idesc,
+                         (kk | j2 | ks) != 0);
+          }
+          mma_commit(&empty[s]);
         }
-        if (!ok) break;
-        mma_commit(&acc_full[buf]);
+        ready = __all_sync(0xffffffffu, next);
       }
-      mma_commit(drain);
-      mbar_wait(drain, 0, nullptr, a.err);
+      if (!ok) break;
+      if (elect_one()) mma_commit(&acc_full[buf]);
+      __syncwarp();
     }
+    if (elect_one()) mma_commit(drain);  // completes once every MMA issued above has finished
+    __syncwarp();
+    mbar_wait_warp(drain, 0, nullptr, a.err);
   } else if (warp < 6) {
     // ---------------- epilogue (as in gemm_tc.cu) ----------------
     const int q = warp & 3;
@@ -285,97 +303,113 @@ __global__ void __launch_bounds__(kGateUp ? 448 : 352, 1)
     }
   } else if (warp >= kDqWarp) {
     // ---------------- dequantisation into TMEM ----------------
-    const int q = warp & 3;   // TMEM lane quarter
+    const int q = warp & 3;       // TMEM lane quarter
     const int r = 32 * q + lane;  // weight row of the tile owned by this thread
+    const uint32_t set = static_cast<uint32_t>(warp - kDqWarp) >> 2;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(32 * q) << 16) + kAStart;
     uint32_t g = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
-      for (int kk = 0; kk < nk; ++kk, ++g) {
-        const int sr = g % kStagesRaw, sa = g % kStagesA;
-        if (!mbar_wait(&raw_full[sr], (g / kStagesRaw) & 1u, abort_flag, a.err) ||
-            !mbar_wait(&a_empty[sa], ((g / kStagesA) & 1u) ^ 1u, abort_flag, a.err)) {
-          ok = false;
-          break;
+    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+      for (int kk = 0; kk < nst; ++kk, ++g) {
+        if ((g % kDqSets) != set) continue;
+        const int sr = g % kStagesRaw, s = g % kStages;
+        const int subs = min(kSubs, nsub - kSubs * kk);
+        if (!(ok = mbar_wait_warp(&raw_full[sr], (g / kStagesRaw) & 1u, abort_flag, a.err))) break;
+        const uint8_t* blk = ring_raw + sr * kRawBytes;
+        uint4 c[kSubs][2];
+        uint32_t sc[kSubs];
+#pragma unroll
+        for (int j2 = 0; j2 < kSubs; ++j2) {
+          if (j2 < subs) {
+            const uint8_t* b = blk + j2 * kFp4BlockBytes;
+            c[j2][0] = *reinterpret_cast<const uint4*>(b + r * 16);
+            c[j2][1] = *reinterpret_cast<const uint4*>(b + 2048 + r * 16);
+            sc[j2] = *reinterpret_cast<const uint16_t*>(b + 4096 + 2 * r);
+          }
         }
-        const uint8_t* blk = ring_raw + sr * kFp4BlockBytes;
-        const uint4 c0 = *reinterpret_cast<const uint4*>(blk + r * 16);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(blk + 2048 + r * 16);
-        const uint32_t sc = *reinterpret_cast<const uint16_t*>(blk + 4096 + 2 * r);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&raw_empty[sr]);  // raw bytes are in registers now
-        uint32_t w[32];
-        dequant16(c0, scale_half2(sc & 0xFFu), w);
-        dequant16(c1, scale_half2(sc >> 8), w + 16);
-        tmem_st_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + kAStart + sa * kACols, w);
+        if (lane == 0) mbar_arrive(&raw_empty[sr]);  // the raw bytes are in registers now
+        if (!(ok = mbar_wait_warp(&empty[s], ((g / kStages) & 1u) ^ 1u, abort_flag, a.err))) break;
+#pragma unroll
+        for (int j2 = 0; j2 < kSubs; ++j2) {
+          if (j2 < subs) {
+            uint32_t w[32];
+            dequant16(c[j2][0], scale_half2(sc[j2] & 0xFFu), w);
+            dequant16(c[j2][1], scale_half2(sc[j2] >> 8), w + 16);
+            tmem_st_32x32b_x32(trow + s * kACols + 32 * j2, w);
+          }
+        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[sa]);
+        if (lane == 0) mbar_arrive(&full[s]);
       }
     }
   } else if (!kGateUp) {
     // ---------------- B producer (down): rows of h by TMA ----------------
-    if (warp == 6 && lane == 0) {
+    if (warp == 6) {
       const uint64_t pol_act = l2_policy_evict_last();
       uint32_t g = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
+      for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
         const Unit un = decode_unit(u, a.segs, tiles);
         const int nbox = (pad16(un.rows) + 31) / 32;
-        for (int kk = 0; kk < nk; ++kk, ++g) {
-          const int slot = g % kStagesB;
-          if (!mbar_wait(&b_empty[slot], ((g / kStagesB) & 1u) ^ 1u, abort_flag, a.err)) {
-            ok = false;
-            break;
+        for (int kk = 0; kk < nst; ++kk, ++g) {
+          const int s = g % kStages;
+          const int subs = min(kSubs, nsub - kSubs * kk);
+          if (!(ok = mbar_wait_warp(&empty[s], ((g / kStages) & 1u) ^ 1u, abort_flag, a.err))) break;
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&full[s], subs * nbox * 32 * kSubK * 2);
+            for (int j2 = 0; j2 < subs; ++j2)
+              for (int i = 0; i < nbox; ++i)
+                tma_load_2d(ring_b + s * kBBytes + j2 * kSubBytes + i * 32 * kSubK * 2, &maps.h, &full[s],
+                            (kSubs * kk + j2) * kSubK, un.row_start + 32 * i, pol_act);
           }
-          mbar_arrive_expect_tx(&b_full[slot], nbox * 32 * BK * 2);
-          for (int i = 0; i < nbox; ++i)
-            tma_load_2d(ring_b + slot * kBBytes + i * 32 * BK * 2, &maps.h, &b_full[slot], kk * BK,
-                        un.row_start + 32 * i, pol_act);
+          __syncwarp();
         }
       }
     }
   } else {
     // ---------------- B producer (gate/up): fp16 token rows gathered with cp.async ----------
-    const int p = threadIdx.x - 192;  // 0..127
-    const int ch = p & 7, r0 = p >> 3;
+    // Gather warps w and w + kStages own ring slot w: they fill every stage g with
+    // g % kStages == w (each half of the rows), wait for their own copies, fence them for the
+    // tensor core and arrive.  All kStages slots can be in flight at once, and no copy waits
+    // behind the issue of a later stage.
+    const int gw = warp - 6;
+    const int slot = gw % kStages, half = gw / kStages;
+    int32_t* tok = tok_tab + kSegRowsMax * gw;  // token row of each row of this warp's unit
+    const int ch = lane & 7;                    // 16-byte chunk
+    const int rs = (lane >> 3) + 4 * half;      // first row; rows rs + 8 i
     const uint64_t pol_x = l2_policy_evict_last();
     uint32_t g = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
+    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
       const Unit un = decode_unit(u, a.segs, tiles);
-      const uint16_t* src[kSegRowsMax / 16];
-#pragma unroll
-      for (int i = 0; i < kSegRowsMax / 16; ++i) {
-        const int n = r0 + 16 * i;
-        src[i] = nullptr;
-        if (n < un.rows) src[i] = a.x16 + static_cast<size_t>(a.perm[un.row_start + n] / a.k) * a.d + ch * 8;
-      }
-      for (int kk = 0; kk < nk; ++kk, ++g) {
-        const int slot = g % kStagesB;
-        if (!mbar_wait(&b_empty[slot], ((g / kStagesB) & 1u) ^ 1u, abort_flag, a.err)) {
-          ok = false;
-          break;
+      bool have_tok = false;
+      for (int kk = 0; kk < nst; ++kk, ++g) {
+        const int s = g % kStages;
+        if (s != slot) continue;
+        if (!have_tok) {
+          for (int n = lane; n < un.rows; n += 32) tok[n] = a.perm[un.row_start + n] / a.k;
+          __syncwarp();
+          have_tok = true;
         }
-        const uint32_t sb = smem_u32(ring_b + slot * kBBytes);
-#pragma unroll
-        for (int i = 0; i < kSegRowsMax / 16; ++i) {
-          const int n = r0 + 16 * i;
-          if (src[i]) cp_async_16_hint(sb + n * 128 + ((ch ^ (n & 7)) << 4), src[i] + kk * BK, pol_x);
+        const int subs = min(kSubs, nsub - kSubs * kk);
+        if (!(ok = mbar_wait_warp(&empty[s], ((g / kStages) & 1u) ^ 1u, abort_flag, a.err))) break;
+        const uint32_t sb = smem_u32(ring_b + s * kBBytes);
+        const int k0 = kSubs * kk * kSubK + ch * 8;
+        for (int n = rs; n < un.rows; n += 8) {
+          const uint16_t* src = a.x16 + static_cast<size_t>(tok[n]) * a.d + k0;
+          const uint32_t dst = sb + n * 128 + ((ch ^ (n & 7)) << 4);
+          cp_async_16_hint(dst, src, pol_x);
+          if (subs > 1) cp_async_16_hint(dst + kSubBytes, src + kSubK, pol_x);
         }
         cp_async_commit();
-        if (g >= kLag) {
-          cp_async_wait<kLag>();
-          fence_proxy_async_smem();
-          mbar_arrive(&b_full[(g - kLag) % kStagesB]);
-        }
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
       }
-    }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    if (ok && !*abort_flag) {
-      const uint32_t first = g >= kLag ? g - kLag : 0;
-      for (uint32_t s = first; s < g; ++s) mbar_arrive(&b_full[s % kStagesB]);
     }
   }
 
@@ -400,7 +434,7 @@ static cudaError_t launch_fq(const TcMaps* maps, const TcArgs& a, int num_sms, c
     if (e != cudaSuccess) return e;
     g_fq_attr[kGateUp] = true;
   }
-  return launch_pdl(kern, dim3(num_sms), dim3(kGateUp ? 448 : 352), fq::kSmemBytes, st, *maps, a);
+  return launch_pdl(kern, dim3(num_sms), dim3(kGateUp ? 704 : 480), fq::kSmemBytes, st, *maps, a);
 }
 
 cudaError_t launch_fp4_gateup(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st) {

@@ -23,16 +23,19 @@
 //
 // Roles (persistent CTAs, one per SM, every role walks the same unit sequence):
 //   warp 0      producer: A by bulk copy; B by TMA (down kernel)
-//   warp 1      TMEM owner and MMA issuer (one thread)
+//   warp 1      TMEM owner and MMA issuer
 //   warps 2-5   epilogue (TMEM lanes 32*(warp%4) .. +31)
-//   warps 6-9   gate/up only: cp.async gather of the token rows
+//   warps 6-17  gate/up only: cp.async gather of the token rows, two warps per stage slot
+// Producer and MMA loops run converged and issue under elect_one() (warp-uniform operands: an
+// MMA issues in a few tens of cycles), and the MMA warp probes the next stage's barrier before
+// issuing the current stage, so the barrier round trip hides behind the issue.
 // Pipeline: 6 shared-memory stages of (A 16 KB + B up to 16 KB), two TMEM accumulators of up
 // to 128 fp32 columns so the epilogue of one unit overlaps the main loop of the next.  An
 // expert with more than 128 rows is split into parts; the units of its parts are ordered
 // tile-major (tile 0 of every part, then tile 1, ...) so that CTAs working on the same
 // weight tile run side by side and the second read of the tile is served by L2.
-// Measured on the 2051-token step: the weight stream alone runs at the measured HBM copy rate;
-// separate rings for A and B, a 7th stage and a longer gather lag were all slower or equal.
+// The gather warps of a slot wait for their own copies and arrive themselves, so every stage
+// of the ring can be in flight at once (a lagged arrive would leave only part of it).
 // Every wait is bounded (see common.cuh); on a timeout the CTA stops issuing work, drains its
 // MMAs, frees TMEM and returns with MOE_DEVERR_TIMEOUT set.
 #include "common.cuh"
@@ -44,14 +47,16 @@ namespace tc {
 constexpr int BM = 128;                          // weight rows per unit (MMA M)
 constexpr int BK = 64;                           // K elements per stage (128-byte rows)
 constexpr int kStages = 6;
-constexpr int kLag = 2;                          // gather completion lag (stages), < kStages
 constexpr int kABytes = BM * BK * 2;             // 16 KB
 constexpr int kBBytes = kSegRowsMax * BK * 2;    // 16 KB (N <= 128)
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kTmemCols = 2 * kSegRowsMax;       // 2 accumulators x 128 columns
 constexpr int kAccCols = kSegRowsMax;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*align slack*/;
-constexpr int kGatherThreads = 128;
+constexpr int kGatherPerSlot = 2;                // gate/up B producers per stage slot
+constexpr int kGatherWarps = kGatherPerSlot * kStages;
+constexpr int kTokBytes = kGatherWarps * kSegRowsMax * 4;  // per gather warp: token of each row
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*align slack*/ + kTokBytes;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct Unit {
   int shared;     // 1: shared-expert segment
@@ -91,7 +96,7 @@ MOE_DEVICE Unit decode_unit(int u, const TcArgs& a, int tiles_r, int tiles_s, in
 MOE_DEVICE int pad16(int rows) { return rows <= 16 ? 16 : ((rows + 15) & ~15); }
 
 template <bool kGateUp>
-__global__ void __launch_bounds__(kGateUp ? 320 : 192, 1)
+__global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
     tc_ffn_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -102,12 +107,13 @@ __global__ void __launch_bounds__(kGateUp ? 320 : 192, 1)
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int32_t* tok_tab = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes + 1024);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], kGateUp ? 1 + kGatherThreads : 1);
+      mbar_init(&full[s], kGateUp ? 1 + kGatherPerSlot : 1);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -143,80 +149,75 @@ __global__ void __launch_bounds__(kGateUp ? 320 : 192, 1)
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      const uint64_t pol_w = l2_policy_evict_first();
-      const uint64_t pol_act = l2_policy_evict_last();
-      uint32_t g = 0;
-      for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x) {
-        const Unit un = decode_unit(u, a, tiles_r, tiles_s, n_shared_units);
-        const int nk = un.shared ? nk_s : nk_r;
-        const int nbox = kGateUp ? 0 : (pad16(un.rows) + 31) / 32;
-        bool ok = true;
-        for (int kk = 0; kk < nk; ++kk, ++g) {
-          const int slot = g % kStages;
-          const uint32_t use = g / kStages;
-          if (!mbar_wait(&empty[slot], (use & 1u) ^ 1u, abort_flag, a.err)) {
-            ok = false;
-            break;
-          }
+    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_act = l2_policy_evict_last();
+    uint32_t g = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+      const Unit un = decode_unit(u, a, tiles_r, tiles_s, n_shared_units);
+      const int nk = un.shared ? nk_s : nk_r;
+      const int nbox = kGateUp ? 0 : (pad16(un.rows) + 31) / 32;
+      const uint16_t* wbase;
+      if (kGateUp)
+        wbase = un.shared ? a.w_gu_s + static_cast<size_t>(un.tile) * nk * kTileElems
+                          : a.w_gu + (static_cast<size_t>(un.expert) * tiles_r + un.tile) * nk * kTileElems;
+      else
+        wbase = un.shared ? a.w_down_s + static_cast<size_t>(un.tile) * nk * kTileElems
+                          : a.w_down + (static_cast<size_t>(un.expert) * tiles_r + un.tile) * nk * kTileElems;
+      const CUtensorMap* hm = un.shared ? &maps.h_s : &maps.h;
+      for (int kk = 0; kk < nk; ++kk, ++g) {
+        const int slot = g % kStages;
+        if (!(ok = mbar_wait_warp(&empty[slot], ((g / kStages) & 1u) ^ 1u, abort_flag, a.err))) break;
+        if (elect_one()) {
           uint8_t* sa = smem + slot * kStageBytes;
-          uint8_t* sb = sa + kABytes;
           mbar_arrive_expect_tx(&full[slot], kABytes + nbox * 32 * BK * 2);
-          const uint16_t* wsrc;
-          if (kGateUp)
-            wsrc = un.shared ? a.w_gu_s + (static_cast<size_t>(un.tile) * nk + kk) * kTileElems
-                             : a.w_gu + ((static_cast<size_t>(un.expert) * tiles_r + un.tile) * nk + kk) * kTileElems;
-          else
-            wsrc = un.shared ? a.w_down_s + (static_cast<size_t>(un.tile) * nk + kk) * kTileElems
-                             : a.w_down + ((static_cast<size_t>(un.expert) * tiles_r + un.tile) * nk + kk) * kTileElems;
-          bulk_load(sa, wsrc, kABytes, &full[slot], pol_w);
-          if (!kGateUp) {
-            const CUtensorMap* hm = un.shared ? &maps.h_s : &maps.h;
+          bulk_load(sa, wbase + static_cast<size_t>(kk) * kTileElems, kABytes, &full[slot], pol_w);
+          if (!kGateUp)
             for (int i = 0; i < nbox; ++i)
-              tma_load_2d(sb + i * 32 * BK * 2, hm, &full[slot], kk * BK, un.row_start + 32 * i, pol_act);
-          }
+              tma_load_2d(sa + kABytes + i * 32 * BK * 2, hm, &full[slot], kk * BK, un.row_start + 32 * i, pol_act);
         }
-        if (!ok) break;
+        __syncwarp();
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      uint32_t g = 0, j = 0;
-      for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x, ++j) {
-        const Unit un = decode_unit(u, a, tiles_r, tiles_s, n_shared_units);
-        const int nk = un.shared ? nk_s : nk_r;
-        const uint32_t N = static_cast<uint32_t>(pad16(un.rows));
-        const uint32_t buf = j & 1u, use_acc = j >> 1;
-        if (!mbar_wait(&acc_empty[buf], (use_acc & 1u) ^ 1u, abort_flag, a.err)) break;
+    // ---------------- MMA issuer: the warp waits, one elected lane issues ----------------
+    uint32_t g = 0, j = 0;
+    bool ok = true, ready = false;  // ready: full[g % kStages] already seen complete for stage g
+    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++j) {
+      const Unit un = decode_unit(u, a, tiles_r, tiles_s, n_shared_units);
+      const int nk = un.shared ? nk_s : nk_r;
+      const uint32_t N = static_cast<uint32_t>(pad16(un.rows));
+      const uint32_t buf = j & 1u, use_acc = j >> 1;
+      if (!(ok = mbar_wait_warp(&acc_empty[buf], (use_acc & 1u) ^ 1u, abort_flag, a.err))) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + buf * kAccCols;
+      // gate/up: bf16 weights x bf16 tokens; down: fp16 weights x fp16 hidden vectors
+      const uint32_t idesc = kGateUp ? idesc_bf16_f32(BM, N) : idesc_f16_f32(BM, N);
+      for (int kk = 0; kk < nk; ++kk, ++g) {
+        const int slot = g % kStages;
+        if (!ready && !(ok = mbar_wait_warp(&full[slot], (g / kStages) & 1u, abort_flag, a.err))) break;
+        const uint32_t gn = g + 1;  // probe the next stage now, use the answer next iteration
+        const bool next = mbar_test(&full[gn % kStages], (gn / kStages) & 1u);
         tc_fence_after();
-        const uint32_t d_tmem = tmem + buf * kAccCols;
-        // gate/up: bf16 weights x bf16 tokens; down: fp16 weights x fp16 hidden vectors
-        const uint32_t idesc = kGateUp ? idesc_bf16_f32(BM, N) : idesc_f16_f32(BM, N);
-        bool ok = true;
-        for (int kk = 0; kk < nk; ++kk, ++g) {
-          const int slot = g % kStages;
-          const uint32_t use = g / kStages;
-          if (!mbar_wait(&full[slot], use & 1u, abort_flag, a.err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = smem_u32(smem + slot * kStageBytes);
-          const uint64_t adesc = smem_desc_sw128(sa);
-          const uint64_t bdesc = smem_desc_sw128(sa + kABytes);
+        const uint32_t sa = smem_u32(smem + slot * kStageBytes);
+        const uint64_t adesc = smem_desc_sw128(sa);
+        const uint64_t bdesc = smem_desc_sw128(sa + kABytes);
+        if (elect_one()) {
 #pragma unroll
           for (int ks = 0; ks < BK / 16; ++ks)  // K = 16 per MMA: +32 bytes = +2 in the address field
             mma_f16_ss(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc, (kk | ks) != 0);
           mma_commit(&empty[slot]);
         }
-        if (!ok) break;
-        mma_commit(&acc_full[buf]);
+        ready = __all_sync(0xffffffffu, next);
       }
-      // all MMAs issued by this thread have finished once `drain` completes
-      mma_commit(drain);
-      mbar_wait(drain, 0, nullptr, a.err);
+      if (!ok) break;
+      if (elect_one()) mma_commit(&acc_full[buf]);
+      __syncwarp();
     }
+    // all MMAs issued by this warp have finished once `drain` completes
+    if (elect_one()) mma_commit(drain);
+    __syncwarp();
+    mbar_wait_warp(drain, 0, nullptr, a.err);
   } else if (warp < 6) {
     // ---------------- epilogue ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -292,51 +293,40 @@ __global__ void __launch_bounds__(kGateUp ? 320 : 192, 1)
     }
   } else if (kGateUp) {
     // ---------------- token-row gather (cp.async) ----------------
-    // 8 consecutive threads copy the 8 16-byte chunks of one row (a full 128-byte line per 8
-    // lanes); thread p handles chunk p % 8 of rows p / 8 + 16 i, i = 0..7.
-    const int p = threadIdx.x - 192;  // 0..127
-    const int ch = p & 7, r0 = p >> 3;
+    // Warps w and w + kStages own stage slot w: they fill every stage g with g % kStages == w
+    // (each half of the rows), wait for their own copies, fence them for the tensor core and
+    // arrive.  8 consecutive lanes copy the 8 16-byte chunks of one row (a 128-byte line).
+    const int gw = warp - 6;
+    const int slot = gw % kStages, half = gw / kStages;
+    int32_t* tok = tok_tab + kSegRowsMax * gw;  // token of each row of this warp's unit
+    const int ch = lane & 7;
+    const int rs = (lane >> 3) + 4 * half;      // first row; rows rs + 8 i
     const uint64_t pol_x = l2_policy_evict_last();  // each x row is gathered once per weight tile
     uint32_t g = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total_units && ok && !*abort_flag; u += gridDim.x) {
+    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
       const Unit un = decode_unit(u, a, tiles_r, tiles_s, n_shared_units);
-      const uint16_t* src[kSegRowsMax / 16];
-#pragma unroll
-      for (int i = 0; i < kSegRowsMax / 16; ++i) {
-        const int n = r0 + 16 * i;
-        src[i] = nullptr;
-        if (n < un.rows) {
-          const int tok = un.shared ? un.row_start + n : a.perm[un.row_start + n] / a.k;
-          src[i] = a.x + static_cast<size_t>(tok) * a.d + ch * 8;
+      const int nk = un.shared ? nk_s : nk_r;
+      bool have_tok = false;
+      for (int kk = 0; kk < nk; ++kk, ++g) {
+        const int s = g % kStages;
+        if (s != slot) continue;
+        if (!have_tok) {
+          for (int n = lane; n < un.rows; n += 32) tok[n] = un.shared ? un.row_start + n : a.perm[un.row_start + n] / a.k;
+          __syncwarp();
+          have_tok = true;
         }
-      }
-      for (int kk = 0; kk < nk_r; ++kk, ++g) {
-        const int slot = g % kStages;
-        const uint32_t use = g / kStages;
-        if (!mbar_wait(&empty[slot], (use & 1u) ^ 1u, abort_flag, a.err)) {
-          ok = false;
-          break;
-        }
-        const uint32_t sb = smem_u32(smem + slot * kStageBytes + kABytes);
-#pragma unroll
-        for (int i = 0; i < kSegRowsMax / 16; ++i) {
-          const int n = r0 + 16 * i;
-          if (src[i]) cp_async_16_hint(sb + n * 128 + ((ch ^ (n & 7)) << 4), src[i] + kk * BK, pol_x);
-        }
+        if (!(ok = mbar_wait_warp(&empty[s], ((g / kStages) & 1u) ^ 1u, abort_flag, a.err))) break;
+        const uint32_t sb = smem_u32(smem + s * kStageBytes + kABytes);
+        const int k0 = kk * BK + ch * 8;
+        for (int n = rs; n < un.rows; n += 8)
+          cp_async_16_hint(sb + n * 128 + ((ch ^ (n & 7)) << 4), a.x + static_cast<size_t>(tok[n]) * a.d + k0, pol_x);
         cp_async_commit();
-        if (g >= kLag) {
-          cp_async_wait<kLag>();
-          fence_proxy_async_smem();
-          mbar_arrive(&full[(g - kLag) % kStages]);
-        }
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
       }
-    }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    if (ok && !*abort_flag) {
-      const uint32_t first = g >= kLag ? g - kLag : 0;
-      for (uint32_t s = first; s < g; ++s) mbar_arrive(&full[s % kStages]);
     }
   }
 
@@ -361,7 +351,8 @@ static cudaError_t launch_tc(const TcMaps* maps, const TcArgs& a, int num_sms, c
     if (e != cudaSuccess) return e;
     g_tc_attr_set[kGateUp] = true;
   }
-  return launch_pdl(kern, dim3(num_sms), dim3(kGateUp ? 320 : 192), tc::kSmemBytes, st, *maps, a);
+  return launch_pdl(kern, dim3(num_sms), dim3(kGateUp ? 192 + 32 * tc::kGatherWarps : 192), tc::kSmemBytes, st,
+                    *maps, a);
 }
 
 cudaError_t launch_tc_gateup(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st) {

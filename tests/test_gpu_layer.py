@@ -217,6 +217,24 @@ def test_fp4_small_layer_both_paths(T, path):
     assert plan.device_error() == 0
 
 
+# d_ff / 64 odd: the down GEMM's last 128-deep K stage holds a single 64-wide block; a hot
+# expert (Zipf routing) spans several 128-row segments
+FP4_ODD = synth.LayerSpec(E=12, k=3, d=384, f=192, n_shared=0, f_s=0, wdtype="mxfp4", zipf_s=1.2)
+
+
+@pytest.mark.parametrize("T", [5, 390])
+def test_fp4_odd_k_blocks_tc(T):
+    w = synth.custom(FP4_ODD, T, n_prefill=T, name=f"fp4odd{T}")
+    plan = make_plan(w)
+    plan.set_path("tc")
+    x = to_dev(w.x(), "bf16")
+    out = bf16_tensor_to_f64(plan.forward(x, n_prefill=w.n_prefill))
+    _, ids, _ = plan.route(x, want_logits=False)
+    ref = oracle_layer(w)
+    compare_layer(out, ref, FP4_ODD.k, TOL_FP4, ids.cpu().numpy())
+    assert plan.device_error() == 0
+
+
 def test_fp4_scales_outside_fp16_range_use_the_reference_path():
     """A scale whose e2m1 multiples are not exact in fp16 keeps the tensor-core path off; the
     CUDA-core path reads the same tiled layout and still matches the oracle."""
