@@ -112,11 +112,15 @@ static WsLayout layout_for(const moe_plan* p, int T_max) {
   // partial router logits of the tensor-core router: splits(T') * T' rows for the worst T' <= T
   size_t part_rows = 0;
   if (p->router_tc_capable())
-    for (size_t m = 2; 128 * (m - 1) < T; ++m) {  // the largest T' of each 128-token tile count
+    for (size_t m = 1; 128 * (m - 1) < T; ++m) {  // the largest T' of each 128-token tile count
       const size_t tt = 128 * m < T ? 128 * m : T;
       const size_t r = static_cast<size_t>(router_tc_splits(static_cast<int>(tt), p->E, p->d, p->num_sms)) * tt;
       if (r > part_rows) part_rows = r;
     }
+  if (p->d % 128 == 0) {  // the small-T router's K-split partials
+    const size_t r = static_cast<size_t>(router_small_splits(p->d)) * (T < 128 ? T : 128);
+    if (r > part_rows) part_rows = r;
+  }
   L.parts = take(part_rows * p->E * sizeof(float));
   L.ids = take(R * sizeof(int32_t));
   L.gates = take(R * sizeof(float));
@@ -321,10 +325,12 @@ extern "C" void moe_plan_destroy(moe_plan* p) {
   delete p;
 }
 
+// Plan-owned device words: [0] the error bits, [1] the small-step routing counter (0 between
+// launches), kept out of the caller's workspace, whose contents may change between calls.
 static moe_status ensure_err_word(moe_plan* p) {
   if (p->err) return MOE_OK;
-  MOE_CUDA_TRY(cudaMalloc(&p->err, sizeof(uint32_t)));
-  MOE_CUDA_TRY(cudaMemset(p->err, 0, sizeof(uint32_t)));
+  MOE_CUDA_TRY(cudaMalloc(&p->err, 2 * sizeof(uint32_t)));
+  MOE_CUDA_TRY(cudaMemset(p->err, 0, 2 * sizeof(uint32_t)));
   return MOE_OK;
 }
 
@@ -625,20 +631,44 @@ static moe_status run_experts(moe_plan* p, const uint16_t* x, int T, const int32
   return MOE_OK;
 }
 
-// Router logits + top-k (+ masks).  T > 128 with a tensor-core-capable shape uses the
-// tensor-core router (K-split partials summed by top-k); otherwise the CUDA-core router.
+// Router logits as nsplit partial matrices [nsplit][T][E] for the top-k to add (in split order,
+// plus *bias when not null).  T > kRouterTcMinT with a tensor-core-capable shape: the
+// tensor-core router; T <= 128 and d % 128 == 0: the small-T K-split router; otherwise the
+// CUDA-core router (bias included).
+static moe_status router_step(moe_plan* p, const uint16_t* x, int T, const float** parts_out, int* nsplit,
+                              const float** bias, cudaStream_t st) {
+  float* parts = ws_ptr<float>(p, p->L.parts);
+  if (p->router_tc && T > kRouterTcMinT) {
+    const int ns = router_tc_splits(T, p->E, p->d, p->num_sms);
+    LAUNCH(p, "router_tc", st, launch_router_tc(&p->map_router3, x, T, p->E, p->d, ns, parts, p->err, st));
+    *parts_out = parts, *nsplit = ns, *bias = p->b_router;
+  } else if (T <= 128 && p->d % 128 == 0) {
+    LAUNCH(p, "router_logits", st, launch_router_parts_small(x, p->w_router, T, p->E, p->d, parts, st));
+    *parts_out = parts, *nsplit = router_small_splits(p->d), *bias = p->b_router;
+  } else {
+    float* lg = ws_ptr<float>(p, p->L.logits);
+    LAUNCH(p, "router_logits", st, launch_router_logits(x, p->w_router, p->b_router, T, p->E, p->d, lg, st));
+    *parts_out = lg, *nsplit = 1, *bias = nullptr;
+  }
+  return MOE_OK;
+}
+
+// The nsplit router_step will produce for T tokens.
+static int router_nsplit(const moe_plan* p, int T) {
+  if (p->router_tc && T > kRouterTcMinT) return router_tc_splits(T, p->E, p->d, p->num_sms);
+  if (T <= 128 && p->d % 128 == 0) return router_small_splits(p->d);
+  return 1;
+}
+
+// Router logits + top-k (+ masks).
 static moe_status route_step(moe_plan* p, const uint16_t* x, int T, float* logits_out, int32_t* ids, float* gates,
                              uint32_t* masks, cudaStream_t st) {
-  if (p->router_tc && T > 128) {
-    const int ns = router_tc_splits(T, p->E, p->d, p->num_sms);
-    float* parts = ws_ptr<float>(p, p->L.parts);
-    LAUNCH(p, "router_tc", st, launch_router_tc(&p->map_router3, x, T, p->E, p->d, ns, parts, p->err, st));
-    LAUNCH(p, "topk", st, launch_topk(parts, ns, p->b_router, logits_out, T, p->E, p->k, ids, gates, masks, p->err, st));
-  } else {
-    float* lg = logits_out ? logits_out : ws_ptr<float>(p, p->L.logits);
-    LAUNCH(p, "router_logits", st, launch_router_logits(x, p->w_router, p->b_router, T, p->E, p->d, lg, st));
-    LAUNCH(p, "topk", st, launch_topk(lg, 1, nullptr, nullptr, T, p->E, p->k, ids, gates, masks, p->err, st));
-  }
+  const float* parts = nullptr;
+  const float* bias = nullptr;
+  int ns = 1;
+  moe_status s = router_step(p, x, T, &parts, &ns, &bias, st);
+  if (s != MOE_OK) return s;
+  LAUNCH(p, "topk", st, launch_topk(parts, ns, bias, logits_out, T, p->E, p->k, ids, gates, masks, p->err, st));
   return MOE_OK;
 }
 
@@ -664,13 +694,25 @@ extern "C" moe_status moe_layer_forward(moe_plan* p, const void* x, int T, int n
   uint16_t* y_s = p->n_shared > 0 ? ws_ptr<uint16_t>(p, p->L.y_s) : nullptr;
   const int n_chunks = (T + kChunk - 1) / kChunk;
   const bool tc = use_tc(p);
-  s = route_step(p, xb, T, nullptr, ids, gates, masks, st);
-  if (s != MOE_OK) return s;
-  LAUNCH(p, "chunk_scan", st, launch_chunk_scan(masks, n_chunks, p->E, chunk_base, counts, st));
-  LAUNCH(p, "scatter", st,
-         launch_scatter(ids, masks, chunk_base, counts, T, p->E, p->k, perm, inv, offsets,
-                        tc ? ws_ptr<Seg>(p, p->L.segs) : nullptr, ws_ptr<int32_t>(p, p->L.n_segs), p->L.max_segs,
-                        p->err, st));
+  Seg* segs = tc ? ws_ptr<Seg>(p, p->L.segs) : nullptr;
+  if (route_small_ok(T, p->E, p->k, router_nsplit(p, T))) {
+    // small step: the whole routing and grouping in one block after the router
+    const float* parts = nullptr;
+    const float* bias = nullptr;
+    int ns = 1;
+    s = router_step(p, xb, T, &parts, &ns, &bias, st);
+    if (s != MOE_OK) return s;
+    LAUNCH(p, "route_small", st,
+           launch_route_small(parts, ns, bias, T, p->E, p->k, ids, gates, counts, offsets, perm, inv, segs,
+                              ws_ptr<int32_t>(p, p->L.n_segs), p->L.max_segs, p->err + 1, p->err, st));
+  } else {
+    s = route_step(p, xb, T, nullptr, ids, gates, masks, st);
+    if (s != MOE_OK) return s;
+    LAUNCH(p, "chunk_scan", st, launch_chunk_scan(masks, n_chunks, p->E, chunk_base, counts, st));
+    LAUNCH(p, "scatter", st,
+           launch_scatter(ids, masks, chunk_base, counts, T, p->E, p->k, perm, inv, offsets, segs,
+                          ws_ptr<int32_t>(p, p->L.n_segs), p->L.max_segs, p->err, st));
+  }
   s = run_experts(p, xb, T, offsets, perm, y, y_s, st);
   if (s != MOE_OK) return s;
   LAUNCH(p, "combine", st, launch_combine(y, gates, inv, y_s, T, p->k, p->d, static_cast<uint16_t*>(out), st));

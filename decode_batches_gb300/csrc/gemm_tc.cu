@@ -55,7 +55,9 @@ constexpr int kAccCols = kSegRowsMax;
 constexpr int kGatherPerSlot = 2;                // gate/up B producers per stage slot
 constexpr int kGatherWarps = kGatherPerSlot * kStages;
 constexpr int kTokBytes = kGatherWarps * kSegRowsMax * 4;  // per gather warp: token of each row
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*align slack*/ + kTokBytes;
+constexpr int kEpiStageBytes = 16 * 32 * 2;     // per epilogue warp: 16 columns x 32 fp16 rows
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*align slack*/ + kTokBytes +
+                           4 * kEpiStageBytes;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct Unit {
@@ -108,6 +110,7 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int32_t* tok_tab = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes + 1024);
+  uint16_t* epi_stage = reinterpret_cast<uint16_t*>(smem + kStages * kStageBytes + 1024 + kTokBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -229,10 +232,17 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
       tc_fence_after();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * kAccCols;
       const int L = 32 * q + lane;  // accumulator row (= weight row of the tile)
+      // Each 16-column chunk goes through a per-warp shared tile [column][row] so that the
+      // global stores are 16-byte vectors of 8 consecutive features of one token.
+      uint16_t* stg = epi_stage + (warp - 2) * (kEpiStageBytes / 2);
+      bool sat = false;
       if (kGateUp) {
+        // lanes L and L ^ 8 hold the gate and up rows of one feature: each computes h for 8 of
+        // the 16 columns (gate lane the even ones); the warp covers 16 consecutive features
         const int w16 = L & 15;
         const bool is_gate = w16 < 8;
-        const int feat = un.tile * 64 + 8 * (L >> 4) + (w16 & 7);
+        const int fl = 8 * ((L >> 4) & 1) + (w16 & 7);  // feature within the warp's 16
+        const int feat0 = un.tile * 64 + 16 * q;
         uint16_t* hout;
         int ldh;
         if (un.shared) {
@@ -242,7 +252,6 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
           hout = a.h;
           ldh = a.f;
         }
-        bool sat = false;
         for (int c0 = 0; c0 < un.rows; c0 += 16) {
           uint32_t r[16];
           tmem_ld_32x32b_x16(tbase + c0, r);
@@ -251,42 +260,56 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
           for (int jj = 0; jj < 8; ++jj) {
             const uint32_t send = is_gate ? r[2 * jj + 1] : r[2 * jj];
             const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 8);
-            const int col = c0 + 2 * jj + (is_gate ? 0 : 1);
+            const int cl = 2 * jj + (is_gate ? 0 : 1);
             const float gv = __uint_as_float(is_gate ? r[2 * jj] : recv);
             const float uv = __uint_as_float(is_gate ? recv : r[2 * jj + 1]);
-            if (col < un.rows) {  // columns past the segment hold padding, never stored
-              float hv = swiglu(gv, uv);
-              if (!(fabsf(hv) <= kF16Max)) {
-                sat = true;
-                hv = fminf(fmaxf(hv, -kF16Max), kF16Max);
-              }
-              hout[static_cast<size_t>(un.row_start + col) * ldh + feat] = f32_to_f16_bits_rn(hv);
+            float hv = swiglu(gv, uv);
+            if (c0 + cl < un.rows && !(fabsf(hv) <= kF16Max)) {  // padding columns never count
+              sat = true;
+              hv = fminf(fmaxf(hv, -kF16Max), kF16Max);
+            }
+            stg[cl * 16 + fl] = f32_to_f16_bits_rn(hv);
+          }
+          __syncwarp();
+          {  // lane i: column i / 2, features 8 (i % 2) .. + 7
+            const int cl = lane >> 1, half = lane & 1;
+            if (c0 + cl < un.rows) {
+              const uint4 v = *reinterpret_cast<const uint4*>(stg + cl * 16 + 8 * half);
+              *reinterpret_cast<uint4*>(hout + static_cast<size_t>(un.row_start + c0 + cl) * ldh + feat0 + 8 * half) = v;
             }
           }
+          __syncwarp();
         }
-        if (__any_sync(0xffffffffu, sat) && lane == 0) set_error(a.err, MOE_DEVERR_RANGE);
       } else {
-        const int feat = un.tile * BM + L;
+        const int feat0 = un.tile * BM + 32 * q;
         uint16_t* yout = un.shared ? a.y_s : a.y;
-        bool sat = false;
         for (int c0 = 0; c0 < un.rows; c0 += 16) {
           uint32_t r[16];
           tmem_ld_32x32b_x16(tbase + c0, r);
           tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
-            if (c0 + c < un.rows) {
-              float v = __uint_as_float(r[c]);
-              if (!(fabsf(v) <= kF16Max)) {
-                sat = true;
-                v = fminf(fmaxf(v, -kF16Max), kF16Max);
-              }
-              yout[static_cast<size_t>(un.row_start + c0 + c) * a.d + feat] = f32_to_f16_bits_rn(v);
+            float v = __uint_as_float(r[c]);
+            if (c0 + c < un.rows && !(fabsf(v) <= kF16Max)) {
+              sat = true;
+              v = fminf(fmaxf(v, -kF16Max), kF16Max);
+            }
+            stg[c * 32 + lane] = f32_to_f16_bits_rn(v);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int pass = 0; pass < 2; ++pass) {  // column (16 pass + lane) / 4, features 8 (lane % 4) .. + 7
+            const int idx = 32 * pass + lane;
+            const int cl = idx >> 2, g = idx & 3;
+            if (c0 + cl < un.rows) {
+              const uint4 v = *reinterpret_cast<const uint4*>(stg + cl * 32 + 8 * g);
+              *reinterpret_cast<uint4*>(yout + static_cast<size_t>(un.row_start + c0 + cl) * a.d + feat0 + 8 * g) = v;
             }
           }
+          __syncwarp();
         }
-        if (__any_sync(0xffffffffu, sat) && lane == 0) set_error(a.err, MOE_DEVERR_RANGE);
       }
+      if (__any_sync(0xffffffffu, sat) && lane == 0) set_error(a.err, MOE_DEVERR_RANGE);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);

@@ -38,6 +38,20 @@ cudaError_t launch_topk(const float* parts, int nsplit, const float* bias, float
 // parts[s][T][E] = x[T][k-range s] . W_r[E][k-range s]^T with W_r split into three bf16 pieces
 // (w3: 2-D map over [3E rows][d], box 64 x 128).  Requires E % 128 == 0 and d % 64 == 0.
 int router_tc_splits(int T, int E, int d, int num_sms);
+constexpr int kRouterTcMinT = 16;  // the tensor-core router serves T > 16
+
+// Small-T router (d % 128 == 0): K-split partials parts[router_small_splits(d)][T][E], no bias.
+int router_small_splits(int d);
+cudaError_t launch_router_parts_small(const uint16_t* x, const float* w_router, int T, int E, int d, float* parts,
+                                      cudaStream_t st);
+
+// Top-k + counts + offsets + segments + stable permutation of a small step in one launch.
+constexpr int kSmallRouteT = 64;
+bool route_small_ok(int T, int E, int k, int nsplit);
+// `done`: a device counter that is 0 between launches (the last block resets it).
+cudaError_t launch_route_small(const float* parts, int nsplit, const float* bias, int T, int E, int k, int32_t* ids,
+                               float* gates, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, Seg* segs,
+                               int32_t* n_segs, int max_segs, uint32_t* done, uint32_t* err, cudaStream_t st);
 cudaError_t launch_router_tc(const CUtensorMap* w3, const uint16_t* x, int T, int E, int d, int nsplit, float* parts,
                              uint32_t* err, cudaStream_t st);
 cudaError_t launch_split_router(const float* w, uint16_t* w3, size_t n, cudaStream_t st);

@@ -143,6 +143,92 @@ __global__ void __launch_bounds__(256) router_logits_tiled_kernel(const uint16_t
   }
 }
 
+// Small T, K split: block (8 experts, one 512-wide K slice); the slice of every token's x is
+// staged in shared memory (G tokens at a time) and each warp forms its expert's partial dot
+// products: lane l holds W_r[e][k0 + 4 l + 128 q + c], q < 4, c < 4.  Partials go to
+// parts[split][t][e] and the top-k adds them in split order (deterministic).  d % 128 == 0.
+constexpr int kRouterKS = 512;
+
+int router_small_splits(int d) { return (d + kRouterKS - 1) / kRouterKS; }
+
+template <int G>  // tokens per group, a power of two <= 32
+__global__ void __launch_bounds__(256) router_parts_small_kernel(const uint16_t* __restrict__ x,
+                                                                 const float* __restrict__ wr, int T, int E, int d,
+                                                                 float* __restrict__ parts) {
+  __shared__ __align__(16) uint16_t xs[G * kRouterKS];
+  pdl_trigger();
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + warp;
+  const int sp = blockIdx.y;
+  const int k0 = sp * kRouterKS;
+  const int ks = min(kRouterKS, d - k0);  // multiple of 128
+  float4 w[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int kk = 4 * lane + 128 * q;
+    w[q] = (e < E && kk < ks) ? *reinterpret_cast<const float4*>(wr + static_cast<size_t>(e) * d + k0 + kk)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int t0 = 0; t0 < T; t0 += G) {
+    const int nt = min(G, T - t0);
+    __syncthreads();  // the previous group's readers are done
+    for (int i = threadIdx.x; i < nt * (ks / 8); i += blockDim.x) {
+      const int tl = i / (ks / 8), c8 = i % (ks / 8);
+      *reinterpret_cast<uint4*>(xs + tl * kRouterKS + 8 * c8) =
+          *reinterpret_cast<const uint4*>(x + static_cast<size_t>(t0 + tl) * d + k0 + 8 * c8);
+    }
+    __syncthreads();
+    if (e < E) {
+      // lane-partial dot products of the group's G tokens (rows past nt read stale shared
+      // memory and are never stored)
+      float acc[G];
+#pragma unroll
+      for (int tl = 0; tl < G; ++tl) {
+        float a = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int kk = 4 * lane + 128 * q;
+          if (kk < ks) {
+            const uint2 xv = *reinterpret_cast<const uint2*>(xs + tl * kRouterKS + kk);
+            a = fmaf(bf16_bits_to_f32(static_cast<uint16_t>(xv.x & 0xFFFFu)), w[q].x, a);
+            a = fmaf(bf16_bits_to_f32(static_cast<uint16_t>(xv.x >> 16)), w[q].y, a);
+            a = fmaf(bf16_bits_to_f32(static_cast<uint16_t>(xv.y & 0xFFFFu)), w[q].z, a);
+            a = fmaf(bf16_bits_to_f32(static_cast<uint16_t>(xv.y >> 16)), w[q].w, a);
+          }
+        }
+        acc[tl] = a;
+      }
+      // transposing butterfly over lane bits below G: after the level for offset o a lane
+      // keeps the half of its values whose index has the lane's bit o, so lane l ends with
+      // token (l mod G) summed over the lanes that agree with it above bit log2(G); plain
+      // butterflies over the remaining bits finish the sums
+#pragma unroll
+      for (int o = G / 2; o >= 1; o >>= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < o; ++i) {
+          const float send = upper ? acc[i] : acc[i + o];
+          const float keep = upper ? acc[i + o] : acc[i];
+          acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+#pragma unroll
+      for (int o = G; o < 32; o <<= 1) acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
+      if (lane < nt) parts[(static_cast<size_t>(sp) * T + t0 + lane) * E + e] = acc[0];
+    }
+  }
+}
+
+cudaError_t launch_router_parts_small(const uint16_t* x, const float* w_router, int T, int E, int d, float* parts,
+                                      cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  dim3 grid((E + 7) / 8, router_small_splits(d));
+  if (T <= 8) return launch_pdl(router_parts_small_kernel<8>, grid, dim3(256), 0, st, x, w_router, T, E, d, parts);
+  if (T <= 16) return launch_pdl(router_parts_small_kernel<16>, grid, dim3(256), 0, st, x, w_router, T, E, d, parts);
+  return launch_pdl(router_parts_small_kernel<32>, grid, dim3(256), 0, st, x, w_router, T, E, d, parts);
+}
+
 cudaError_t launch_router_logits(const uint16_t* x, const float* w_router, const float* b_router, int T,
                                  int E, int d, float* logits, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
@@ -181,6 +267,96 @@ MOE_DEVICE uint64_t rank_key(float v, int e) {
 template <int PL>
 constexpr int topk_threads() { return PL >= 16 ? 512 : 1024; }  // 64 registers/thread at 1024
 
+// Selection and gates of token t by one warp from its logits v (lane l holds experts
+// l + 32 i): writes ids / gates of the token and returns, in lane j < k, the expert chosen in
+// round j.
+template <int PL>
+MOE_DEVICE int topk_select(const float (&v)[PL], int t, int E, int k, int32_t* __restrict__ ids,
+                           float* __restrict__ gates, uint32_t* err) {
+  const int lane = threadIdx.x & 31;
+  uint64_t key[PL];
+#pragma unroll
+  for (int i = 0; i < PL; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = e < E ? rank_key(v[i], e) : 0ull;
+  }
+  int sel_i = 0;  // lane j keeps the expert chosen in round j
+  for (int j = 0; j < k; ++j) {
+    uint64_t best = key[0];
+#pragma unroll
+    for (int i = 1; i < PL; ++i) best = key[i] > best ? key[i] : best;
+    const uint32_t hi = static_cast<uint32_t>(best >> 32);
+    const uint32_t win_hi = __reduce_max_sync(0xffffffffu, hi);
+    const uint32_t win_lo = __reduce_max_sync(0xffffffffu, hi == win_hi ? static_cast<uint32_t>(best) : 0u);
+    const int win_e = static_cast<int>(~win_lo);
+    if ((win_e & 31) == lane) {
+#pragma unroll
+      for (int i = 0; i < PL; ++i)
+        if (i == (win_e >> 5)) key[i] = 0ull;
+    }
+    if (lane == j) sel_i = win_e;
+  }
+  // gates: softmax over the k selected logits, slot 0 holds the maximum
+  float sel_v = 0.f;
+#pragma unroll
+  for (int i = 0; i < PL; ++i) {
+    const float vi = __shfl_sync(0xffffffffu, v[i], sel_i & 31);
+    if (i == (sel_i >> 5)) sel_v = vi;
+  }
+  const float vmax = __shfl_sync(0xffffffffu, sel_v, 0);
+  const float ex = (lane < k) ? expf(sel_v - vmax) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const bool bad = (lane < k) && !isfinite(sel_v);
+  if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(err, MOE_DEVERR_NONFINITE);
+  if (lane < k) {
+    ids[static_cast<size_t>(t) * k + lane] = sel_i;
+    gates[static_cast<size_t>(t) * k + lane] = ex / sum;
+  }
+  return sel_i;
+}
+
+// Top-k of token t by one warp: sums the partial logits (split order fixed) and the bias,
+// optionally stores the logits, then selects (topk_select).
+template <int PL>
+MOE_DEVICE int topk_token(const float* __restrict__ parts, int nsplit, const float* __restrict__ bias,
+                          float* __restrict__ logits_out, int t, int T, int E, int k, int32_t* __restrict__ ids,
+                          float* __restrict__ gates, uint32_t* err) {
+  const int lane = threadIdx.x & 31;
+  // U partial matrices in flight at a time (one L2 round trip per U splits), added in order
+  constexpr int U = PL <= 8 ? 4 : (PL <= 16 ? 2 : 1);
+  float v[PL];
+#pragma unroll
+  for (int i = 0; i < PL; ++i) v[i] = 0.f;
+  for (int sp = 0; sp < nsplit; sp += U) {
+    float w[U][PL];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float* ps = parts + (static_cast<size_t>(sp + u) * T + t) * E;
+#pragma unroll
+      for (int i = 0; i < PL; ++i) {
+        const int e = lane + 32 * i;
+        w[u][i] = (e < E && sp + u < nsplit) ? ps[e] : 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int i = 0; i < PL; ++i)
+        if (sp + u < nsplit) v[i] = (sp + u == 0) ? w[u][i] : v[i] + w[u][i];
+  }
+#pragma unroll
+  for (int i = 0; i < PL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      if (bias) v[i] += bias[e];
+      if (logits_out) logits_out[static_cast<size_t>(t) * E + e] = v[i];
+    }
+  }
+  return topk_select<PL>(v, t, E, k, ids, gates, err);
+}
+
 template <int PL>
 __global__ void __launch_bounds__(topk_threads<PL>()) topk_kernel(const float* __restrict__ parts, int nsplit,
                                                                   const float* __restrict__ bias,
@@ -199,71 +375,8 @@ __global__ void __launch_bounds__(topk_threads<PL>()) topk_kernel(const float* _
   for (int tl = warp; tl < kChunk; tl += blockDim.x / 32) {
     const int t = c * kChunk + tl;
     if (t >= T) break;
-    // all loads of one partial matrix are issued together, then added (split order fixed)
-    float v[PL];
-#pragma unroll
-    for (int i = 0; i < PL; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = e < E ? parts[static_cast<size_t>(t) * E + e] : 0.f;
-    }
-    for (int sp = 1; sp < nsplit; ++sp) {
-      const float* ps = parts + (static_cast<size_t>(sp) * T + t) * E;
-      float w[PL];
-#pragma unroll
-      for (int i = 0; i < PL; ++i) {
-        const int e = lane + 32 * i;
-        w[i] = e < E ? ps[e] : 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < PL; ++i) v[i] += w[i];
-    }
-    uint64_t key[PL];
-#pragma unroll
-    for (int i = 0; i < PL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) {
-        if (bias) v[i] += bias[e];
-        if (logits_out) logits_out[static_cast<size_t>(t) * E + e] = v[i];
-        key[i] = rank_key(v[i], e);
-      } else {
-        key[i] = 0ull;
-      }
-    }
-    int sel_i = 0;  // lane j keeps the expert chosen in round j
-    for (int j = 0; j < k; ++j) {
-      uint64_t best = key[0];
-#pragma unroll
-      for (int i = 1; i < PL; ++i) best = key[i] > best ? key[i] : best;
-      const uint32_t hi = static_cast<uint32_t>(best >> 32);
-      const uint32_t win_hi = __reduce_max_sync(0xffffffffu, hi);
-      const uint32_t win_lo = __reduce_max_sync(0xffffffffu, hi == win_hi ? static_cast<uint32_t>(best) : 0u);
-      const int win_e = static_cast<int>(~win_lo);
-      if ((win_e & 31) == lane) {
-#pragma unroll
-        for (int i = 0; i < PL; ++i)
-          if (i == (win_e >> 5)) key[i] = 0ull;
-      }
-      if (lane == j) sel_i = win_e;
-    }
-    // gates: softmax over the k selected logits, slot 0 holds the maximum
-    float sel_v = 0.f;
-#pragma unroll
-    for (int i = 0; i < PL; ++i) {
-      const float vi = __shfl_sync(0xffffffffu, v[i], sel_i & 31);
-      if (i == (sel_i >> 5)) sel_v = vi;
-    }
-    const float vmax = __shfl_sync(0xffffffffu, sel_v, 0);
-    const float ex = (lane < k) ? expf(sel_v - vmax) : 0.f;
-    float sum = ex;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    const bool bad = (lane < k) && !isfinite(sel_v);
-    if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(err, MOE_DEVERR_NONFINITE);
-    if (lane < k) {
-      ids[static_cast<size_t>(t) * k + lane] = sel_i;
-      gates[static_cast<size_t>(t) * k + lane] = ex / sum;
-      if (masks) atomicOr(&smask[sel_i], 1u << tl);
-    }
+    const int sel = topk_token<PL>(parts, nsplit, bias, logits_out, t, T, E, k, ids, gates, err);
+    if (masks && lane < k) atomicOr(&smask[sel], 1u << tl);
   }
   if (masks) {
     __syncthreads();
@@ -524,6 +637,187 @@ cudaError_t launch_scatter(const int32_t* ids, const uint32_t* masks, const int3
   const int n_chunks = (T + kChunk - 1) / kChunk;
   return launch_pdl(scatter_kernel, dim3(n_chunks > 0 ? n_chunks : 1), dim3(kScanThreads), 0, st, ids, masks, chunk_base,
                     counts, T, E, k, n_chunks, perm, inv, offsets, segs, n_segs, max_segs, err);
+}
+
+// Routing and grouping of a small step in one launch.  One block per token adds its partial
+// logits (every load of the block issued at once; split order fixed, then the bias: the same
+// arithmetic as the top-k kernel) into shared memory, and one warp selects the top k and
+// publishes ids / gates.  The last block to finish (a counter the plan owns, reset by that
+// block) groups the step: per-chunk expert masks from the ids, counts, chunk bases, offsets,
+// segments and the stable scatter -- the rows of chunk_scan + scatter, without their
+// launches.  Needs route_small_ok(T, E, k, nsplit).
+constexpr int kSmallSplitsMax = 16;
+constexpr int kRgThreads = 256;
+constexpr int kRgPer = 4;  // experts per thread (E <= 1024)
+
+size_t route_small_smem(int T, int E, int k) {
+  const int nch = (T + kChunk - 1) / kChunk;
+  const size_t grouping = (2 * static_cast<size_t>(nch) * E + static_cast<size_t>(T) * k + E + 1) * 4;
+  const size_t logits = static_cast<size_t>(E) * 4;
+  return grouping > logits ? grouping : logits;
+}
+
+template <int PL>
+__global__ void __launch_bounds__(kRgThreads) route_group_kernel(
+    const float* __restrict__ parts, int nsplit, const float* __restrict__ bias, int T, int E, int k,
+    int32_t* __restrict__ ids, float* __restrict__ gates, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ perm, int32_t* __restrict__ inv, Seg* segs, int32_t* n_segs, int max_segs,
+    uint32_t* done, uint32_t* err) {
+  extern __shared__ uint32_t sm[];
+  __shared__ int s_last;
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x;
+  {
+    float* slog = reinterpret_cast<float*>(sm);  // [E]
+    float w[kRgPer][kSmallSplitsMax];
+#pragma unroll
+    for (int q = 0; q < kRgPer; ++q) {
+      const int e = threadIdx.x + kRgThreads * q;
+#pragma unroll
+      for (int sp = 0; sp < kSmallSplitsMax; ++sp)
+        w[q][sp] = (e < E && sp < nsplit) ? parts[(static_cast<size_t>(sp) * T + t) * E + e] : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < kRgPer; ++q) {
+      const int e = threadIdx.x + kRgThreads * q;
+      if (e < E) {
+        float v = w[q][0];
+#pragma unroll
+        for (int sp = 1; sp < kSmallSplitsMax; ++sp)
+          if (sp < nsplit) v += w[q][sp];
+        if (bias) v += bias[e];
+        slog[e] = v;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      float v[PL];
+#pragma unroll
+      for (int i = 0; i < PL; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = e < E ? slog[e] : 0.f;
+      }
+      topk_select<PL>(v, t, E, k, ids, gates, err);
+    }
+  }
+  // publish this token's ids, then count finished blocks
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // ---- grouping, by the last block ----
+  const int nch = (T + kChunk - 1) / kChunk;
+  uint32_t* smask = sm;                                       // [e][c]: bit tl = token c*32+tl chose e
+  int32_t* scb = reinterpret_cast<int32_t*>(smask + nch * E);  // [e][c]: rows of e before chunk c
+  int32_t* sids = scb + nch * E;                              // [T][k]
+  int* s_off = sids + T * k;                                  // [E + 1]
+  for (int i = threadIdx.x; i < nch * E; i += kRgThreads) smask[i] = 0u;
+  for (int i = threadIdx.x; i < T * k; i += kRgThreads) sids[i] = __ldcg(ids + i);
+  __syncthreads();
+  for (int a = threadIdx.x; a < T * k; a += kRgThreads) {
+    const int tt = a / k, j = a % k;
+    const int e = sids[a];
+    if (assignment_valid(sids + tt * k, j, e, E)) atomicOr(&smask[e * nch + tt / kChunk], 1u << (tt % kChunk));
+  }
+  __syncthreads();
+  // experts threadIdx.x * per + q, q < per (contiguous, so one block scan orders them)
+  const int per = (E + kRgThreads - 1) / kRgThreads;  // <= kRgPer
+  int cl[kRgPer], mine = 0;
+#pragma unroll
+  for (int q = 0; q < kRgPer; ++q) {
+    cl[q] = 0;
+    const int e = threadIdx.x * per + q;
+    if (q < per && e < E) {
+      int run = 0;
+      for (int c = 0; c < nch; ++c) {
+        scb[e * nch + c] = run;
+        run += __popc(smask[e * nch + c]);
+      }
+      counts[e] = run;
+      cl[q] = run;
+      mine += run;
+    }
+  }
+  int total;
+  int base = block_exclusive_scan(mine, &total);
+#pragma unroll
+  for (int q = 0; q < kRgPer; ++q) {
+    const int e = threadIdx.x * per + q;
+    if (q < per && e < E) s_off[e] = base;
+    base += cl[q];
+  }
+  if (threadIdx.x == 0) s_off[E] = total;
+  if (segs) {
+    int nsl[kRgPer], ns_mine = 0;
+#pragma unroll
+    for (int q = 0; q < kRgPer; ++q) {
+      const int e = threadIdx.x * per + q;
+      nsl[q] = (q < per && e < E) ? num_segments(cl[q]) : 0;
+      ns_mine += nsl[q];
+    }
+    int seg_total;
+    int sbase = block_exclusive_scan(ns_mine, &seg_total);  // also publishes s_off (barriers)
+#pragma unroll
+    for (int q = 0; q < kRgPer; ++q) {
+      const int e = threadIdx.x * per + q;
+      if (q < per && e < E) write_segments(segs, sbase, max_segs, e, s_off[e], cl[q], err);
+      sbase += nsl[q];
+    }
+    if (threadIdx.x == 0) *n_segs = min(seg_total, max_segs);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += kRgThreads) offsets[e] = s_off[e];
+  for (int a = threadIdx.x; a < T * k; a += kRgThreads) {
+    const int tt = a / k, j = a % k;
+    const int32_t* row = sids + tt * k;
+    const int e = row[j];
+    if (!assignment_valid(row, j, e, E)) {
+      inv[a] = -1;
+      continue;
+    }
+    const int c = tt / kChunk, tl = tt % kChunk;
+    const int r = s_off[e] + scb[e * nch + c] + __popc(smask[e * nch + c] & ((1u << tl) - 1u));
+    perm[r] = a;
+    inv[a] = r;
+  }
+  if (threadIdx.x == 0) *done = 0u;  // ready for the next launch (stream-ordered)
+}
+
+bool route_small_ok(int T, int E, int k, int nsplit) {
+  return T > 0 && T <= kSmallRouteT && E <= kRgThreads * kRgPer && nsplit <= kSmallSplitsMax &&
+         route_small_smem(T, E, k) <= 48 * 1024;
+}
+
+template <int PL>
+static cudaError_t launch_route_small_pl(const float* parts, int nsplit, const float* bias, int T, int E, int k,
+                                         int32_t* ids, float* gates, int32_t* counts, int32_t* offsets, int32_t* perm,
+                                         int32_t* inv, Seg* segs, int32_t* n_segs, int max_segs, uint32_t* done,
+                                         uint32_t* err, cudaStream_t st) {
+  return launch_pdl(route_group_kernel<PL>, dim3(T), dim3(kRgThreads), route_small_smem(T, E, k), st, parts, nsplit,
+                    bias, T, E, k, ids, gates, counts, offsets, perm, inv, segs, n_segs, max_segs, done, err);
+}
+
+cudaError_t launch_route_small(const float* parts, int nsplit, const float* bias, int T, int E, int k, int32_t* ids,
+                               float* gates, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, Seg* segs,
+                               int32_t* n_segs, int max_segs, uint32_t* done, uint32_t* err, cudaStream_t st) {
+  if (!route_small_ok(T, E, k, nsplit)) return cudaErrorInvalidValue;
+  const int pl = (E + 31) / 32;
+#define MOE_RS(PLV)                                                                                             \
+  launch_route_small_pl<PLV>(parts, nsplit, bias, T, E, k, ids, gates, counts, offsets, perm, inv, segs, n_segs, \
+                             max_segs, done, err, st)
+  if (pl <= 1) return MOE_RS(1);
+  if (pl <= 2) return MOE_RS(2);
+  if (pl <= 4) return MOE_RS(4);
+  if (pl <= 8) return MOE_RS(8);
+  if (pl <= 12) return MOE_RS(12);
+  if (pl <= 16) return MOE_RS(16);
+  return MOE_RS(32);
+#undef MOE_RS
 }
 
 // Segment list from offsets only (the separate experts entry point).  One block of 256 threads.

@@ -173,14 +173,16 @@ __global__ void __launch_bounds__(320, 1)
 
 }  // namespace rt
 
-// K splits: at least ceil(d / 512) (short accumulation chains), more (up to 8) while the grid
-// is below one CTA per SM, at most one split per 64-wide K chunk.
+// K splits: at least ceil(d / 512) (short accumulation chains), more while the grid is below
+// one CTA per SM (up to 8; 16 for a single token tile, where the whole grid is a few CTAs), at
+// most one split per 64-wide K chunk.
 int router_tc_splits(int T, int E, int d, int num_sms) {
   const int tiles = (E / rt::BM) * ((T + rt::BN - 1) / rt::BN);
   const int nk = d / rt::BK;
   int s = tiles > 0 ? num_sms / tiles : 1;
   const int s_min = (nk + 7) / 8;
-  if (s > 8) s = 8;                  // the top-k kernel reads every partial
+  const int s_cap = T <= rt::BN ? 16 : 8;  // the top-k reads every partial
+  if (s > s_cap) s = s_cap;
   if (s < s_min) s = s_min;
   if (s > nk) s = nk;
   if (s < 1) s = 1;
