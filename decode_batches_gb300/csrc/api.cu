@@ -695,7 +695,14 @@ extern "C" moe_status moe_layer_forward(moe_plan* p, const void* x, int T, int n
   const int n_chunks = (T + kChunk - 1) / kChunk;
   const bool tc = use_tc(p);
   Seg* segs = tc ? ws_ptr<Seg>(p, p->L.segs) : nullptr;
-  if (route_small_ok(T, p->E, p->k, router_nsplit(p, T))) {
+  if (router_nsplit(p, T) == router_small_splits(p->d) && !(p->router_tc && T > kRouterTcMinT) &&
+      router_route_tiny_ok(T, p->E, p->d, p->k)) {
+    // tiny step: router, top-k and grouping in one launch
+    LAUNCH(p, "router_route", st,
+           launch_router_route_tiny(xb, p->w_router, p->b_router, T, p->E, p->d, ws_ptr<float>(p, p->L.parts), p->k,
+                                    ids, gates, counts, offsets, perm, inv, segs, ws_ptr<int32_t>(p, p->L.n_segs),
+                                    p->L.max_segs, p->err + 1, p->err, st));
+  } else if (route_small_ok(T, p->E, p->k, router_nsplit(p, T))) {
     // small step: the whole routing and grouping in one block after the router
     const float* parts = nullptr;
     const float* bias = nullptr;

@@ -22,20 +22,28 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     s_g[threadIdx.x] = gates[static_cast<size_t>(t) * k + threadIdx.x];
   }
   __syncthreads();
+  const uint64_t pol = l2_policy_evict_first();  // y and y_s are read once, here
   for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      const int r = s_row[j];
-      if (r < 0) continue;
-      const uint4 v = *reinterpret_cast<const uint4*>(y + static_cast<size_t>(r) * d + c);
-      float yf[8];
-      f16x8_to_f32(v, yf);
-      const float g = s_g[j];
+    for (int j0 = 0; j0 < k; j0 += 8) {  // the loads of 8 slots are in flight together
+      uint4 v[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = fmaf(g, yf[q], acc[q]);
+      for (int u = 0; u < 8; ++u) {
+        const int r = j0 + u < k ? s_row[j0 + u] : -1;
+        v[u] = r >= 0 ? ld_global_v4_hint(y + static_cast<size_t>(r) * d + c, pol) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (j0 + u >= k || s_row[j0 + u] < 0) continue;
+        float yf[8];
+        f16x8_to_f32(v[u], yf);
+        const float g = s_g[j0 + u];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = fmaf(g, yf[q], acc[q]);
+      }
     }
     if (ys) {
-      const uint4 v = *reinterpret_cast<const uint4*>(ys + static_cast<size_t>(t) * d + c);
+      const uint4 v = ld_global_v4_hint(ys + static_cast<size_t>(t) * d + c, pol);
       float sf[8];
       f16x8_to_f32(v, sf);
 #pragma unroll

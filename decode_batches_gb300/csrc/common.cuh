@@ -182,6 +182,26 @@ MOE_DEVICE void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, in
       : "memory");
 }
 
+// Raise the phase's expected transaction bytes without arriving (the arrival comes later).
+MOE_DEVICE void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// 16-byte global load / store with an L2 eviction policy (intermediates that should stay in,
+// or leave, L2 between the kernel that writes them and the one that reads them).
+MOE_DEVICE uint4 ld_global_v4_hint(const void* p, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
+}
+MOE_DEVICE void st_global_v4_hint(void* p, const uint4& v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w), "l"(policy)
+               : "memory");
+}
+
 // Bulk copy of `bytes` contiguous bytes (multiple of 16, both addresses 16-byte aligned) into
 // shared memory, completing `bytes` transactions on the mbarrier.
 MOE_DEVICE void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t policy) {

@@ -68,6 +68,13 @@ struct Unit {
   int tile;       // 128-row weight tile index
 };
 
+MOE_DEVICE Seg load_seg(const Seg* p) {
+  const int4 lo = __ldcg(reinterpret_cast<const int4*>(p));
+  const int4 hi = __ldcg(reinterpret_cast<const int4*>(p) + 1);
+  return Seg{lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+}
+
+template <bool kL2 = false>
 MOE_DEVICE Unit decode_unit(int u, const TcArgs& a, int tiles_r, int tiles_s, int n_shared_units) {
   Unit un;
   if (u < n_shared_units) {
@@ -82,10 +89,12 @@ MOE_DEVICE Unit decode_unit(int u, const TcArgs& a, int tiles_r, int tiles_s, in
   } else {
     // The parts [first, first + nparts) of one expert own units [first, first + nparts) * tiles;
     // inside that range the tile index is the slow one and the part the fast one.
+    // kL2: read the segment records through L2 (the down kernel's producer reads them before
+    // its grid-dependency wait, so nothing may come from a stale L1 line)
     const int v = u - n_shared_units;
-    const Seg any = a.segs[v / tiles_r];
+    const Seg any = kL2 ? load_seg(a.segs + v / tiles_r) : a.segs[v / tiles_r];
     const int o = v - any.first * tiles_r;
-    const Seg s = a.segs[any.first + o % any.nparts];
+    const Seg s = kL2 ? load_seg(a.segs + any.first + o % any.nparts) : a.segs[any.first + o % any.nparts];
     un.shared = 0;
     un.expert = s.expert;
     un.tile = o / any.nparts;
@@ -139,13 +148,21 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_trigger();
-  pdl_wait();  // the predecessor's outputs (segments, perm, h) are visible from here on
+  // gate/up lets its dependents start only once its own predecessors (the routing) are
+  // complete, so the down kernel may read the unit list -- and stream its first weight stages
+  // -- before its grid-dependency wait; everything that reads h waits.
+  if (kGateUp) {
+    pdl_wait();
+    pdl_trigger();
+  } else {
+    pdl_trigger();
+    if (warp != 0) pdl_wait();
+  }
 
   const int tiles_r = kGateUp ? a.f / 64 : a.d / BM;
   const int tiles_s = kGateUp ? (a.n_shared * a.f_s) / 64 : a.d / BM;
   const int n_shared_units = a.n_shared ? a.n_shared_segs * tiles_s : 0;
-  const int n_routed_units = a.routed ? (*a.n_segs) * tiles_r : 0;
+  const int n_routed_units = a.routed ? __ldcg(a.n_segs) * tiles_r : 0;
   const int total_units = n_shared_units + n_routed_units;
   const int nk_r = kGateUp ? a.d / BK : a.f / BK;
   const int nk_s = kGateUp ? a.d / BK : (a.n_shared * a.f_s) / BK;
@@ -154,6 +171,23 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
     // ---------------- TMA producer ----------------
     const uint64_t pol_w = l2_policy_evict_first();
     const uint64_t pol_act = l2_policy_evict_last();
+    uint32_t pre = 0;  // down: stages whose weights were requested before the dependency wait
+    if (!kGateUp) {
+      for (int u = blockIdx.x; u < total_units && pre < static_cast<uint32_t>(kStages); u += gridDim.x) {
+        const Unit un = decode_unit<true>(u, a, tiles_r, tiles_s, n_shared_units);
+        const int nk = un.shared ? nk_s : nk_r;
+        const uint16_t* wbase = un.shared ? a.w_down_s + static_cast<size_t>(un.tile) * nk * kTileElems
+                                          : a.w_down + (static_cast<size_t>(un.expert) * tiles_r + un.tile) * nk * kTileElems;
+        for (int kk = 0; kk < nk && pre < static_cast<uint32_t>(kStages); ++kk, ++pre) {
+          if (elect_one()) {  // a fresh slot: no wait; the arrival comes with the h rows below
+            mbar_expect_tx(&full[pre], kABytes);
+            bulk_load(smem + pre * kStageBytes, wbase + static_cast<size_t>(kk) * kTileElems, kABytes, &full[pre], pol_w);
+          }
+          __syncwarp();
+        }
+      }
+      pdl_wait();
+    }
     uint32_t g = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
@@ -173,8 +207,9 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
         if (!(ok = mbar_wait_warp(&empty[slot], ((g / kStages) & 1u) ^ 1u, abort_flag, a.err))) break;
         if (elect_one()) {
           uint8_t* sa = smem + slot * kStageBytes;
-          mbar_arrive_expect_tx(&full[slot], kABytes + nbox * 32 * BK * 2);
-          bulk_load(sa, wbase + static_cast<size_t>(kk) * kTileElems, kABytes, &full[slot], pol_w);
+          const bool early = g < pre;  // weights already requested
+          mbar_arrive_expect_tx(&full[slot], (early ? 0 : kABytes) + nbox * 32 * BK * 2);
+          if (!early) bulk_load(sa, wbase + static_cast<size_t>(kk) * kTileElems, kABytes, &full[slot], pol_w);
           if (!kGateUp)
             for (int i = 0; i < nbox; ++i)
               tma_load_2d(sa + kABytes + i * 32 * BK * 2, hm, &full[slot], kk * BK, un.row_start + 32 * i, pol_act);

@@ -48,6 +48,13 @@ cudaError_t launch_router_parts_small(const uint16_t* x, const float* w_router, 
 // Top-k + counts + offsets + segments + stable permutation of a small step in one launch.
 constexpr int kSmallRouteT = 64;
 bool route_small_ok(int T, int E, int k, int nsplit);
+// Router + top-k + grouping of a step of at most 8 tokens (d % 128 == 0) in one launch.
+bool router_route_tiny_ok(int T, int E, int d, int k);
+cudaError_t launch_router_route_tiny(const uint16_t* x, const float* w_router, const float* bias, int T, int E, int d,
+                                     float* parts, int k, int32_t* ids, float* gates, int32_t* counts,
+                                     int32_t* offsets, int32_t* perm, int32_t* inv, Seg* segs, int32_t* n_segs,
+                                     int max_segs, uint32_t* done, uint32_t* err, cudaStream_t st);
+
 // `done`: a device counter that is 0 between launches (the last block resets it).
 cudaError_t launch_route_small(const float* parts, int nsplit, const float* bias, int T, int E, int k, int32_t* ids,
                                float* gates, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, Seg* segs,

@@ -151,13 +151,9 @@ constexpr int kRouterKS = 512;
 
 int router_small_splits(int d) { return (d + kRouterKS - 1) / kRouterKS; }
 
-template <int G>  // tokens per group, a power of two <= 32
-__global__ void __launch_bounds__(256) router_parts_small_kernel(const uint16_t* __restrict__ x,
-                                                                 const float* __restrict__ wr, int T, int E, int d,
-                                                                 float* __restrict__ parts) {
-  __shared__ __align__(16) uint16_t xs[G * kRouterKS];
-  pdl_trigger();
-  pdl_wait();
+template <int G>  // tokens per group, a power of two <= 32; xs: G * kRouterKS shared elements
+MOE_DEVICE void router_parts_block(const uint16_t* __restrict__ x, const float* __restrict__ wr, int T, int E, int d,
+                                   float* __restrict__ parts, uint16_t* xs) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * 8 + warp;
   const int sp = blockIdx.y;
@@ -218,6 +214,16 @@ __global__ void __launch_bounds__(256) router_parts_small_kernel(const uint16_t*
       if (lane < nt) parts[(static_cast<size_t>(sp) * T + t0 + lane) * E + e] = acc[0];
     }
   }
+}
+
+template <int G>
+__global__ void __launch_bounds__(256) router_parts_small_kernel(const uint16_t* __restrict__ x,
+                                                                 const float* __restrict__ wr, int T, int E, int d,
+                                                                 float* __restrict__ parts) {
+  __shared__ __align__(16) uint16_t xs[G * kRouterKS];
+  pdl_trigger();
+  pdl_wait();
+  router_parts_block<G>(x, wr, T, E, d, parts, xs);
 }
 
 cudaError_t launch_router_parts_small(const uint16_t* x, const float* w_router, int T, int E, int d, float* parts,
@@ -657,67 +663,19 @@ size_t route_small_smem(int T, int E, int k) {
   return grouping > logits ? grouping : logits;
 }
 
-template <int PL>
-__global__ void __launch_bounds__(kRgThreads) route_group_kernel(
-    const float* __restrict__ parts, int nsplit, const float* __restrict__ bias, int T, int E, int k,
-    int32_t* __restrict__ ids, float* __restrict__ gates, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-    int32_t* __restrict__ perm, int32_t* __restrict__ inv, Seg* segs, int32_t* n_segs, int max_segs,
-    uint32_t* done, uint32_t* err) {
-  extern __shared__ uint32_t sm[];
-  __shared__ int s_last;
-  pdl_trigger();
-  pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x;
-  {
-    float* slog = reinterpret_cast<float*>(sm);  // [E]
-    float w[kRgPer][kSmallSplitsMax];
-#pragma unroll
-    for (int q = 0; q < kRgPer; ++q) {
-      const int e = threadIdx.x + kRgThreads * q;
-#pragma unroll
-      for (int sp = 0; sp < kSmallSplitsMax; ++sp)
-        w[q][sp] = (e < E && sp < nsplit) ? parts[(static_cast<size_t>(sp) * T + t) * E + e] : 0.f;
-    }
-#pragma unroll
-    for (int q = 0; q < kRgPer; ++q) {
-      const int e = threadIdx.x + kRgThreads * q;
-      if (e < E) {
-        float v = w[q][0];
-#pragma unroll
-        for (int sp = 1; sp < kSmallSplitsMax; ++sp)
-          if (sp < nsplit) v += w[q][sp];
-        if (bias) v += bias[e];
-        slog[e] = v;
-      }
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      float v[PL];
-#pragma unroll
-      for (int i = 0; i < PL; ++i) {
-        const int e = lane + 32 * i;
-        v[i] = e < E ? slog[e] : 0.f;
-      }
-      topk_select<PL>(v, t, E, k, ids, gates, err);
-    }
-  }
-  // publish this token's ids, then count finished blocks
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(done, 1u) == gridDim.x - 1;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-
-  // ---- grouping, by the last block ----
+// Grouping of a small step by one block of kRgThreads threads, from the step's ids held in
+// shared memory: per-chunk expert masks, counts, chunk bases, offsets, segments and the
+// stable scatter (the rows of chunk_scan + scatter).  sm: [2 n_chunks E] words of scratch, then
+// ids [T][k], then [E + 1] words.
+MOE_DEVICE void group_small(int T, int E, int k, uint32_t* sm, int32_t* __restrict__ counts,
+                            int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                            Seg* segs, int32_t* n_segs, int max_segs, uint32_t* err) {
   const int nch = (T + kChunk - 1) / kChunk;
-  uint32_t* smask = sm;                                       // [e][c]: bit tl = token c*32+tl chose e
+  uint32_t* smask = sm;                                        // [e][c]: bit tl = token c*32+tl chose e
   int32_t* scb = reinterpret_cast<int32_t*>(smask + nch * E);  // [e][c]: rows of e before chunk c
-  int32_t* sids = scb + nch * E;                              // [T][k]
-  int* s_off = sids + T * k;                                  // [E + 1]
+  int32_t* sids = scb + nch * E;                               // [T][k]
+  int* s_off = sids + T * k;                                   // [E + 1]
   for (int i = threadIdx.x; i < nch * E; i += kRgThreads) smask[i] = 0u;
-  for (int i = threadIdx.x; i < T * k; i += kRgThreads) sids[i] = __ldcg(ids + i);
   __syncthreads();
   for (int a = threadIdx.x; a < T * k; a += kRgThreads) {
     const int tt = a / k, j = a % k;
@@ -785,7 +743,163 @@ __global__ void __launch_bounds__(kRgThreads) route_group_kernel(
     perm[r] = a;
     inv[a] = r;
   }
+}
+
+template <int PL>
+__global__ void __launch_bounds__(kRgThreads) route_group_kernel(
+    const float* __restrict__ parts, int nsplit, const float* __restrict__ bias, int T, int E, int k,
+    int32_t* __restrict__ ids, float* __restrict__ gates, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ perm, int32_t* __restrict__ inv, Seg* segs, int32_t* n_segs, int max_segs,
+    uint32_t* done, uint32_t* err) {
+  extern __shared__ uint32_t sm[];
+  __shared__ int s_last;
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x;
+  {
+    float* slog = reinterpret_cast<float*>(sm);  // [E]
+    float w[kRgPer][kSmallSplitsMax];
+#pragma unroll
+    for (int q = 0; q < kRgPer; ++q) {
+      const int e = threadIdx.x + kRgThreads * q;
+#pragma unroll
+      for (int sp = 0; sp < kSmallSplitsMax; ++sp)
+        w[q][sp] = (e < E && sp < nsplit) ? parts[(static_cast<size_t>(sp) * T + t) * E + e] : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < kRgPer; ++q) {
+      const int e = threadIdx.x + kRgThreads * q;
+      if (e < E) {
+        float v = w[q][0];
+#pragma unroll
+        for (int sp = 1; sp < kSmallSplitsMax; ++sp)
+          if (sp < nsplit) v += w[q][sp];
+        if (bias) v += bias[e];
+        slog[e] = v;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      float v[PL];
+#pragma unroll
+      for (int i = 0; i < PL; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = e < E ? slog[e] : 0.f;
+      }
+      topk_select<PL>(v, t, E, k, ids, gates, err);
+    }
+  }
+  // publish this token's ids, then count finished blocks
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // ---- grouping, by the last block ----
+  const int nch = (T + kChunk - 1) / kChunk;
+  int32_t* sids = reinterpret_cast<int32_t*>(sm) + 2 * nch * E;
+  for (int i = threadIdx.x; i < T * k; i += kRgThreads) sids[i] = __ldcg(ids + i);
+  __syncthreads();
+  group_small(T, E, k, sm, counts, offsets, perm, inv, segs, n_segs, max_segs, err);
   if (threadIdx.x == 0) *done = 0u;  // ready for the next launch (stream-ordered)
+}
+
+// Router, top-k and grouping of a step of at most 8 tokens in one launch: every block forms its
+// K-split partial logits (router_parts_block); the last block to finish adds them (split order,
+// then the bias, as the top-k kernel does), selects each token's top k with one warp per token
+// and groups the step (group_small).
+template <int PL>
+__global__ void __launch_bounds__(kRgThreads) router_route_tiny_kernel(
+    const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias, int T, int E,
+    int d, float* __restrict__ parts, int k, int32_t* __restrict__ ids, float* __restrict__ gates,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+    int32_t* __restrict__ inv, Seg* segs, int32_t* n_segs, int max_segs, uint32_t* done, uint32_t* err) {
+  extern __shared__ __align__(16) uint32_t sm[];
+  __shared__ int s_last;
+  pdl_trigger();
+  pdl_wait();
+  router_parts_block<8>(x, wr, T, E, d, parts, reinterpret_cast<uint16_t*>(sm));
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(done, 1u) == gridDim.x * gridDim.y - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int nsplit = gridDim.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int32_t* sids = reinterpret_cast<int32_t*>(sm) + 2 * E;  // one chunk: T <= 8
+  if (warp < T) {
+    const int t = warp;
+    float v[PL], bv[PL];
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+      v[i] = 0.f;
+      bv[i] = (bias && lane + 32 * i < E) ? bias[lane + 32 * i] : 0.f;  // in flight with the partials
+    }
+    for (int sp = 0; sp < nsplit; sp += 4) {  // partials of other blocks: read through L2
+      float w[4][PL];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int i = 0; i < PL; ++i) {
+          const int e = lane + 32 * i;
+          w[u][i] = (e < E && sp + u < nsplit) ? __ldcg(parts + (static_cast<size_t>(sp + u) * T + t) * E + e) : 0.f;
+        }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int i = 0; i < PL; ++i)
+          if (sp + u < nsplit) v[i] = (sp + u == 0) ? w[u][i] : v[i] + w[u][i];
+    }
+    if (bias)
+#pragma unroll
+      for (int i = 0; i < PL; ++i) v[i] += bv[i];
+    const int sel = topk_select<PL>(v, t, E, k, ids, gates, err);
+    if (lane < k) sids[t * k + lane] = sel;
+  }
+  __syncthreads();
+  group_small(T, E, k, sm, counts, offsets, perm, inv, segs, n_segs, max_segs, err);
+  if (threadIdx.x == 0) *done = 0u;  // ready for the next launch (stream-ordered)
+}
+
+bool router_route_tiny_ok(int T, int E, int d, int k) {
+  return T > 0 && T <= 8 && d % 128 == 0 && E <= kRgThreads * kRgPer && router_small_splits(d) <= kSmallSplitsMax &&
+         route_small_smem(T, E, k) <= 48 * 1024;
+}
+
+template <int PL>
+static cudaError_t launch_rrt_pl(const uint16_t* x, const float* wr, const float* bias, int T, int E, int d,
+                                 float* parts, int k, int32_t* ids, float* gates, int32_t* counts, int32_t* offsets,
+                                 int32_t* perm, int32_t* inv, Seg* segs, int32_t* n_segs, int max_segs, uint32_t* done,
+                                 uint32_t* err, cudaStream_t st) {
+  const size_t xs_bytes = 8 * kRouterKS * 2;
+  const size_t g_bytes = route_small_smem(T, E, k);
+  dim3 grid((E + 7) / 8, router_small_splits(d));
+  return launch_pdl(router_route_tiny_kernel<PL>, grid, dim3(kRgThreads), xs_bytes > g_bytes ? xs_bytes : g_bytes, st,
+                    x, wr, bias, T, E, d, parts, k, ids, gates, counts, offsets, perm, inv, segs, n_segs, max_segs,
+                    done, err);
+}
+
+cudaError_t launch_router_route_tiny(const uint16_t* x, const float* w_router, const float* bias, int T, int E, int d,
+                                     float* parts, int k, int32_t* ids, float* gates, int32_t* counts,
+                                     int32_t* offsets, int32_t* perm, int32_t* inv, Seg* segs, int32_t* n_segs,
+                                     int max_segs, uint32_t* done, uint32_t* err, cudaStream_t st) {
+  if (!router_route_tiny_ok(T, E, d, k)) return cudaErrorInvalidValue;
+  const int pl = (E + 31) / 32;
+#define MOE_RRT(PLV)                                                                                            \
+  launch_rrt_pl<PLV>(x, w_router, bias, T, E, d, parts, k, ids, gates, counts, offsets, perm, inv, segs, n_segs, \
+                     max_segs, done, err, st)
+  if (pl <= 1) return MOE_RRT(1);
+  if (pl <= 2) return MOE_RRT(2);
+  if (pl <= 4) return MOE_RRT(4);
+  if (pl <= 8) return MOE_RRT(8);
+  if (pl <= 12) return MOE_RRT(12);
+  if (pl <= 16) return MOE_RRT(16);
+  return MOE_RRT(32);
+#undef MOE_RRT
 }
 
 bool route_small_ok(int T, int E, int k, int nsplit) {
