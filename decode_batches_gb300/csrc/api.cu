@@ -2,6 +2,7 @@
 // sequence of each entry point (see include/moe.h for the contract of every call).
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -577,6 +578,20 @@ static FfnWeights ffn_weights(const moe_plan* p) {
 
 // Expert FFN over grouped rows; y/y_s outputs, h/h_s in the workspace.  For the tensor-core
 // path `segs`/`n_segs` must already describe the routed segments.
+// Weight tiles per unit of the 16-bit grouped GEMMs: 2 (the pair shares each token-row stage:
+// half the activation traffic, and twice the weight bytes in flight per stage) unless that
+// leaves fewer units than a quarter of the SMs, where single tiles double the parallelism.  The
+// routed unit count is estimated from the number of segments, about min(E, T k) + T k / 128.
+static int tc_pair(const moe_plan* p, int T, bool routed, bool gate_up) {
+  const long tiles_r = gate_up ? p->f / 64 : p->d / 128;
+  const long tiles_s = gate_up ? static_cast<long>(p->n_shared) * p->f_s / 64 : p->d / 128;
+  const long R = static_cast<long>(T) * p->k;
+  const long segs_r = routed ? std::min<long>(p->E, R) + R / kSegRowsMax : 0;
+  const long segs_s = p->n_shared > 0 ? (T + kSegRowsMax - 1) / kSegRowsMax : 0;
+  const long units2 = segs_r * ((tiles_r + 1) / 2) + segs_s * ((tiles_s + 1) / 2);
+  return 4 * units2 >= p->num_sms ? 2 : 1;
+}
+
 static moe_status run_experts(moe_plan* p, const uint16_t* x, int T, const int32_t* offsets, const int32_t* perm,
                               uint16_t* y, uint16_t* y_s, cudaStream_t st) {
   uint16_t* h = ws_ptr<uint16_t>(p, p->L.h);
@@ -616,11 +631,15 @@ static moe_status run_experts(moe_plan* p, const uint16_t* x, int T, const int32
       LAUNCH(p, "fp4_gateup", st, launch_fp4_gateup(&p->maps, a, p->num_sms, st));
       TcArgs sh = a;
       sh.routed = 0;
+      sh.pair = tc_pair(p, T, false, true);
       if (p->n_shared > 0) LAUNCH(p, "tc_gateup_shared", st, launch_tc_gateup(&p->maps, sh, p->num_sms, st));
       LAUNCH(p, "fp4_down", st, launch_fp4_down(&p->maps, a, p->num_sms, st));
+      sh.pair = tc_pair(p, T, false, false);
       if (p->n_shared > 0) LAUNCH(p, "tc_down_shared", st, launch_tc_down(&p->maps, sh, p->num_sms, st));
     } else {
+      a.pair = tc_pair(p, T, true, true);
       LAUNCH(p, "tc_gateup", st, launch_tc_gateup(&p->maps, a, p->num_sms, st));
+      a.pair = tc_pair(p, T, true, false);
       LAUNCH(p, "tc_down", st, launch_tc_down(&p->maps, a, p->num_sms, st));
     }
   } else {

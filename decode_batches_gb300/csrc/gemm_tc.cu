@@ -2,7 +2,8 @@
 //
 // The grouped problem is a list of segments: consecutive grouped rows of one routed expert
 // (at most 128), or consecutive tokens for the shared experts.  Each unit of work is one
-// segment times one 128-row tile of that expert's weight matrix.  The MMA computes
+// segment times a pair of 128-row tiles of that expert's weight matrix (two MMAs per K step
+// share the segment's B stage, which halves the token-row traffic).  The MMA computes
 //     D[weight row][token] = W[128 x K] . X[N x K]^T
 // ("swap-AB": the weight tile is the M=128 operand, the segment's tokens are N <= 128), so the
 // weights -- the bytes that bound this layer -- stream through shared memory exactly once per
@@ -25,12 +26,13 @@
 //   warp 0      producer: A by bulk copy; B by TMA (down kernel)
 //   warp 1      TMEM owner and MMA issuer
 //   warps 2-5   epilogue (TMEM lanes 32*(warp%4) .. +31)
-//   warps 6-17  gate/up only: cp.async gather of the token rows, two warps per stage slot
+//   warps 6-13  gate/up only: cp.async gather of the token rows, two warps per stage slot
 // Producer and MMA loops run converged and issue under elect_one() (warp-uniform operands: an
 // MMA issues in a few tens of cycles), and the MMA warp probes the next stage's barrier before
 // issuing the current stage, so the barrier round trip hides behind the issue.
-// Pipeline: 6 shared-memory stages of (A 16 KB + B up to 16 KB), two TMEM accumulators of up
-// to 128 fp32 columns so the epilogue of one unit overlaps the main loop of the next.  An
+// Pipeline: 4 shared-memory stages of (2 x A 16 KB + B up to 16 KB); two TMEM accumulator pairs
+// (2 x 2 x 128 fp32 columns, all 512) so the epilogue of one unit overlaps the main loop of the
+// next.  An
 // expert with more than 128 rows is split into parts; the units of its parts are ordered
 // tile-major (tile 0 of every part, then tile 1, ...) so that CTAs working on the same
 // weight tile run side by side and the second read of the tile is served by L2.
@@ -44,14 +46,15 @@
 namespace moe {
 namespace tc {
 
-constexpr int BM = 128;                          // weight rows per unit (MMA M)
+constexpr int BM = 128;                          // weight rows per tile (MMA M)
 constexpr int BK = 64;                           // K elements per stage (128-byte rows)
-constexpr int kStages = 6;
-constexpr int kABytes = BM * BK * 2;             // 16 KB
+constexpr int kPair = 2;                         // weight tiles per unit (sharing the B stage)
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK * 2;             // 16 KB per tile
 constexpr int kBBytes = kSegRowsMax * BK * 2;    // 16 KB (N <= 128)
-constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kTmemCols = 2 * kSegRowsMax;       // 2 accumulators x 128 columns
+constexpr int kStageBytes = kPair * kABytes + kBBytes;  // 48 KB
 constexpr int kAccCols = kSegRowsMax;
+constexpr int kTmemCols = 2 * kPair * kAccCols;  // 2 buffers x 2 tiles x 128 columns = 512
 constexpr int kGatherPerSlot = 2;                // gate/up B producers per stage slot
 constexpr int kGatherWarps = kGatherPerSlot * kStages;
 constexpr int kTokBytes = kGatherWarps * kSegRowsMax * 4;  // per gather warp: token of each row
@@ -65,7 +68,8 @@ struct Unit {
   int expert;     // routed expert (shared: -1)
   int row_start;  // grouped row (routed) or token (shared) of column 0
   int rows;       // valid columns
-  int tile;       // 128-row weight tile index
+  int tile;       // first 128-row weight tile (even)
+  int ntile;      // 1 or 2 tiles
 };
 
 MOE_DEVICE Seg load_seg(const Seg* p) {
@@ -74,30 +78,38 @@ MOE_DEVICE Seg load_seg(const Seg* p) {
   return Seg{lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 }
 
+// A unit is one segment times a.pair (1 or 2) consecutive weight tiles (the last group of an
+// odd tile count has one).  groups(tiles): tile groups of one weight matrix.
+MOE_DEVICE int groups(int tiles, int pair) { return (tiles + pair - 1) / pair; }
+
 template <bool kL2 = false>
 MOE_DEVICE Unit decode_unit(int u, const TcArgs& a, int tiles_r, int tiles_s, int n_shared_units) {
   Unit un;
   if (u < n_shared_units) {
-    const int ss = u / tiles_s;
+    const int pairs_s = groups(tiles_s, a.pair);
+    const int ss = u / pairs_s;
     const int nss = a.n_shared_segs;
     const int q = a.T / nss, rem = a.T % nss;
     un.shared = 1;
     un.expert = -1;
-    un.tile = u % tiles_s;
+    un.tile = a.pair * (u % pairs_s);
+    un.ntile = min(a.pair, tiles_s - un.tile);
     un.row_start = ss * q + min(ss, rem);
     un.rows = q + (ss < rem ? 1 : 0);
   } else {
-    // The parts [first, first + nparts) of one expert own units [first, first + nparts) * tiles;
-    // inside that range the tile index is the slow one and the part the fast one.
+    // The parts [first, first + nparts) of one expert own units [first, first + nparts) * pairs;
+    // inside that range the pair index is the slow one and the part the fast one.
     // kL2: read the segment records through L2 (the down kernel's producer reads them before
     // its grid-dependency wait, so nothing may come from a stale L1 line)
+    const int pairs_r = groups(tiles_r, a.pair);
     const int v = u - n_shared_units;
-    const Seg any = kL2 ? load_seg(a.segs + v / tiles_r) : a.segs[v / tiles_r];
-    const int o = v - any.first * tiles_r;
+    const Seg any = kL2 ? load_seg(a.segs + v / pairs_r) : a.segs[v / pairs_r];
+    const int o = v - any.first * pairs_r;
     const Seg s = kL2 ? load_seg(a.segs + any.first + o % any.nparts) : a.segs[any.first + o % any.nparts];
     un.shared = 0;
     un.expert = s.expert;
-    un.tile = o / any.nparts;
+    un.tile = a.pair * (o / any.nparts);
+    un.ntile = min(a.pair, tiles_r - un.tile);
     un.row_start = s.row_start;
     un.rows = s.rows;
   }
@@ -161,8 +173,8 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
 
   const int tiles_r = kGateUp ? a.f / 64 : a.d / BM;
   const int tiles_s = kGateUp ? (a.n_shared * a.f_s) / 64 : a.d / BM;
-  const int n_shared_units = a.n_shared ? a.n_shared_segs * tiles_s : 0;
-  const int n_routed_units = a.routed ? __ldcg(a.n_segs) * tiles_r : 0;
+  const int n_shared_units = a.n_shared ? a.n_shared_segs * groups(tiles_s, a.pair) : 0;
+  const int n_routed_units = a.routed ? __ldcg(a.n_segs) * groups(tiles_r, a.pair) : 0;
   const int total_units = n_shared_units + n_routed_units;
   const int nk_r = kGateUp ? a.d / BK : a.f / BK;
   const int nk_s = kGateUp ? a.d / BK : (a.n_shared * a.f_s) / BK;
@@ -180,8 +192,10 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
                                           : a.w_down + (static_cast<size_t>(un.expert) * tiles_r + un.tile) * nk * kTileElems;
         for (int kk = 0; kk < nk && pre < static_cast<uint32_t>(kStages); ++kk, ++pre) {
           if (elect_one()) {  // a fresh slot: no wait; the arrival comes with the h rows below
-            mbar_expect_tx(&full[pre], kABytes);
-            bulk_load(smem + pre * kStageBytes, wbase + static_cast<size_t>(kk) * kTileElems, kABytes, &full[pre], pol_w);
+            mbar_expect_tx(&full[pre], un.ntile * kABytes);
+            for (int t = 0; t < un.ntile; ++t)
+              bulk_load(smem + pre * kStageBytes + t * kABytes,
+                        wbase + (static_cast<size_t>(t) * nk + kk) * kTileElems, kABytes, &full[pre], pol_w);
           }
           __syncwarp();
         }
@@ -208,11 +222,15 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
         if (elect_one()) {
           uint8_t* sa = smem + slot * kStageBytes;
           const bool early = g < pre;  // weights already requested
-          mbar_arrive_expect_tx(&full[slot], (early ? 0 : kABytes) + nbox * 32 * BK * 2);
-          if (!early) bulk_load(sa, wbase + static_cast<size_t>(kk) * kTileElems, kABytes, &full[slot], pol_w);
+          mbar_arrive_expect_tx(&full[slot], (early ? 0 : un.ntile * kABytes) + nbox * 32 * BK * 2);
+          if (!early)
+            for (int t = 0; t < un.ntile; ++t)
+              bulk_load(sa + t * kABytes, wbase + (static_cast<size_t>(t) * nk + kk) * kTileElems, kABytes, &full[slot],
+                        pol_w);
           if (!kGateUp)
             for (int i = 0; i < nbox; ++i)
-              tma_load_2d(sa + kABytes + i * 32 * BK * 2, hm, &full[slot], kk * BK, un.row_start + 32 * i, pol_act);
+              tma_load_2d(sa + kPair * kABytes + i * 32 * BK * 2, hm, &full[slot], kk * BK, un.row_start + 32 * i,
+                          pol_act);
         }
         __syncwarp();
       }
@@ -228,7 +246,7 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
       const uint32_t buf = j & 1u, use_acc = j >> 1;
       if (!(ok = mbar_wait_warp(&acc_empty[buf], (use_acc & 1u) ^ 1u, abort_flag, a.err))) break;
       tc_fence_after();
-      const uint32_t d_tmem = tmem + buf * kAccCols;
+      const uint32_t d_tmem = tmem + buf * (kPair * kAccCols);  // tile t: + t * kAccCols
       // gate/up: bf16 weights x bf16 tokens; down: fp16 weights x fp16 hidden vectors
       const uint32_t idesc = kGateUp ? idesc_bf16_f32(BM, N) : idesc_f16_f32(BM, N);
       for (int kk = 0; kk < nk; ++kk, ++g) {
@@ -238,12 +256,16 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
         const bool next = mbar_test(&full[gn % kStages], (gn / kStages) & 1u);
         tc_fence_after();
         const uint32_t sa = smem_u32(smem + slot * kStageBytes);
-        const uint64_t adesc = smem_desc_sw128(sa);
-        const uint64_t bdesc = smem_desc_sw128(sa + kABytes);
+        const uint64_t adesc0 = smem_desc_sw128(sa);
+        const uint64_t adesc1 = smem_desc_sw128(sa + kABytes);
+        const uint64_t bdesc = smem_desc_sw128(sa + kPair * kABytes);
+        const bool two = un.ntile > 1;
         if (elect_one()) {
 #pragma unroll
-          for (int ks = 0; ks < BK / 16; ++ks)  // K = 16 per MMA: +32 bytes = +2 in the address field
-            mma_f16_ss(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc, (kk | ks) != 0);
+          for (int ks = 0; ks < BK / 16; ++ks) {  // K = 16 per MMA: +32 bytes = +2 in the address field
+            mma_f16_ss(d_tmem, adesc0 + 2 * ks, bdesc + 2 * ks, idesc, (kk | ks) != 0);
+            if (two) mma_f16_ss(d_tmem + kAccCols, adesc1 + 2 * ks, bdesc + 2 * ks, idesc, (kk | ks) != 0);
+          }
           mma_commit(&empty[slot]);
         }
         ready = __all_sync(0xffffffffu, next);
@@ -265,19 +287,21 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
       const uint32_t buf = j & 1u, use_acc = j >> 1;
       if (!mbar_wait(&acc_full[buf], use_acc & 1u, abort_flag, a.err)) break;
       tc_fence_after();
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * kAccCols;
       const int L = 32 * q + lane;  // accumulator row (= weight row of the tile)
       // Each 16-column chunk goes through a per-warp shared tile [column][row] so that the
       // global stores are 16-byte vectors of 8 consecutive features of one token.
       uint16_t* stg = epi_stage + (warp - 2) * (kEpiStageBytes / 2);
       bool sat = false;
+      for (int t = 0; t < un.ntile; ++t) {
+      const int tile = un.tile + t;
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + (buf * kPair + t) * kAccCols;
       if (kGateUp) {
         // lanes L and L ^ 8 hold the gate and up rows of one feature: each computes h for 8 of
         // the 16 columns (gate lane the even ones); the warp covers 16 consecutive features
         const int w16 = L & 15;
         const bool is_gate = w16 < 8;
         const int fl = 8 * ((L >> 4) & 1) + (w16 & 7);  // feature within the warp's 16
-        const int feat0 = un.tile * 64 + 16 * q;
+        const int feat0 = tile * 64 + 16 * q;
         uint16_t* hout;
         int ldh;
         if (un.shared) {
@@ -316,7 +340,7 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
           __syncwarp();
         }
       } else {
-        const int feat0 = un.tile * BM + 32 * q;
+        const int feat0 = tile * BM + 32 * q;
         uint16_t* yout = un.shared ? a.y_s : a.y;
         for (int c0 = 0; c0 < un.rows; c0 += 16) {
           uint32_t r[16];
@@ -344,6 +368,7 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
           __syncwarp();
         }
       }
+      }  // tiles of the unit
       if (__any_sync(0xffffffffu, sat) && lane == 0) set_error(a.err, MOE_DEVERR_RANGE);
       tc_fence_before();
       __syncwarp();
@@ -375,7 +400,7 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
           have_tok = true;
         }
         if (!(ok = mbar_wait_warp(&empty[s], ((g / kStages) & 1u) ^ 1u, abort_flag, a.err))) break;
-        const uint32_t sb = smem_u32(smem + s * kStageBytes + kABytes);
+        const uint32_t sb = smem_u32(smem + s * kStageBytes + kPair * kABytes);
         const int k0 = kk * BK + ch * 8;
         for (int n = rs; n < un.rows; n += 8)
           cp_async_16_hint(sb + n * 128 + ((ch ^ (n & 7)) << 4), a.x + static_cast<size_t>(tok[n]) * a.d + k0, pol_x);

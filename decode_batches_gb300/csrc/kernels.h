@@ -136,6 +136,7 @@ struct TcArgs {
   uint32_t* err = nullptr;
   int T = 0, E = 0, k = 0, d = 0, f = 0, n_shared = 0, f_s = 0;
   int n_shared_segs = 0;   // ceil(T / kSegRowsMax) when n_shared > 0 (shared tokens split evenly)
+  int pair = 2;            // bf16 kernels: weight tiles per unit (2 shares each B stage; 1 for few units)
 };
 
 cudaError_t launch_tc_gateup(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st);

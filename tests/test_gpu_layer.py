@@ -157,6 +157,24 @@ def test_forward_ragged_sizes(T):
     compare_layer(out[rows], ref, w.spec.k, TOL_BF16)
 
 
+# odd tile counts everywhere (gate/up 3, down 3, shared gate/up 5): with T = 4000 the 16-bit
+# kernels run two tiles per unit, and the last unit of each matrix holds one
+ODD_TILES = synth.LayerSpec(E=8, k=2, d=384, f=192, n_shared=1, f_s=320, wdtype="bf16")
+
+
+@pytest.mark.parametrize("T", [3, 4000])
+def test_odd_tile_counts(T):
+    w = synth.custom(ODD_TILES, T, n_prefill=T, name=f"oddtiles{T}")
+    plan = make_plan(w)
+    plan.set_path("tc")
+    x = to_dev(w.x(), "bf16")
+    out = bf16_tensor_to_f64(plan.forward(x, n_prefill=w.n_prefill))
+    rows = sample_rows(w, 64)
+    ref = oracle_layer(w, rows)
+    compare_layer(out[rows], ref, w.spec.k, TOL_BF16)
+    assert plan.device_error() == 0
+
+
 def test_forward_edge_arguments_and_canaries():
     from decode_batches_gb300 import MoeError
     w = workload("tiny", 0)
