@@ -31,25 +31,34 @@ namespace fq {
 constexpr int BM = 128;
 constexpr int kSubK = 64;                        // one 128-byte-swizzled K slice / one 4-bit block
 constexpr int kSubs = 2;                         // K slices per pipeline stage (K = 128)
-constexpr int kStages = 4;                       // A (TMEM) + B (shared memory) stages, one ring
 constexpr int kStagesRaw = 8;                    // 4-bit stages in shared memory (~70 KB in flight)
 constexpr int kDqSets = 2;                       // dequant quartets; quartet s takes stages g % 2 == s
-constexpr int kSubBytes = kSegRowsMax * kSubK * 2;         // 16 KB: one K slice of up to 128 rows
-constexpr int kBBytes = kSubs * kSubBytes;                 // 32 KB per stage
 constexpr int kRawBytes = kSubs * kFp4BlockBytes;          // 8704 B per stage
-constexpr int kAccCols = kSegRowsMax;            // 128 fp32 columns per accumulator
 constexpr int kACols = kSubs * kSubK / 2;        // 64 columns (fp16 pairs) per A stage
-constexpr int kAStart = 2 * kAccCols;            // A stages after the two accumulators
-constexpr int kTmemCols = 512;                   // 256 accumulator + 256 A columns
-constexpr int kGatherPerSlot = 2;                // gate/up B producers per ring slot
-constexpr int kGatherWarps = kGatherPerSlot * kStages;
-constexpr int kTokBytes = kGatherWarps * kSegRowsMax * 4;  // per gather warp: token of each row
+constexpr int kTmemCols = 512;                   // accumulators + A stages
 constexpr int kEpiStageBytes = 16 * 32 * 2;     // per epilogue warp: 16 columns x 32 fp16 rows
-constexpr int kSmemBytes = kStages * kBBytes + kStagesRaw * kRawBytes + 1024 + 1024 + kTokBytes + 4 * kEpiStageBytes;
 
-static_assert(kStagesRaw % kDqSets == 0 && kStages % kDqSets == 0, "stage rings must split evenly between quartets");
-static_assert(kAStart + kStages * kACols <= kTmemCols, "TMEM columns");
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+// Geometry for segments of at most kN rows (128, or 64 for steps of at most 64 tokens): the two
+// accumulators take 2 kN TMEM columns and the rest of the 512 hold A stages, so small segments
+// get a deeper ring (6 stages instead of 4) with smaller activation stages.
+template <int kN>
+struct Geo {
+  static constexpr int kStages = (kTmemCols - 2 * kN) / kACols;  // A (TMEM) + B (smem) stages, one ring
+  static constexpr int kSubBytes = kN * kSubK * 2;                // one K slice of up to kN rows
+  static constexpr int kBBytes = kSubs * kSubBytes;
+  static constexpr int kAccCols = kN;
+  static constexpr int kAStart = 2 * kAccCols;                   // A stages after the accumulators
+  static constexpr int kGatherPerSlot = kN > 64 ? 2 : 1;         // gate/up B producers per slot
+  static constexpr int kGatherWarps = kGatherPerSlot * kStages;
+  static constexpr int kTokBytes = kGatherWarps * kN * 4;         // per gather warp: token per row
+  static constexpr int kSmemBytes =
+      kStages * kBBytes + kStagesRaw * kRawBytes + 1024 + 1024 + kTokBytes + 4 * kEpiStageBytes;
+  static constexpr int threads(bool gate_up) { return 32 * (gate_up ? 6 + kGatherWarps + 8 : 7 + 8); }
+  static_assert(kStagesRaw % kDqSets == 0 && kStages % kDqSets == 0, "rings must split evenly between quartets");
+  static_assert(kAStart + kStages * kACols <= kTmemCols, "TMEM columns");
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+  static_assert(kN <= kSegRowsMax && kN % 32 == 0, "segment rows");
+};
 
 MOE_DEVICE int pad16(int rows) { return rows <= 16 ? 16 : ((rows + 15) & ~15); }
 
@@ -127,9 +136,17 @@ MOE_DEVICE void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uin
 //                        the quartet (4 arrivals) and the B producer (the slot's gather warp, or
 //                        one arrive.expect_tx for TMA) are done, empty when the MMAs reading it finish.
 // The MMA warp thus waits on one barrier and commits once per 128 K.
-template <bool kGateUp>
-__global__ void __launch_bounds__(kGateUp ? 704 : 480, 1)
+template <bool kGateUp, int kN>
+__global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
     fp4_ffn_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
+  constexpr int kStages = Geo<kN>::kStages;
+  constexpr int kSubBytes = Geo<kN>::kSubBytes;
+  constexpr int kBBytes = Geo<kN>::kBBytes;
+  constexpr int kAccCols = Geo<kN>::kAccCols;
+  constexpr int kAStart = Geo<kN>::kAStart;
+  constexpr int kGatherPerSlot = Geo<kN>::kGatherPerSlot;
+  constexpr int kGatherWarps = Geo<kN>::kGatherWarps;
+  constexpr int kTokBytes = Geo<kN>::kTokBytes;
   constexpr int kDqWarp = kGateUp ? 6 + kGatherWarps : 7;  // first dequant warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -399,9 +416,9 @@ __global__ void __launch_bounds__(kGateUp ? 704 : 480, 1)
     // behind the issue of a later stage.
     const int gw = warp - 6;
     const int slot = gw % kStages, half = gw / kStages;
-    int32_t* tok = tok_tab + kSegRowsMax * gw;  // token row of each row of this warp's unit
+    int32_t* tok = tok_tab + kN * gw;           // token row of each row of this warp's unit
     const int ch = lane & 7;                    // 16-byte chunk
-    const int rs = (lane >> 3) + 4 * half;      // first row; rows rs + 8 i
+    const int rs = (lane >> 3) + 4 * half;      // first row; rows rs + 4 kGatherPerSlot i
     const uint64_t pol_x = l2_policy_evict_last();
     uint32_t g = 0;
     bool ok = true;
@@ -420,7 +437,7 @@ __global__ void __launch_bounds__(kGateUp ? 704 : 480, 1)
         if (!(ok = mbar_wait_warp(&empty[s], ((g / kStages) & 1u) ^ 1u, abort_flag, a.err))) break;
         const uint32_t sb = smem_u32(ring_b + s * kBBytes);
         const int k0 = kSubs * kk * kSubK + ch * 8;
-        for (int n = rs; n < un.rows; n += 8) {
+        for (int n = rs; n < un.rows; n += 4 * kGatherPerSlot) {
           const uint16_t* src = a.x16 + static_cast<size_t>(tok[n]) * a.d + k0;
           const uint32_t dst = sb + n * 128 + ((ch ^ (n & 7)) << 4);
           cp_async_16_hint(dst, src, pol_x);
@@ -446,17 +463,23 @@ __global__ void __launch_bounds__(kGateUp ? 704 : 480, 1)
 
 }  // namespace fq
 
-static bool g_fq_attr[2] = {false, false};
+template <bool kGateUp, int kN>
+static cudaError_t launch_fq_n(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st) {
+  auto kern = fq::fp4_ffn_kernel<kGateUp, kN>;
+  static bool attr = false;  // one per instantiation
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, fq::Geo<kN>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  return launch_pdl(kern, dim3(num_sms), dim3(fq::Geo<kN>::threads(kGateUp)), fq::Geo<kN>::kSmemBytes, st, *maps, a);
+}
 
+// Steps of at most 64 tokens have segments of at most 64 rows: the deeper-ring geometry.
 template <bool kGateUp>
 static cudaError_t launch_fq(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st) {
-  auto kern = fq::fp4_ffn_kernel<kGateUp>;
-  if (!g_fq_attr[kGateUp]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, fq::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    g_fq_attr[kGateUp] = true;
-  }
-  return launch_pdl(kern, dim3(num_sms), dim3(kGateUp ? 704 : 480), fq::kSmemBytes, st, *maps, a);
+  if (a.T <= 64) return launch_fq_n<kGateUp, 64>(maps, a, num_sms, st);
+  return launch_fq_n<kGateUp, 128>(maps, a, num_sms, st);
 }
 
 cudaError_t launch_fp4_gateup(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st) {
