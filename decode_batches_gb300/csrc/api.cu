@@ -433,7 +433,7 @@ extern "C" moe_status moe_plan_set_weights(moe_plan* p, const float* w_router, c
   MOE_CUDA_TRY(cudaMalloc(&p->w_down, E * d * dn_row));
   if (p->tiled) {
     MOE_CUDA_TRY(launch_tile_gate_up(static_cast<const uint16_t*>(w_gate), static_cast<const uint16_t*>(w_up),
-                                     reinterpret_cast<uint16_t*>(p->w_gu), p->E, p->f, p->d, 0));
+                                     reinterpret_cast<uint16_t*>(p->w_gu), p->E, p->f, p->d, 0, 0));
     s = tile_down_f16(reinterpret_cast<uint16_t*>(p->w_down), w_down, p->E, p->d, p->f, 1);
     if (s != MOE_OK) {
       free_weights(p);
@@ -484,7 +484,7 @@ extern "C" moe_status moe_plan_set_shared(moe_plan* p, int d_ff_shared, const vo
   p->tiled_s = d % 128 == 0 && fs % 64 == 0;
   if (p->tiled_s) {
     MOE_CUDA_TRY(launch_tile_gate_up(static_cast<const uint16_t*>(w_gate), static_cast<const uint16_t*>(w_up), p->w_gu_s,
-                                     p->n_shared, p->f_s, p->d, 0));
+                                     p->n_shared, p->f_s, p->d, 1, 0));
     s = tile_down_f16(p->w_down_s, w_down, p->n_shared, p->d, p->f_s, 0);
   } else {
     MOE_CUDA_TRY(launch_interleave_gate_up(static_cast<const uint8_t*>(w_gate), static_cast<const uint8_t*>(w_up),

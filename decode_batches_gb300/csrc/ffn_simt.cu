@@ -48,12 +48,13 @@ MOE_DEVICE float warp_dot_f16(const float* act, const uint16_t* wrow, int K, int
 }
 
 // Dot product with one row of a tile-contiguous matrix: `blocks` points at the row's first
-// 128 x 64 block, consecutive K chunks are consecutive blocks, r is the row inside the block.
+// 128 x 64 block, consecutive K chunks are `stride` elements apart (tile_chunk_stride), r is the
+// row inside the block.
 template <bool kF16>
-MOE_DEVICE float warp_dot_tiled(const float* act, const uint16_t* blocks, int r, int K, int lane) {
+MOE_DEVICE float warp_dot_tiled(const float* act, const uint16_t* blocks, size_t stride, int r, int K, int lane) {
   float acc = 0.f;
   for (int k = lane * 8; k < K; k += 256) {
-    const uint4 wv = *reinterpret_cast<const uint4*>(blocks + static_cast<size_t>(k >> 6) * kTileElems +
+    const uint4 wv = *reinterpret_cast<const uint4*>(blocks + static_cast<size_t>(k >> 6) * stride +
                                                      tile_elem_offset(r, k & 63));
     float wf[8];
     if (kF16)
@@ -170,10 +171,12 @@ __global__ void __launch_bounds__(256) simt_gateup_kernel(FfnWeights w, const ui
         g = warp_dot_fp4(act, c + static_cast<size_t>(gu_row(F, 0)) * (w.d / 2), s + static_cast<size_t>(gu_row(F, 0)) * (w.d / 32), w.d, lane);
         u = warp_dot_fp4(act, c + static_cast<size_t>(gu_row(F, 1)) * (w.d / 2), s + static_cast<size_t>(gu_row(F, 1)) * (w.d / 32), w.d, lane);
       } else if (w.tiled) {
-        const uint16_t* blocks = static_cast<const uint16_t*>(w.w_gu) +
-                                 (static_cast<size_t>(e) * (w.f / 64) + F / 64) * (w.d / 64) * kTileElems;
-        g = warp_dot_tiled<false>(act, blocks, gu_tile_row(F, 0), w.d, lane);
-        u = warp_dot_tiled<false>(act, blocks, gu_tile_row(F, 1), w.d, lane);
+        const int tiles = w.f / 64, t = F / 64;
+        const uint16_t* blocks = static_cast<const uint16_t*>(w.w_gu) + static_cast<size_t>(e) * tiles * (w.d / 64) * kTileElems +
+                                 tile_chunk_offset(t, 0, tiles, w.d / 64);
+        const size_t stride = tile_chunk_stride(t, tiles);
+        g = warp_dot_tiled<false>(act, blocks, stride, gu_tile_row(F, 0), w.d, lane);
+        u = warp_dot_tiled<false>(act, blocks, stride, gu_tile_row(F, 1), w.d, lane);
       } else {
         const uint16_t* base = static_cast<const uint16_t*>(w.w_gu) + static_cast<size_t>(e) * 2 * w.f * w.d;
         g = warp_dot_bf16(act, base + static_cast<size_t>(gu_row(F, 0)) * w.d, w.d, lane);
@@ -192,10 +195,11 @@ __global__ void __launch_bounds__(256) simt_gateup_kernel(FfnWeights w, const ui
       const int s = F / w.f_s, Fl = F % w.f_s;
       float g, u;
       if (w.tiled_s) {
-        const uint16_t* blocks =
-            w.w_gu_s + (static_cast<size_t>(s) * (w.f_s / 64) + Fl / 64) * (w.d / 64) * kTileElems;
-        g = warp_dot_tiled<false>(act, blocks, gu_tile_row(Fl, 0), w.d, lane);
-        u = warp_dot_tiled<false>(act, blocks, gu_tile_row(Fl, 1), w.d, lane);
+        const int tiles = w.n_shared * (w.f_s / 64), t = s * (w.f_s / 64) + Fl / 64;  // one matrix
+        const uint16_t* blocks = w.w_gu_s + tile_chunk_offset(t, 0, tiles, w.d / 64);
+        const size_t stride = tile_chunk_stride(t, tiles);
+        g = warp_dot_tiled<false>(act, blocks, stride, gu_tile_row(Fl, 0), w.d, lane);
+        u = warp_dot_tiled<false>(act, blocks, stride, gu_tile_row(Fl, 1), w.d, lane);
       } else {
         const uint16_t* base = w.w_gu_s + static_cast<size_t>(s) * 2 * w.f_s * w.d;
         g = warp_dot_bf16(act, base + static_cast<size_t>(gu_row(Fl, 0)) * w.d, w.d, lane);
@@ -237,9 +241,10 @@ __global__ void __launch_bounds__(256) simt_down_kernel(FfnWeights w, int T, con
         const uint8_t* s = w.s_down + (static_cast<size_t>(e) * w.d + n) * (w.f / 32);
         v = warp_dot_fp4(act, c, s, w.f, lane);
       } else if (w.tiled) {
-        const uint16_t* blocks = static_cast<const uint16_t*>(w.w_down) +
-                                 (static_cast<size_t>(e) * (w.d / 128) + n / 128) * (w.f / 64) * kTileElems;
-        v = warp_dot_tiled<true>(act, blocks, n & 127, w.f, lane);
+        const int tiles = w.d / 128, t = n / 128;
+        const uint16_t* blocks = static_cast<const uint16_t*>(w.w_down) + static_cast<size_t>(e) * tiles * (w.f / 64) * kTileElems +
+                                 tile_chunk_offset(t, 0, tiles, w.f / 64);
+        v = warp_dot_tiled<true>(act, blocks, tile_chunk_stride(t, tiles), n & 127, w.f, lane);
       } else {
         v = warp_dot_f16(act, static_cast<const uint16_t*>(w.w_down) + (static_cast<size_t>(e) * w.d + n) * w.f, w.f, lane);
       }
@@ -259,9 +264,9 @@ __global__ void __launch_bounds__(256) simt_down_kernel(FfnWeights w, int T, con
       float v = 0.f;
       for (int s = 0; s < w.n_shared; ++s)
         v += w.tiled_s ? warp_dot_tiled<true>(act + s * w.f_s,
-                                              w.w_down_s + (static_cast<size_t>(n / 128) * w.n_shared + s) *
-                                                               (w.f_s / 64) * kTileElems,
-                                              n & 127, w.f_s, lane)
+                                              w.w_down_s + tile_chunk_offset(n / 128, s * (w.f_s / 64), w.d / 128,
+                                                                             w.n_shared * (w.f_s / 64)),
+                                              tile_chunk_stride(n / 128, w.d / 128), n & 127, w.f_s, lane)
                        : warp_dot_f16(act + s * w.f_s, w.w_down_s + (static_cast<size_t>(s) * w.d + n) * w.f_s, w.f_s, lane);
       bool sat = false;
       const uint16_t yv = to_f16_sat(v, sat);

@@ -188,14 +188,13 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
       for (int u = blockIdx.x; u < total_units && pre < static_cast<uint32_t>(kStages); u += gridDim.x) {
         const Unit un = decode_unit<true>(u, a, tiles_r, tiles_s, n_shared_units);
         const int nk = un.shared ? nk_s : nk_r;
-        const uint16_t* wbase = un.shared ? a.w_down_s + static_cast<size_t>(un.tile) * nk * kTileElems
-                                          : a.w_down + (static_cast<size_t>(un.expert) * tiles_r + un.tile) * nk * kTileElems;
+        const int tiles_m = un.shared ? tiles_s : tiles_r;
+        const uint16_t* mbase = un.shared ? a.w_down_s : a.w_down + static_cast<size_t>(un.expert) * tiles_r * nk * kTileElems;
         for (int kk = 0; kk < nk && pre < static_cast<uint32_t>(kStages); ++kk, ++pre) {
           if (elect_one()) {  // a fresh slot: no wait; the arrival comes with the h rows below
             mbar_expect_tx(&full[pre], un.ntile * kABytes);
-            for (int t = 0; t < un.ntile; ++t)
-              bulk_load(smem + pre * kStageBytes + t * kABytes,
-                        wbase + (static_cast<size_t>(t) * nk + kk) * kTileElems, kABytes, &full[pre], pol_w);
+            bulk_load(smem + pre * kStageBytes, mbase + tile_chunk_offset(un.tile, kk, tiles_m, nk), un.ntile * kABytes,
+                      &full[pre], pol_w);
           }
           __syncwarp();
         }
@@ -208,13 +207,12 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
       const Unit un = decode_unit(u, a, tiles_r, tiles_s, n_shared_units);
       const int nk = un.shared ? nk_s : nk_r;
       const int nbox = kGateUp ? 0 : (pad16(un.rows) + 31) / 32;
-      const uint16_t* wbase;
-      if (kGateUp)
-        wbase = un.shared ? a.w_gu_s + static_cast<size_t>(un.tile) * nk * kTileElems
-                          : a.w_gu + (static_cast<size_t>(un.expert) * tiles_r + un.tile) * nk * kTileElems;
-      else
-        wbase = un.shared ? a.w_down_s + static_cast<size_t>(un.tile) * nk * kTileElems
-                          : a.w_down + (static_cast<size_t>(un.expert) * tiles_r + un.tile) * nk * kTileElems;
+      // the unit's weight matrix (an expert, or all shared experts); with the paired tile layout
+      // both tiles of a pair unit at one K chunk are one contiguous 32 KB run
+      const int tiles_m = un.shared ? tiles_s : tiles_r;
+      const uint16_t* mbase =
+          kGateUp ? (un.shared ? a.w_gu_s : a.w_gu + static_cast<size_t>(un.expert) * tiles_r * nk * kTileElems)
+                  : (un.shared ? a.w_down_s : a.w_down + static_cast<size_t>(un.expert) * tiles_r * nk * kTileElems);
       const CUtensorMap* hm = un.shared ? &maps.h_s : &maps.h;
       for (int kk = 0; kk < nk; ++kk, ++g) {
         const int slot = g % kStages;
@@ -224,9 +222,7 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
           const bool early = g < pre;  // weights already requested
           mbar_arrive_expect_tx(&full[slot], (early ? 0 : un.ntile * kABytes) + nbox * 32 * BK * 2);
           if (!early)
-            for (int t = 0; t < un.ntile; ++t)
-              bulk_load(sa + t * kABytes, wbase + (static_cast<size_t>(t) * nk + kk) * kTileElems, kABytes, &full[slot],
-                        pol_w);
+            bulk_load(sa, mbase + tile_chunk_offset(un.tile, kk, tiles_m, nk), un.ntile * kABytes, &full[slot], pol_w);
           if (!kGateUp)
             for (int i = 0; i < nbox; ++i)
               tma_load_2d(sa + kPair * kABytes + i * 32 * BK * 2, hm, &full[slot], kk * BK, un.row_start + 32 * i,

@@ -161,10 +161,15 @@ cudaError_t launch_interleave_gate_up(const uint8_t* gate, const uint8_t* up, ui
 // dst fp16 <- src bf16 (round to nearest even); *bad |= 1 if a value is outside the fp16 range.
 cudaError_t launch_bf16_to_f16(const uint16_t* src, uint16_t* dst, size_t n, uint32_t* bad, cudaStream_t st);
 // Tile-contiguous, pre-swizzled layouts of the tensor-core path (16 KB blocks of 128 rows x 64
-// K elements).  Gate/up of n experts -> [n][f/64][d/64] blocks (rows interleaved by 8).  Down
-// (bf16 -> fp16) of n matrices [rows][K] -> by_matrix ? [n][rows/128][K/64] : [rows/128][n][K/64].
+// K elements).  A weight matrix of `tiles` 128-row tiles and nk K chunks stores its blocks at
+// tile_chunk_offset: tiles are paired and the two tiles of a pair alternate along K, so both
+// blocks of one K chunk are adjacent (one 32 KB copy); an odd last tile stands alone.
+//   gate/up of n experts (rows interleaved by 8): one matrix per expert (f/64 tiles, d/64 chunks),
+//     or with one_matrix the n experts as one matrix of n f/64 tiles (the shared experts);
+//   down (bf16 -> fp16) of n matrices [rows][K]: by_matrix ? one matrix per expert (rows/128
+//     tiles, K/64 chunks) : one matrix of rows/128 tiles whose K runs over all n (n K/64 chunks).
 cudaError_t launch_tile_gate_up(const uint16_t* gate, const uint16_t* up, uint16_t* dst, int n, int f, int d,
-                                cudaStream_t st);
+                                int one_matrix, cudaStream_t st);
 cudaError_t launch_tile_down(const uint16_t* src, uint16_t* dst, int n, int rows, int K, int by_matrix, uint32_t* bad,
                              cudaStream_t st);
 constexpr int kTileElems = 128 * 64;
@@ -177,6 +182,16 @@ constexpr int kFp4ScaleMax = 140;
 cudaError_t launch_tile_fp4(const uint8_t* codes_a, const uint8_t* scales_a, const uint8_t* codes_b,
                             const uint8_t* scales_b, uint8_t* dst, int n, int rows, int K, int gate_up,
                             uint32_t* scale_oor, cudaStream_t st);
+// Element offset of block (tile t, K chunk kc) inside one tile-contiguous weight matrix.
+__host__ __device__ inline size_t tile_chunk_offset(int t, int kc, int tiles, int nk) {
+  const int pr = t >> 1, w = t & 1;
+  const int np = tiles - 2 * pr < 2 ? tiles - 2 * pr : 2;
+  return (static_cast<size_t>(pr) * 2 * nk + static_cast<size_t>(kc) * np + w) * kTileElems;
+}
+// Elements between consecutive K chunks of tile t (2 blocks inside a pair, 1 for a lone tile).
+__host__ __device__ inline size_t tile_chunk_stride(int t, int tiles) {
+  return static_cast<size_t>(tiles - 2 * (t >> 1) < 2 ? 1 : 2) * kTileElems;
+}
 // Element offset of (row r, K element kk) inside one 128 x 64 block (128-byte swizzle).
 __host__ __device__ inline size_t tile_elem_offset(int r, int kk) {
   return static_cast<size_t>(r) * 64 + ((((kk >> 3) ^ (r & 7)) << 3) | (kk & 7));

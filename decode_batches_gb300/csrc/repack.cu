@@ -64,11 +64,12 @@ cudaError_t launch_bf16_to_f16(const uint16_t* src, uint16_t* dst, size_t n, uin
 // Gate/up of n experts ([n][f][d] each) -> blocks [n][f/64][d/64]; block row r of feature tile t
 // is gate row 64t + 8(r/16) + r%8 when r%16 < 8, else the up row of that feature.
 __global__ void tile_gate_up_kernel(const uint16_t* __restrict__ gate, const uint16_t* __restrict__ up,
-                                    uint16_t* __restrict__ dst, int f, int d, size_t n_chunks16) {
+                                    uint16_t* __restrict__ dst, int n, int f, int d, int one_matrix,
+                                    size_t n_chunks16) {
   const int nk = d / 64, tiles = f / 64;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n_chunks16;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    // destination chunk i: block b = i / 1024, row r = (i % 1024) / 8, physical chunk pc = i % 8
+    // logical 16-byte chunk i: block b = i / 1024 = (e * tiles + t) * nk + kc, row r, physical chunk pc
     const size_t b = i >> 10;
     const int r = static_cast<int>((i >> 3) & 127), pc = static_cast<int>(i & 7);
     const int kc = static_cast<int>(b % nk);
@@ -77,21 +78,24 @@ __global__ void tile_gate_up_kernel(const uint16_t* __restrict__ gate, const uin
     const size_t e = et / tiles;
     const int F = 64 * t + 8 * (r >> 4) + (r & 7);
     const uint16_t* src = ((r & 15) < 8 ? gate : up) + (e * f + F) * static_cast<size_t>(d) + kc * 64 + 8 * (pc ^ (r & 7));
-    reinterpret_cast<uint4*>(dst)[i] = *reinterpret_cast<const uint4*>(src);
+    const size_t blk = one_matrix ? tile_chunk_offset(static_cast<int>(e) * tiles + t, kc, n * tiles, nk)
+                                  : e * tiles * nk * kTileElems + tile_chunk_offset(t, kc, tiles, nk);
+    reinterpret_cast<uint4*>(dst + blk + r * 64)[pc] = *reinterpret_cast<const uint4*>(src);
   }
 }
 
 cudaError_t launch_tile_gate_up(const uint16_t* gate, const uint16_t* up, uint16_t* dst, int n, int f, int d,
-                                cudaStream_t st) {
+                                int one_matrix, cudaStream_t st) {
   const size_t chunks = static_cast<size_t>(n) * 2 * f * d / 8;
   if (chunks == 0) return cudaSuccess;
-  tile_gate_up_kernel<<<2048, 256, 0, st>>>(gate, up, dst, f, d, chunks);
+  tile_gate_up_kernel<<<2048, 256, 0, st>>>(gate, up, dst, n, f, d, one_matrix, chunks);
   return cudaGetLastError();
 }
 
-// Down projections of n matrices ([n][rows][K] bf16) -> fp16 blocks.  Routed order (by_matrix):
-// block (m, rows/128 tile dt, K chunk kc) at (m * (rows/128) + dt) * (K/64) + kc.  Shared order:
-// at (dt * n + m) * (K/64) + kc, so one output tile's K loop runs over all n matrices.
+// Down projections of n matrices ([n][rows][K] bf16) -> fp16 blocks.  Routed (by_matrix): one
+// tile-contiguous matrix per m (rows/128 tiles, K/64 chunks).  Shared: one matrix of rows/128
+// tiles whose K chunks run over all n matrices (chunk m * K/64 + kc), so one output tile's K loop
+// covers every shared expert.
 __global__ void tile_down_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst, int n, int rows, int K,
                                  int by_matrix, size_t n_chunks16, uint32_t* bad) {
   const int nk = K / 64, dts = rows / 128;
@@ -112,6 +116,8 @@ __global__ void tile_down_kernel(const uint16_t* __restrict__ src, uint16_t* __r
     }
     const uint16_t* s = src + (static_cast<size_t>(m) * rows + dt * 128 + r) * K + kc * 64 + 8 * (pc ^ (r & 7));
     const uint4 v = *reinterpret_cast<const uint4*>(s);
+    const size_t blk = by_matrix ? static_cast<size_t>(m) * dts * nk * kTileElems + tile_chunk_offset(dt, kc, dts, nk)
+                                 : tile_chunk_offset(dt, m * nk + kc, dts, n * nk);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t o[4];
 #pragma unroll
@@ -121,7 +127,7 @@ __global__ void tile_down_kernel(const uint16_t* __restrict__ src, uint16_t* __r
       if (!(fabsf(lo) <= kF16Max) || !(fabsf(hi) <= kF16Max)) oor = true;
       o[q] = static_cast<uint32_t>(f32_to_f16_bits_rn(lo)) | (static_cast<uint32_t>(f32_to_f16_bits_rn(hi)) << 16);
     }
-    reinterpret_cast<uint4*>(dst)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    reinterpret_cast<uint4*>(dst + blk + r * 64)[pc] = make_uint4(o[0], o[1], o[2], o[3]);
   }
   if (oor) atomicOr(bad, 1u);
 }
