@@ -289,81 +289,81 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
       uint16_t* stg = epi_stage + (warp - 2) * (kEpiStageBytes / 2);
       bool sat = false;
       for (int t = 0; t < un.ntile; ++t) {
-      const int tile = un.tile + t;
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + (buf * kPair + t) * kAccCols;
-      if (kGateUp) {
-        // lanes L and L ^ 8 hold the gate and up rows of one feature: each computes h for 8 of
-        // the 16 columns (gate lane the even ones); the warp covers 16 consecutive features
-        const int w16 = L & 15;
-        const bool is_gate = w16 < 8;
-        const int fl = 8 * ((L >> 4) & 1) + (w16 & 7);  // feature within the warp's 16
-        const int feat0 = tile * 64 + 16 * q;
-        uint16_t* hout;
-        int ldh;
-        if (un.shared) {
-          hout = a.h_s;
-          ldh = a.n_shared * a.f_s;
+        const int tile = un.tile + t;
+        const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + (buf * kPair + t) * kAccCols;
+        if (kGateUp) {
+          // lanes L and L ^ 8 hold the gate and up rows of one feature: each computes h for 8 of
+          // the 16 columns (gate lane the even ones); the warp covers 16 consecutive features
+          const int w16 = L & 15;
+          const bool is_gate = w16 < 8;
+          const int fl = 8 * ((L >> 4) & 1) + (w16 & 7);  // feature within the warp's 16
+          const int feat0 = tile * 64 + 16 * q;
+          uint16_t* hout;
+          int ldh;
+          if (un.shared) {
+            hout = a.h_s;
+            ldh = a.n_shared * a.f_s;
+          } else {
+            hout = a.h;
+            ldh = a.f;
+          }
+          for (int c0 = 0; c0 < un.rows; c0 += 16) {
+            uint32_t r[16];
+            tmem_ld_32x32b_x16(tbase + c0, r);
+            tmem_wait_ld();
+  #pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+              const uint32_t send = is_gate ? r[2 * jj + 1] : r[2 * jj];
+              const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 8);
+              const int cl = 2 * jj + (is_gate ? 0 : 1);
+              const float gv = __uint_as_float(is_gate ? r[2 * jj] : recv);
+              const float uv = __uint_as_float(is_gate ? recv : r[2 * jj + 1]);
+              float hv = swiglu(gv, uv);
+              if (c0 + cl < un.rows && !(fabsf(hv) <= kF16Max)) {  // padding columns never count
+                sat = true;
+                hv = fminf(fmaxf(hv, -kF16Max), kF16Max);
+              }
+              stg[cl * 16 + fl] = f32_to_f16_bits_rn(hv);
+            }
+            __syncwarp();
+            {  // lane i: column i / 2, features 8 (i % 2) .. + 7
+              const int cl = lane >> 1, half = lane & 1;
+              if (c0 + cl < un.rows) {
+                const uint4 v = *reinterpret_cast<const uint4*>(stg + cl * 16 + 8 * half);
+                *reinterpret_cast<uint4*>(hout + static_cast<size_t>(un.row_start + c0 + cl) * ldh + feat0 + 8 * half) = v;
+              }
+            }
+            __syncwarp();
+          }
         } else {
-          hout = a.h;
-          ldh = a.f;
+          const int feat0 = tile * BM + 32 * q;
+          uint16_t* yout = un.shared ? a.y_s : a.y;
+          for (int c0 = 0; c0 < un.rows; c0 += 16) {
+            uint32_t r[16];
+            tmem_ld_32x32b_x16(tbase + c0, r);
+            tmem_wait_ld();
+  #pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              float v = __uint_as_float(r[c]);
+              if (c0 + c < un.rows && !(fabsf(v) <= kF16Max)) {
+                sat = true;
+                v = fminf(fmaxf(v, -kF16Max), kF16Max);
+              }
+              stg[c * 32 + lane] = f32_to_f16_bits_rn(v);
+            }
+            __syncwarp();
+  #pragma unroll
+            for (int pass = 0; pass < 2; ++pass) {  // column (16 pass + lane) / 4, features 8 (lane % 4) .. + 7
+              const int idx = 32 * pass + lane;
+              const int cl = idx >> 2, g = idx & 3;
+              if (c0 + cl < un.rows) {
+                const uint4 v = *reinterpret_cast<const uint4*>(stg + cl * 32 + 8 * g);
+                *reinterpret_cast<uint4*>(yout + static_cast<size_t>(un.row_start + c0 + cl) * a.d + feat0 + 8 * g) = v;
+              }
+            }
+            __syncwarp();
+          }
         }
-        for (int c0 = 0; c0 < un.rows; c0 += 16) {
-          uint32_t r[16];
-          tmem_ld_32x32b_x16(tbase + c0, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const uint32_t send = is_gate ? r[2 * jj + 1] : r[2 * jj];
-            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 8);
-            const int cl = 2 * jj + (is_gate ? 0 : 1);
-            const float gv = __uint_as_float(is_gate ? r[2 * jj] : recv);
-            const float uv = __uint_as_float(is_gate ? recv : r[2 * jj + 1]);
-            float hv = swiglu(gv, uv);
-            if (c0 + cl < un.rows && !(fabsf(hv) <= kF16Max)) {  // padding columns never count
-              sat = true;
-              hv = fminf(fmaxf(hv, -kF16Max), kF16Max);
-            }
-            stg[cl * 16 + fl] = f32_to_f16_bits_rn(hv);
-          }
-          __syncwarp();
-          {  // lane i: column i / 2, features 8 (i % 2) .. + 7
-            const int cl = lane >> 1, half = lane & 1;
-            if (c0 + cl < un.rows) {
-              const uint4 v = *reinterpret_cast<const uint4*>(stg + cl * 16 + 8 * half);
-              *reinterpret_cast<uint4*>(hout + static_cast<size_t>(un.row_start + c0 + cl) * ldh + feat0 + 8 * half) = v;
-            }
-          }
-          __syncwarp();
-        }
-      } else {
-        const int feat0 = tile * BM + 32 * q;
-        uint16_t* yout = un.shared ? a.y_s : a.y;
-        for (int c0 = 0; c0 < un.rows; c0 += 16) {
-          uint32_t r[16];
-          tmem_ld_32x32b_x16(tbase + c0, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            float v = __uint_as_float(r[c]);
-            if (c0 + c < un.rows && !(fabsf(v) <= kF16Max)) {
-              sat = true;
-              v = fminf(fmaxf(v, -kF16Max), kF16Max);
-            }
-            stg[c * 32 + lane] = f32_to_f16_bits_rn(v);
-          }
-          __syncwarp();
-#pragma unroll
-          for (int pass = 0; pass < 2; ++pass) {  // column (16 pass + lane) / 4, features 8 (lane % 4) .. + 7
-            const int idx = 32 * pass + lane;
-            const int cl = idx >> 2, g = idx & 3;
-            if (c0 + cl < un.rows) {
-              const uint4 v = *reinterpret_cast<const uint4*>(stg + cl * 32 + 8 * g);
-              *reinterpret_cast<uint4*>(yout + static_cast<size_t>(un.row_start + c0 + cl) * a.d + feat0 + 8 * g) = v;
-            }
-          }
-          __syncwarp();
-        }
-      }
       }  // tiles of the unit
       if (__any_sync(0xffffffffu, sat) && lane == 0) set_error(a.err, MOE_DEVERR_RANGE);
       tc_fence_before();
