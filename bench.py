@@ -264,28 +264,52 @@ def time_forward(plan, x, n_prefill, steps, warmup, world, timing=False):
 
 
 def time_e2e(plan, x_host, n_prefill, steps, warmup, world):
-    """Same metric through host buffers: pinned x -> device, forward, out -> pinned host."""
+    """Same metric through host buffers: every step copies its input from pinned host memory to
+    the device, runs the layer and copies its output back to pinned host memory.  The two copies
+    run on their own streams with double-buffered device tensors, so step i+1's input copy and
+    step i-1's output copy overlap step i's layer, as a serving loop would; every copy of every
+    timed step is inside the timed region."""
     import torch
     st = torch.cuda.current_stream()
-    x_dev = torch.empty(x_host.shape, dtype=x_host.dtype, device="cuda")
-    out_dev = torch.empty_like(x_dev)
-    out_host = torch.empty(x_host.shape, dtype=x_host.dtype, pin_memory=True)
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    x_dev = [torch.empty(x_host.shape, dtype=x_host.dtype, device="cuda") for _ in range(2)]
+    out_dev = [torch.empty_like(x_dev[0]) for _ in range(2)]
+    out_host = [torch.empty(x_host.shape, dtype=x_host.dtype, pin_memory=True) for _ in range(2)]
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def step():
-        x_dev.copy_(x_host, non_blocking=True)
-        plan.forward(x_dev, n_prefill, out=out_dev)
-        out_host.copy_(out_dev, non_blocking=True)
+    def run(n, first):
+        for i in range(n):
+            b = i % 2
+            reuse = not (first and i < 2)
+            with torch.cuda.stream(h2d):
+                if reuse:
+                    h2d.wait_event(ev_done[b])     # step i-2's layer has read x_dev[b]
+                x_dev[b].copy_(x_host, non_blocking=True)
+                ev_in[b].record(h2d)
+            st.wait_event(ev_in[b])
+            if reuse:
+                st.wait_event(ev_out[b])           # step i-2's output has left out_dev[b]
+            plan.forward(x_dev[b], n_prefill, out=out_dev[b])
+            ev_done[b].record(st)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(ev_done[b])
+                out_host[b].copy_(out_dev[b], non_blocking=True)
+                ev_out[b].record(d2h)
 
-    for _ in range(warmup):
-        step()
+    run(warmup, True)
     torch.cuda.synchronize()
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(st)
-    for _ in range(steps):
-        step()
+    h2d.wait_event(e0)
+    d2h.wait_event(e0)
+    run(steps, True)
+    st.wait_stream(h2d)
+    st.wait_stream(d2h)  # the last output copy is inside the timed region
     e1.record(st)
     torch.cuda.synchronize()
     ms = reduce_max(e0.elapsed_time(e1), world, device="cuda" if world > 1 else None) / steps

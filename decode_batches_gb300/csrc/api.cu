@@ -88,6 +88,10 @@ struct moe_plan {
   WsLayout L{};
   TcMaps maps{};
   bool maps_weights = false, maps_ws = false;
+  // plan-owned second stream: the shared expert's gate/up runs there, beside the routing, when
+  // it occupies at most half of the SMs; forked from and joined back into the caller's stream
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   // timing
   bool timing = false;
   std::vector<TimedLaunch> timed;
@@ -143,7 +147,7 @@ static WsLayout layout_for(const moe_plan* p, int T_max) {
 }
 
 template <typename Tp>
-static Tp* ws_ptr(moe_plan* p, size_t off) {
+static Tp* ws_ptr(const moe_plan* p, size_t off) {
   return reinterpret_cast<Tp*>(p->ws + off);
 }
 
@@ -323,6 +327,9 @@ extern "C" void moe_plan_destroy(moe_plan* p) {
     cudaEventDestroy(t.stop);
   }
   for (auto e : p->event_pool) cudaEventDestroy(e);
+  if (p->ev_fork) cudaEventDestroy(p->ev_fork);
+  if (p->ev_join) cudaEventDestroy(p->ev_join);
+  if (p->side) cudaStreamDestroy(p->side);
   delete p;
 }
 
@@ -332,6 +339,18 @@ static moe_status ensure_err_word(moe_plan* p) {
   if (p->err) return MOE_OK;
   MOE_CUDA_TRY(cudaMalloc(&p->err, 2 * sizeof(uint32_t)));
   MOE_CUDA_TRY(cudaMemset(p->err, 0, 2 * sizeof(uint32_t)));
+  return MOE_OK;
+}
+
+// The plan's second stream (highest priority, so that its few blocks start ahead of queued ones)
+// and its fork/join events.
+static moe_status ensure_side_stream(moe_plan* p) {
+  if (p->side) return MOE_OK;
+  int lo = 0, hi = 0;
+  MOE_CUDA_TRY(cudaDeviceGetStreamPriorityRange(&lo, &hi));
+  if (!p->ev_fork) MOE_CUDA_TRY(cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming));
+  if (!p->ev_join) MOE_CUDA_TRY(cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming));
+  MOE_CUDA_TRY(cudaStreamCreateWithPriority(&p->side, cudaStreamNonBlocking, hi));
   return MOE_OK;
 }
 
@@ -526,6 +545,7 @@ extern "C" moe_status moe_plan_set_workspace(moe_plan* p, void* dev_ptr, size_t 
   p->L = L;
   moe_status s = ensure_err_word(p);
   if (s != MOE_OK) return s;
+  if ((s = ensure_side_stream(p)) != MOE_OK) return s;
   return build_ws_maps(p);
 }
 
@@ -592,50 +612,94 @@ static int tc_pair(const moe_plan* p, int T, bool routed, bool gate_up) {
   return 4 * units2 >= p->num_sms ? 2 : 1;
 }
 
+// Arguments of the grouped tensor-core kernels for one step.
+static TcArgs tc_args(const moe_plan* p, const uint16_t* x, int T, const int32_t* perm, uint16_t* y, uint16_t* y_s) {
+  TcArgs a;
+  a.w_gu = reinterpret_cast<const uint16_t*>(p->w_gu);
+  a.w_gu_s = p->w_gu_s;
+  a.w_down = reinterpret_cast<const uint16_t*>(p->w_down);
+  a.w_down_s = p->w_down_s;
+  a.segs = ws_ptr<Seg>(p, p->L.segs);
+  a.n_segs = ws_ptr<int32_t>(p, p->L.n_segs);
+  a.perm = perm;
+  a.x = x;
+  a.h = ws_ptr<uint16_t>(p, p->L.h);
+  a.h_s = ws_ptr<uint16_t>(p, p->L.h_s);
+  a.y = y;
+  a.y_s = y_s;
+  a.err = p->err;
+  a.T = T;
+  a.E = p->E;
+  a.k = p->k;
+  a.d = p->d;
+  a.f = p->f;
+  a.n_shared = p->n_shared;
+  a.f_s = p->f_s;
+  a.n_shared_segs = p->n_shared > 0 ? (T + kSegRowsMax - 1) / kSegRowsMax : 0;
+  if (p->wdtype == MOE_W_MXFP4) {
+    a.q_gu = p->w_gu;
+    a.q_down = p->w_down;
+    a.x16 = ws_ptr<uint16_t>(p, p->L.x16);
+  }
+  return a;
+}
+
+// The shared experts' arguments: the 16-bit kernels restricted to their units.
+static TcArgs shared_args(const moe_plan* p, const TcArgs& a, int T, bool gate_up) {
+  TcArgs sh = a;
+  sh.routed = 0;
+  sh.pair = tc_pair(p, T, false, gate_up);
+  return sh;
+}
+
+// With 4-bit routed weights the shared experts run on their own launches.  Their gate/up
+// depends on x alone, so when it fills at most half of the SMs it runs on the plan's second
+// stream beside the router and the grouping (which leave most SMs idle at such T) instead of
+// after them.
+static bool shared_gate_up_beside(const moe_plan* p, int T) {
+  if (!use_tc(p) || p->wdtype != MOE_W_MXFP4 || p->n_shared == 0 || !p->side) return false;
+  const long tiles = static_cast<long>(p->n_shared) * p->f_s / 64;
+  const int pair = tc_pair(p, T, false, true);
+  const long units = static_cast<long>((T + kSegRowsMax - 1) / kSegRowsMax) * ((tiles + pair - 1) / pair);
+  return 2 * units <= p->num_sms;
+}
+
+// Fork the shared gate/up onto the side stream (after everything already queued on st).
+static moe_status launch_shared_gate_up_beside(moe_plan* p, const uint16_t* x, int T, cudaStream_t st) {
+  if (!p->maps_weights || !p->maps_ws) return fail(MOE_ERR_NOT_READY, "tensor maps not built");
+  MOE_CUDA_TRY(cudaEventRecord(p->ev_fork, st));
+  MOE_CUDA_TRY(cudaStreamWaitEvent(p->side, p->ev_fork, 0));
+  const TcArgs sh = shared_args(p, tc_args(p, x, T, nullptr, nullptr, nullptr), T, true);
+  LAUNCH(p, "tc_gateup_shared", p->side, launch_tc_gateup(&p->maps, sh, p->num_sms, p->side));
+  MOE_CUDA_TRY(cudaEventRecord(p->ev_join, p->side));
+  return MOE_OK;
+}
+
+// Expert FFN over grouped rows; y/y_s outputs, h/h_s in the workspace.  For the tensor-core
+// path `segs`/`n_segs` must already describe the routed segments.  shared_forked: the shared
+// gate/up was launched on the side stream (launch_shared_gate_up_beside); st joins it before the
+// shared down projection.
 static moe_status run_experts(moe_plan* p, const uint16_t* x, int T, const int32_t* offsets, const int32_t* perm,
-                              uint16_t* y, uint16_t* y_s, cudaStream_t st) {
-  uint16_t* h = ws_ptr<uint16_t>(p, p->L.h);
-  uint16_t* h_s = ws_ptr<uint16_t>(p, p->L.h_s);
+                              uint16_t* y, uint16_t* y_s, cudaStream_t st, bool shared_forked = false) {
   if (use_tc(p)) {
     if (!p->maps_weights || !p->maps_ws) return fail(MOE_ERR_NOT_READY, "tensor maps not built");
-    TcArgs a;
-    a.w_gu = reinterpret_cast<const uint16_t*>(p->w_gu);
-    a.w_gu_s = p->w_gu_s;
-    a.w_down = reinterpret_cast<const uint16_t*>(p->w_down);
-    a.w_down_s = p->w_down_s;
-    a.segs = ws_ptr<Seg>(p, p->L.segs);
-    a.n_segs = ws_ptr<int32_t>(p, p->L.n_segs);
-    a.perm = perm;
-    a.x = x;
-    a.h = h;
-    a.h_s = h_s;
-    a.y = y;
-    a.y_s = y_s;
-    a.err = p->err;
-    a.T = T;
-    a.E = p->E;
-    a.k = p->k;
-    a.d = p->d;
-    a.f = p->f;
-    a.n_shared = p->n_shared;
-    a.f_s = p->f_s;
-    a.n_shared_segs = p->n_shared > 0 ? (T + kSegRowsMax - 1) / kSegRowsMax : 0;
+    TcArgs a = tc_args(p, x, T, perm, y, y_s);
     if (p->wdtype == MOE_W_MXFP4) {
       // routed experts on the 4-bit kernels (fp16 activations), shared experts on the 16-bit
       // kernels restricted to their units
       uint16_t* x16 = ws_ptr<uint16_t>(p, p->L.x16);
-      a.q_gu = p->w_gu;
-      a.q_down = p->w_down;
-      a.x16 = x16;
       LAUNCH(p, "x_to_f16", st, launch_x_to_f16(x, x16, static_cast<size_t>(T) * p->d, p->err, st));
       LAUNCH(p, "fp4_gateup", st, launch_fp4_gateup(&p->maps, a, p->num_sms, st));
-      TcArgs sh = a;
-      sh.routed = 0;
-      sh.pair = tc_pair(p, T, false, true);
-      if (p->n_shared > 0) LAUNCH(p, "tc_gateup_shared", st, launch_tc_gateup(&p->maps, sh, p->num_sms, st));
+      if (p->n_shared > 0 && !shared_forked) {
+        const TcArgs sh = shared_args(p, a, T, true);
+        LAUNCH(p, "tc_gateup_shared", st, launch_tc_gateup(&p->maps, sh, p->num_sms, st));
+      }
       LAUNCH(p, "fp4_down", st, launch_fp4_down(&p->maps, a, p->num_sms, st));
-      sh.pair = tc_pair(p, T, false, false);
-      if (p->n_shared > 0) LAUNCH(p, "tc_down_shared", st, launch_tc_down(&p->maps, sh, p->num_sms, st));
+      if (p->n_shared > 0) {
+        if (shared_forked) MOE_CUDA_TRY(cudaStreamWaitEvent(st, p->ev_join, 0));
+        const TcArgs sh = shared_args(p, a, T, false);
+        LAUNCH(p, "tc_down_shared", st, launch_tc_down(&p->maps, sh, p->num_sms, st));
+      }
     } else {
       a.pair = tc_pair(p, T, true, true);
       LAUNCH(p, "tc_gateup", st, launch_tc_gateup(&p->maps, a, p->num_sms, st));
@@ -644,6 +708,8 @@ static moe_status run_experts(moe_plan* p, const uint16_t* x, int T, const int32
     }
   } else {
     FfnWeights w = ffn_weights(p);
+    uint16_t* h = ws_ptr<uint16_t>(p, p->L.h);
+    uint16_t* h_s = ws_ptr<uint16_t>(p, p->L.h_s);
     LAUNCH(p, "simt_ffn", st, launch_ffn_simt(w, x, T, offsets, perm, h, h_s, y, y_s, st));
     p->launch_count += 1;  // the SIMT FFN is two kernels
   }
@@ -714,6 +780,16 @@ extern "C" moe_status moe_layer_forward(moe_plan* p, const void* x, int T, int n
   const int n_chunks = (T + kChunk - 1) / kChunk;
   const bool tc = use_tc(p);
   Seg* segs = tc ? ws_ptr<Seg>(p, p->L.segs) : nullptr;
+  const bool forked = shared_gate_up_beside(p, T);
+  if (forked && (s = launch_shared_gate_up_beside(p, xb, T, st)) != MOE_OK) return s;
+  struct Join {  // an error return between the fork and the join still joins the side stream
+    cudaStream_t st;
+    cudaEvent_t ev;
+    bool armed;
+    ~Join() {
+      if (armed) cudaStreamWaitEvent(st, ev, 0);
+    }
+  } join{st, p->ev_join, forked};
   if (router_nsplit(p, T) == router_small_splits(p->d) && !(p->router_tc && T > kRouterTcMinT) &&
       router_route_tiny_ok(T, p->E, p->d, p->k)) {
     // tiny step: router, top-k and grouping in one launch
@@ -739,8 +815,9 @@ extern "C" moe_status moe_layer_forward(moe_plan* p, const void* x, int T, int n
            launch_scatter(ids, masks, chunk_base, counts, T, p->E, p->k, perm, inv, offsets, segs,
                           ws_ptr<int32_t>(p, p->L.n_segs), p->L.max_segs, p->err, st));
   }
-  s = run_experts(p, xb, T, offsets, perm, y, y_s, st);
+  s = run_experts(p, xb, T, offsets, perm, y, y_s, st, forked);
   if (s != MOE_OK) return s;
+  join.armed = false;  // joined before the shared down projection
   LAUNCH(p, "combine", st, launch_combine(y, gates, inv, y_s, T, p->k, p->d, static_cast<uint16_t*>(out), st));
   return MOE_OK;
 }

@@ -31,6 +31,10 @@
  *     plan's device error word, read with moe_plan_get_device_error().
  *   - A plan is not thread-safe: one host thread issues its calls, and calls that share the
  *     plan's workspace must be ordered on one stream.
+ *   - moe_layer_forward may run part of its work on a second stream the plan owns: forked from
+ *     `stream` (an event recorded on it) and joined back (`stream` waits for an event of the
+ *     second stream) before the call's last launch, so every effect is ordered on `stream` as
+ *     if all of it ran there, and a graph capture of `stream` captures both.
  */
 #ifndef MOE_H_
 #define MOE_H_
