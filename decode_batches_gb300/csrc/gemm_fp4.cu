@@ -32,8 +32,11 @@ constexpr int BM = 128;
 constexpr int kSubK = 64;                        // one 128-byte-swizzled K slice / one 4-bit block
 constexpr int kSubs = 2;                         // K slices per pipeline stage (K = 128)
 constexpr int kStagesRaw = 8;                    // 4-bit stages in shared memory (~70 KB in flight)
-constexpr int kDqSets = 2;                       // dequant quartets; quartet s takes stages g % 2 == s
+constexpr int kDqSets = 2;                       // dequant quartets; quartet q takes the stages kk % 2 == q
 constexpr int kRawBytes = kSubs * kFp4BlockBytes;          // 8704 B per stage
+constexpr int kRawPer = 2;                       // stages per raw bulk copy (one per quartet)
+constexpr int kRawSlots = kStagesRaw / kRawPer;  // raw ring slots of kRawPer stages
+constexpr int kRawSlotBytes = kRawPer * kRawBytes;
 constexpr int kACols = kSubs * kSubK / 2;        // 64 columns (fp16 pairs) per A stage
 constexpr int kTmemCols = 512;                   // accumulators + A stages
 constexpr int kEpiStageBytes = 16 * 32 * 2;     // per epilogue warp: 16 columns x 32 fp16 rows
@@ -54,7 +57,7 @@ struct Geo {
   static constexpr int kSmemBytes =
       kStages * kBBytes + kStagesRaw * kRawBytes + 1024 + 1024 + kTokBytes + 4 * kEpiStageBytes;
   static constexpr int threads(bool gate_up) { return 32 * (gate_up ? 6 + kGatherWarps + 8 : 7 + 8); }
-  static_assert(kStagesRaw % kDqSets == 0 && kStages % kDqSets == 0, "rings must split evenly between quartets");
+  static_assert(kRawPer == kDqSets && kStagesRaw % kRawPer == 0, "one stage of each raw copy per quartet");
   static_assert(kAStart + kStages * kACols <= kTmemCols, "TMEM columns");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(kN <= kSegRowsMax && kN % 32 == 0, "segment rows");
@@ -131,7 +134,10 @@ MOE_DEVICE void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uin
 
 // Pipeline.  Stage g covers K slices [2g, 2g + 2) of the unit (the last stage of an odd K/64
 // has one).  Rings:
-//   raw[g % kStagesRaw]  4-bit blocks, filled by one bulk copy, freed by the quartet that read them
+//   raw[p % kRawSlots]   the 4-bit blocks of stages 2p', 2p' + 1 of a unit (p' the pair within the
+//                        unit, p counting pairs): one bulk copy per pair (a fixed cost per bulk
+//                        operation makes fewer, larger copies stream faster); quartet q reads
+//                        stage 2p' + q, and both quartets free the slot
 //   A/B[g % kStages]     dequantised weights in TMEM + activation rows in shared memory; full when
 //                        the quartet (4 arrivals) and the B producer (the slot's gather warp, or
 //                        one arrive.expect_tx for TMA) are done, empty when the MMAs reading it finish.
@@ -166,9 +172,9 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStagesRaw; ++s) {
+    for (int s = 0; s < kRawSlots; ++s) {
       mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], 4);
+      mbar_init(&raw_empty[s], 4 * kDqSets);
     }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 4 + (kGateUp ? kGatherPerSlot : 1));  // dequant quartet + B producer(s)
@@ -197,24 +203,26 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
   const int tiles = kGateUp ? a.f / 64 : a.d / BM;
   const int nsub = (kGateUp ? a.d : a.f) / kSubK;          // K slices (4-bit blocks) per unit
   const int nst = (nsub + kSubs - 1) / kSubs;              // stages per unit
+  const int npair = (nst + kRawPer - 1) / kRawPer;         // raw copies per unit
   const int total_units = (*a.n_segs) * tiles;
   const uint8_t* wq = kGateUp ? a.q_gu : a.q_down;
 
   if (warp == 0) {
     // ---------------- raw 4-bit blocks: one bulk copy per stage (the blocks are adjacent) -----
     const uint64_t pol_w = l2_policy_evict_first();
-    uint32_t g = 0;
+    uint32_t p = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
       const Unit un = decode_unit(u, a.segs, tiles);
       const uint8_t* w0 = wq + (static_cast<size_t>(un.expert) * tiles + un.tile) * nsub * kFp4BlockBytes;
-      for (int kk = 0; kk < nst; ++kk, ++g) {
-        const int slot = g % kStagesRaw;
-        const uint32_t bytes = static_cast<uint32_t>(min(kSubs, nsub - kSubs * kk)) * kFp4BlockBytes;
-        if (!(ok = mbar_wait_warp(&raw_empty[slot], ((g / kStagesRaw) & 1u) ^ 1u, abort_flag, a.err))) break;
+      for (int kp = 0; kp < npair; ++kp, ++p) {
+        const int slot = p % kRawSlots;
+        const int sub0 = kRawPer * kSubs * kp;
+        const uint32_t bytes = static_cast<uint32_t>(min(kRawPer * kSubs, nsub - sub0)) * kFp4BlockBytes;
+        if (!(ok = mbar_wait_warp(&raw_empty[slot], ((p / kRawSlots) & 1u) ^ 1u, abort_flag, a.err))) break;
         if (elect_one()) {
           mbar_arrive_expect_tx(&raw_full[slot], bytes);
-          bulk_load(ring_raw + slot * kRawBytes, w0 + static_cast<size_t>(kSubs * kk) * kFp4BlockBytes, bytes,
+          bulk_load(ring_raw + slot * kRawSlotBytes, w0 + static_cast<size_t>(sub0) * kFp4BlockBytes, bytes,
                     &raw_full[slot], pol_w);
         }
         __syncwarp();
@@ -346,15 +354,18 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
     const int r = 32 * q + lane;  // weight row of the tile owned by this thread
     const uint32_t set = static_cast<uint32_t>(warp - kDqWarp) >> 2;
     const uint32_t trow = tmem + (static_cast<uint32_t>(32 * q) << 16) + kAStart;
-    uint32_t g = 0;
+    uint32_t p = 0, uidx = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-      for (int kk = 0; kk < nst; ++kk, ++g) {
-        if ((g % kDqSets) != set) continue;
-        const int sr = g % kStagesRaw, s = g % kStages;
-        const int subs = min(kSubs, nsub - kSubs * kk);
-        if (!(ok = mbar_wait_warp(&raw_full[sr], (g / kStagesRaw) & 1u, abort_flag, a.err))) break;
-        const uint8_t* blk = ring_raw + sr * kRawBytes;
+    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++uidx) {
+      for (int kp = 0; kp < npair; ++kp, ++p) {
+        const int kk = kRawPer * kp + static_cast<int>(set);
+        const bool have = kk < nst;  // the last pair of an odd stage count has one stage
+        const int sr = p % kRawSlots;
+        const uint32_t g = uidx * static_cast<uint32_t>(nst) + static_cast<uint32_t>(kk);
+        const int s = g % kStages;
+        const int subs = have ? min(kSubs, nsub - kSubs * kk) : 0;
+        if (!(ok = mbar_wait_warp(&raw_full[sr], (p / kRawSlots) & 1u, abort_flag, a.err))) break;
+        const uint8_t* blk = ring_raw + sr * kRawSlotBytes + set * kRawBytes;
         uint4 c[kSubs][2];
         uint32_t sc[kSubs];
 #pragma unroll
@@ -368,6 +379,7 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&raw_empty[sr]);  // the raw bytes are in registers now
+        if (!have) continue;
         if (!(ok = mbar_wait_warp(&empty[s], ((g / kStages) & 1u) ^ 1u, abort_flag, a.err))) break;
 #pragma unroll
         for (int j2 = 0; j2 < kSubs; ++j2) {
