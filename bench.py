@@ -341,7 +341,8 @@ def run_gpu(args):
     x_np = w.x()
     T = w.T
     sweep_q = [q for q in synth.QUANTA] if (args.workload == "mixed" and not args.no_sweep) else []
-    T_max = max([T] + [q + 3 for q in sweep_q])
+    serve = args.workload == "mixed" and not args.no_extra
+    T_max = max([T] + [q + 3 for q in sweep_q] + ([SERVE_CAP_MAX + SERVE_DECODE_ROWS] if serve else []))
     # weights: identical layer on every rank (seed 0); tokens per rank from the rank's seed
     wl_weights = synth.workload(args.workload, quantum=args.quantum, seed=0)
     plan = upload_plan(wl_weights, T_max)
@@ -398,6 +399,8 @@ def run_gpu(args):
                       "bound": "hbm" if bq["bytes"] / (hbm * 1e9) >= bq["flops"] / (tflops * 1e12) else "tensor",
                       "kernel_us": {k: round(v[1] / v[0] * 1e3, 2) for k, v in kq.items()}})
 
+    serving = serving_runs(plan, world, rank) if serve else None
+
     extra = {}
     if not args.no_extra and args.workload == "mixed":
         # the other configurations of the layer: 4-token decode on the same plan; the 4-bit Zipf
@@ -445,6 +448,7 @@ def run_gpu(args):
         "clocks": clk,
         "sweep": sweep,
         "workloads": extra,
+        "serving": serving,
         "cpu_baseline": cpu,
     }
     if rank == 0:
@@ -453,6 +457,50 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.barrier()
         dist.destroy_process_group()
+
+
+SERVE_DECODE_ROWS = 3      # generating sessions riding along in every prefill call (c2's mix)
+SERVE_CAP_MAX = 4096       # the engine's default prefill_cap
+
+
+def serving_runs(plan, world: int, rank: int, reps: int = 3) -> dict:
+    """Whole prompts prefilled through the step composer (the library's moe_compose_prefill), one
+    layer call per composed call with SERVE_DECODE_ROWS decode rows appended while sessions are
+    generating -- the one-layer analogue of the "moe-prefill-quantum" page's Figure 1 / Table 3
+    (a 20,000-token cold prefill per quantum, three sessions decoding), Table 11 (an 8,478-token
+    span at a context of 81,920 cut at boundaries 4096 / 3072 / 2560) and Table 1's first row
+    (nothing generating: the quantum is not used).  Time per prompt: CUDA events around all its
+    calls, median of `reps` after one warm-up run."""
+    import torch
+    from decode_batches_gb300 import compose_prefill
+    src = synth.workload("mixed", quantum=SERVE_CAP_MAX, seed=rank_seed(7, rank))
+    x_all = torch.from_numpy(np.ascontiguousarray(src.x())).cuda().view(torch.bfloat16)
+    out = torch.empty_like(x_all)
+    st = torch.cuda.current_stream()
+
+    def run(start, n, q, active, cap):
+        calls = compose_prefill(start, n, q, active, cap)
+        dec = SERVE_DECODE_ROWS if active else 0
+        times = []
+        for r in range(reps + 1):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            for _, c, _ in calls:
+                plan.forward(x_all[:c + dec], n_prefill=c, out=out[:c + dec])
+            e1.record(st)
+            torch.cuda.synchronize()
+            if r:
+                times.append(e0.elapsed_time(e1))
+        ms = reduce_max(statistics.median(times), world, device="cuda" if world > 1 else None)
+        return {"prompt_tokens": n, "start_pos": start, "quantum": q, "generation_active": active,
+                "prefill_cap": cap, "calls": len(calls), "mean_call": round(n / len(calls), 1),
+                "decode_rows_per_call": dec, "ms": round(ms, 3),
+                "prefill_tokens_per_s": round(world * n / (ms * 1e-3), 1)}
+
+    fig1 = [run(0, 20000, q, True, SERVE_CAP_MAX) for q in synth.QUANTA]
+    t11 = [run(81920, 8478, 2048, True, cap) for cap in (4096, 3072, 2560)]
+    idle = [run(0, 20000, q, False, SERVE_CAP_MAX) for q in (128, 2048)]
+    return {"prefill_vs_quantum": fig1, "calls_vs_boundary": t11, "no_generation": idle}
 
 
 def measure_workload(plan, w: synth.Workload, hbm: float, tflops: float, world: int, args, committed=None) -> dict:

@@ -31,10 +31,15 @@ EXPORTED = (
     "moe_plan_workspace_bytes", "moe_plan_set_workspace", "moe_plan_set_path", "moe_layer_forward",
     "moe_route", "moe_route_logits", "moe_permute", "moe_experts", "moe_combine",
     "moe_plan_get_device_error", "moe_plan_enable_timing", "moe_plan_timing_report",
-    "moe_plan_last_launch_count",
+    "moe_plan_last_launch_count", "moe_compose_prefill",
 )
 
 _lib = None
+
+
+class PrefillCall(ctypes.Structure):
+    """moe_prefill_call: one layer call of a prompt's prefill."""
+    _fields_ = [("pos", ctypes.c_int64), ("n", ctypes.c_int32), ("piece", ctypes.c_int32)]
 
 
 class MoeError(RuntimeError):
@@ -72,6 +77,8 @@ def load_library(path: str = LIB_PATH):
         "moe_plan_enable_timing": ([vp, i32], i32),
         "moe_plan_timing_report": ([vp, ctypes.c_char_p, sz], sz),
         "moe_plan_last_launch_count": ([vp], i32),
+        "moe_compose_prefill": ([ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                 ctypes.POINTER(PrefillCall), ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -79,6 +86,20 @@ def load_library(path: str = LIB_PATH):
         fn.restype = res
     _lib = lib
     return lib
+
+
+def compose_prefill(start_pos: int, n_tokens: int, quantum: int, generation_active: bool,
+                    prefill_cap: int = 4096):
+    """The layer calls that prefill ``n_tokens`` prompt tokens from context position
+    ``start_pos`` (moe_compose_prefill): a list of (pos, n, piece) tuples, in order."""
+    lib = load_library()
+    total = ctypes.c_int64(0)
+    _check(lib.moe_compose_prefill(start_pos, n_tokens, quantum, int(bool(generation_active)), prefill_cap, None, 0,
+                                   ctypes.byref(total)))
+    arr = (PrefillCall * max(1, total.value))()
+    _check(lib.moe_compose_prefill(start_pos, n_tokens, quantum, int(bool(generation_active)), prefill_cap, arr,
+                                   total.value, ctypes.byref(total)))
+    return [(c.pos, c.n, c.piece) for c in arr[:total.value]]
 
 
 def _check(status: int):

@@ -39,6 +39,11 @@ static moe_status fail(moe_status s, const char* fmt, ...) {
 
 extern "C" const char* moe_last_error(void) { return g_last_error.c_str(); }
 
+moe_status moe::fail_message(moe_status s, const char* msg) {
+  g_last_error = msg;
+  return s;
+}
+
 // ============================================================================================
 // plan
 // ============================================================================================

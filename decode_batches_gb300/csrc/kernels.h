@@ -5,7 +5,12 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/moe.h"
+
 namespace moe {
+
+// Sets the thread's moe_last_error() message and returns s (api.cu).
+moe_status fail_message(moe_status s, const char* msg);
 
 // Tokens per chunk of the grouping step: one 32-bit mask word per (chunk, expert).
 constexpr int kChunk = 32;

@@ -236,6 +236,33 @@ size_t moe_plan_timing_report(moe_plan* plan, char* buf, size_t len);
 /* Number of kernels the most recent moe_layer_forward call launched. */
 int moe_plan_last_launch_count(const moe_plan* plan);
 
+/*
+ * Step composer: the layer calls (serving steps) a prompt's prefill is cut into.
+ * Source: "moe-prefill-quantum" -- the cause section's source excerpt (the server hands the
+ * prompt over in pieces of `quantum` tokens while any request is generating, else of 2048) and
+ * the section on prefill_cap boundaries with its code excerpt and Table 11 (the engine cuts a
+ * piece where the absolute context position crosses a multiple of prefill_cap; a prompt that
+ * starts off a boundary keeps being cut, e.g. 2048, 509, 1539, ... from 1539 mod 4096).
+ * Reading where the excerpt is silent: no call exceeds prefill_cap tokens.
+ *
+ * Host-only and pure (no device work, no plan).  Prefilling n_tokens prompt tokens from
+ * context position start_pos: writes the first min(total, max_calls) calls, in order, to
+ * `calls` (host memory; may be NULL when max_calls == 0) and the total number of calls to
+ * *n_calls (host pointer).  Each call's `n` prompt rows go to moe_layer_forward as its
+ * n_prefill rows, followed by one row per generating request.
+ * MOE_ERR_INVALID_ARG when start_pos < 0, n_tokens < 0, quantum < 1, prefill_cap < 1 or
+ * n_calls is NULL.
+ */
+typedef struct {
+  int64_t pos;   /* context position of the call's first prompt token */
+  int32_t n;     /* prompt tokens in the call, 1 <= n <= prefill_cap */
+  int32_t piece; /* index of the server piece the call belongs to */
+} moe_prefill_call;
+
+moe_status moe_compose_prefill(int64_t start_pos, int64_t n_tokens, int32_t quantum,
+                               int32_t generation_active, int32_t prefill_cap,
+                               moe_prefill_call* calls, int64_t max_calls, int64_t* n_calls);
+
 #ifdef __cplusplus
 }
 #endif

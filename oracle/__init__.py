@@ -32,4 +32,6 @@ from .moe_ref import (  # noqa: F401
     expected_unique_experts,
     tokens_per_expert,
     quantum_for_tokens_per_expert,
+    prefill_piece_size,
+    prefill_calls,
 )

@@ -267,3 +267,47 @@ def tokens_per_expert(Q: int, k: int, E: int) -> float:
 def quantum_for_tokens_per_expert(target: float, E: int, k: int) -> float:
     """[P1] the inversion: quantum = target * E / k."""
     return target * E / k
+
+
+# ---------------------------------------------------------------------------------------
+# Prefill chunking of the serving loop from [P1] (the step composer's definition)
+# ---------------------------------------------------------------------------------------
+
+def prefill_piece_size(quantum: int, generation_active: bool) -> int:
+    """[P1] the cause section's source excerpt: the server's prefill piece is the configured
+    quantum only while some request is generating tokens; otherwise it is a fixed 2048."""
+    return quantum if generation_active else 2048
+
+
+def prefill_calls(start_pos: int, n_tokens: int, quantum: int, generation_active: bool,
+                  prefill_cap: int = 4096) -> list:
+    """[P1] the GPU calls that prefill ``n_tokens`` prompt tokens starting at context position
+    ``start_pos``, as (pos, n) pairs in order.
+
+    Two levels, as the page describes them:
+      * the server hands the prompt over in pieces of ``prefill_piece_size`` tokens, counted
+        from the start of the prompt;
+      * the engine cuts each piece at the multiples of ``prefill_cap`` in absolute position (the
+        section on ``prefill_cap`` boundaries and its code excerpt): a call starting at ``pos``
+        with ``pos % prefill_cap != 0`` ends at the next multiple at the latest.
+    Reading where the excerpt is silent: a call also never exceeds ``prefill_cap`` tokens (the
+    engine's batch buffer is sized by it), so a piece larger than ``prefill_cap`` is cut at the
+    boundaries too.  With a prompt starting at 1539 modulo 4096 and pieces of 2048 this gives
+    the page's repeating 2048, 509, 1539."""
+    if n_tokens < 0 or quantum < 1 or prefill_cap < 1 or start_pos < 0:
+        raise ValueError("bad arguments")
+    piece = prefill_piece_size(quantum, generation_active)
+    calls = []
+    pos, left = start_pos, n_tokens
+    while left > 0:
+        rem = min(piece, left)
+        while rem > 0:
+            n = min(rem, prefill_cap)
+            mod = pos % prefill_cap
+            if mod != 0:
+                n = min(n, prefill_cap - mod)
+            calls.append((pos, n))
+            pos += n
+            rem -= n
+            left -= n
+    return calls

@@ -276,3 +276,28 @@ def test_fp4_scales_outside_fp16_range_use_the_reference_path():
     ref = oracle.moe_layer(w.x(), w.router_weight(), None, s.k,
                            oracle.DecodedExperts(ex.gate, ex.up, ex.down, gs, ex.up_scale, ex.down_scale), sh)
     compare_layer(out, ref, s.k, TOL_FP4)
+
+
+def test_composed_prefill_calls_vs_oracle():
+    """A prompt prefilled through the step composer: each composed call (its prompt rows plus two
+    decode rows) goes through moe_layer_forward with its own T, and every row matches the oracle
+    (the layer is per token, so the calls reassemble the whole prompt's output)."""
+    from decode_batches_gb300 import compose_prefill
+    n_prompt, n_dec = 700, 2
+    w = synth.custom(synth.TINY, n_prompt + n_dec, n_prefill=n_prompt, name="composed")
+    plan = make_plan(w, T_max=300)
+    plan.set_path("tc")
+    xs = w.x()
+    calls = compose_prefill(1539, n_prompt, 128, True, prefill_cap=256)
+    assert sum(c for _, c, _ in calls) == n_prompt and max(c for _, c, _ in calls) <= 128
+    ref = oracle_layer(w)
+    got = np.zeros_like(ref["out"])
+    done = 0
+    for _, c, _ in calls:
+        rows = np.concatenate([np.arange(done, done + c), np.arange(n_prompt, n_prompt + n_dec)])
+        out = bf16_tensor_to_f64(plan.forward(to_dev(xs[rows], "bf16"), n_prefill=c))
+        got[done:done + c] = out[:c]
+        got[n_prompt:] = out[c:]
+        done += c
+    compare_layer(got, ref, synth.TINY.k, TOL_BF16)
+    assert plan.device_error() == 0

@@ -380,3 +380,73 @@ def test_selection_wakes_the_expected_number_of_experts():
     # tokens per expert: counts average Q*k/E (Table 9: 3.0 at Q = 128)
     counts = oracle.expert_histogram(oracle.select_topk(rng.normal(size=(Q, E)), k), E)
     assert counts.sum() == Q * k and counts.mean() == 3.0
+
+
+# ---------------------------------------------------------------------------------------
+# Prefill chunking of the serving loop ("moe-prefill-quantum": the cause section's source
+# excerpt, the prefill_cap section and Table 11)
+# ---------------------------------------------------------------------------------------
+def _golden_calls():
+    seq, t11 = [], []
+    for line in open(os.path.join(GOLDEN, "p1_prefill_calls.txt")):
+        f = line.split()
+        if not f or f[0].startswith("#"):
+            continue
+        if f[0] == "SEQ":
+            seq.append((int(f[1]), int(f[2]), int(f[3]), int(f[4]), [int(v) for v in f[5:]]))
+        elif f[0] == "T11":
+            t11.append(tuple(int(v) for v in f[1:]))
+    return seq, t11
+
+
+def test_prefill_calls_reproduce_the_pages_sequences():
+    seq, _ = _golden_calls()
+    assert len(seq) == 2
+    for start, q, cap, n, want in seq:
+        got = [c for _, c in oracle.prefill_calls(start, n, q, True, cap)]
+        assert got == want
+
+
+def test_prefill_calls_reproduce_table_11():
+    """Table 11 prints calls and mean chunk per boundary for an 8,478-token span at a context of
+    about 82K.  Reading: the span starts at 81,920 (= 20 x 4096), the only start between 78,000
+    and 86,000 that gives the printed call counts for all three boundaries."""
+    _, t11 = _golden_calls()
+    assert len(t11) == 3
+    for n, cap, calls, mean in t11:
+        c = oracle.prefill_calls(81920, n, 2048, True, cap)
+        assert len(c) == calls and n // len(c) == mean
+    hits = [s for s in range(78000, 86000)
+            if all(len(oracle.prefill_calls(s, n, 2048, True, cap)) == calls for n, cap, calls, _ in t11)]
+    assert hits == [81920]
+
+
+def test_prefill_calls_ignore_the_quantum_when_nothing_generates():
+    """Table 1's first row: without decoding load quantum 128 and 2048 run identically (the
+    hard-coded 2048 piece)."""
+    for start in (0, 1539, 81920):
+        assert oracle.prefill_calls(start, 5964, 128, False) == oracle.prefill_calls(start, 5964, 2048, False)
+        assert oracle.prefill_calls(start, 5964, 128, False) == oracle.prefill_calls(start, 5964, 2048, True)
+    assert len(oracle.prefill_calls(0, 5964, 128, True)) == 47
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_prefill_calls_invariants(seed):
+    rng = np.random.default_rng(seed)
+    for _ in range(200):
+        start = int(rng.integers(0, 300000))
+        n = int(rng.integers(0, 40000))
+        q = int(rng.choice([1, 7, 128, 512, 1000, 2048, 4096, 8192, 100000]))
+        cap = int(rng.choice([1, 64, 2560, 3072, 4096, 8192]))
+        active = bool(rng.integers(0, 2))
+        piece = q if active else 2048
+        calls = oracle.prefill_calls(start, n, q, active, cap)
+        assert sum(c for _, c in calls) == n
+        pos = start
+        for p, c in calls:
+            assert p == pos and 1 <= c <= min(piece, cap)
+            assert (p % cap) + c <= cap  # never crosses a boundary
+            pos += c
+        # every piece edge (multiples of the piece from the prompt start) is a call edge
+        edges = {p - start for p, _ in calls} | {n}
+        assert all(e in edges for e in range(0, n, piece))
