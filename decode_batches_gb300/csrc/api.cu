@@ -660,7 +660,11 @@ static TcArgs shared_args(const moe_plan* p, const TcArgs& a, int T, bool gate_u
 // With 4-bit routed weights the shared experts run on their own launches.  Their gate/up
 // depends on x alone, so when it fills at most half of the SMs it runs on the plan's second
 // stream beside the router and the grouping (which leave most SMs idle at such T) instead of
-// after them.
+// after them.  The shared down projection follows it there when kSharedDownBeside (it needs h_s
+// alone; its blocks take the SMs the routed gate/up's last, partial round of units leaves idle,
+// the side stream having the higher priority), and the caller's stream joins before the combine.
+constexpr bool kSharedDownBeside = true;
+
 static bool shared_gate_up_beside(const moe_plan* p, int T) {
   if (!use_tc(p) || p->wdtype != MOE_W_MXFP4 || p->n_shared == 0 || !p->side) return false;
   const long tiles = static_cast<long>(p->n_shared) * p->f_s / 64;
@@ -676,14 +680,18 @@ static moe_status launch_shared_gate_up_beside(moe_plan* p, const uint16_t* x, i
   MOE_CUDA_TRY(cudaStreamWaitEvent(p->side, p->ev_fork, 0));
   const TcArgs sh = shared_args(p, tc_args(p, x, T, nullptr, nullptr, nullptr), T, true);
   LAUNCH(p, "tc_gateup_shared", p->side, launch_tc_gateup(&p->maps, sh, p->num_sms, p->side));
+  if (kSharedDownBeside) {
+    const TcArgs shd = shared_args(p, tc_args(p, x, T, nullptr, nullptr, ws_ptr<uint16_t>(p, p->L.y_s)), T, false);
+    LAUNCH(p, "tc_down_shared", p->side, launch_tc_down(&p->maps, shd, p->num_sms, p->side));
+  }
   MOE_CUDA_TRY(cudaEventRecord(p->ev_join, p->side));
   return MOE_OK;
 }
 
 // Expert FFN over grouped rows; y/y_s outputs, h/h_s in the workspace.  For the tensor-core
 // path `segs`/`n_segs` must already describe the routed segments.  shared_forked: the shared
-// gate/up was launched on the side stream (launch_shared_gate_up_beside); st joins it before the
-// shared down projection.
+// expert was launched on the side stream (launch_shared_gate_up_beside); unless its down
+// projection went there too, st joins the side stream before launching it.
 static moe_status run_experts(moe_plan* p, const uint16_t* x, int T, const int32_t* offsets, const int32_t* perm,
                               uint16_t* y, uint16_t* y_s, cudaStream_t st, bool shared_forked = false) {
   if (use_tc(p)) {
@@ -700,7 +708,7 @@ static moe_status run_experts(moe_plan* p, const uint16_t* x, int T, const int32
         LAUNCH(p, "tc_gateup_shared", st, launch_tc_gateup(&p->maps, sh, p->num_sms, st));
       }
       LAUNCH(p, "fp4_down", st, launch_fp4_down(&p->maps, a, p->num_sms, st));
-      if (p->n_shared > 0) {
+      if (p->n_shared > 0 && !(shared_forked && kSharedDownBeside)) {
         if (shared_forked) MOE_CUDA_TRY(cudaStreamWaitEvent(st, p->ev_join, 0));
         const TcArgs sh = shared_args(p, a, T, false);
         LAUNCH(p, "tc_down_shared", st, launch_tc_down(&p->maps, sh, p->num_sms, st));
@@ -822,7 +830,8 @@ extern "C" moe_status moe_layer_forward(moe_plan* p, const void* x, int T, int n
   }
   s = run_experts(p, xb, T, offsets, perm, y, y_s, st, forked);
   if (s != MOE_OK) return s;
-  join.armed = false;  // joined before the shared down projection
+  if (forked && kSharedDownBeside) MOE_CUDA_TRY(cudaStreamWaitEvent(st, p->ev_join, 0));
+  join.armed = false;  // joined (before the shared down projection or here)
   LAUNCH(p, "combine", st, launch_combine(y, gates, inv, y_s, T, p->k, p->d, static_cast<uint16_t*>(out), st));
   return MOE_OK;
 }
