@@ -240,25 +240,38 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
       tc_fence_after();
       const uint32_t d_tmem = tmem + buf * kAccCols;
       const uint32_t idesc = idesc_f16_f32(BM, N);
-      for (int kk = 0; kk < nst; ++kk, ++g) {
+      // The elected lane issues a run of consecutive stages that are already full (testing each
+      // next barrier itself), so the warp-wide bookkeeping is paid once per run, not per stage.
+      for (int kk = 0; kk < nst;) {
         const int s = g % kStages;
         if (!ready && !(ok = mbar_wait_warp(&full[s], (g / kStages) & 1u, abort_flag, a.err))) break;
-        const uint32_t gn = g + 1;  // probe the next stage now, use the answer next iteration
-        const bool next = mbar_test(&full[gn % kStages], (gn / kStages) & 1u);
         tc_fence_after();
-        const uint32_t a_tmem = tmem + kAStart + s * kACols;
-        const uint64_t bdesc = smem_desc_sw128(smem_u32(ring_b + s * kBBytes));
-        const int subs = min(kSubs, nsub - kSubs * kk);
+        int issued = 0;
         if (elect_one()) {
-          for (int j2 = 0; j2 < subs; ++j2) {
+          uint32_t gg = g;
+          int k2 = kk;
+          while (true) {
+            const int ss = gg % kStages;
+            const uint32_t a_tmem = tmem + kAStart + ss * kACols;
+            const uint64_t bdesc = smem_desc_sw128(smem_u32(ring_b + ss * kBBytes));
+            const int subs = min(kSubs, nsub - kSubs * k2);
+            for (int j2 = 0; j2 < subs; ++j2) {
 #pragma unroll
-            for (int ks = 0; ks < kSubK / 16; ++ks)  // K = 16 per MMA: 8 TMEM columns of A, +32 B of B
-              mma_f16_ts(d_tmem, a_tmem + 32 * j2 + 8 * ks, bdesc + (kSubBytes >> 4) * j2 + 2 * ks, idesc,
-                         (kk | j2 | ks) != 0);
+              for (int ks = 0; ks < kSubK / 16; ++ks)  // K = 16 per MMA: 8 TMEM columns of A, +32 B of B
+                mma_f16_ts(d_tmem, a_tmem + 32 * j2 + 8 * ks, bdesc + (kSubBytes >> 4) * j2 + 2 * ks, idesc,
+                           (k2 | j2 | ks) != 0);
+            }
+            mma_commit(&empty[ss]);
+            ++gg, ++k2, ++issued;
+            if (k2 >= nst || !mbar_test(&full[gg % kStages], (gg / kStages) & 1u)) break;
+            tc_fence_after();
           }
-          mma_commit(&empty[s]);
         }
-        ready = __all_sync(0xffffffffu, next);
+        issued = static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<uint32_t>(issued)));
+        kk += issued;
+        g += static_cast<uint32_t>(issued);
+        // probe the next stage (possibly the next unit's first) now, use the answer next iteration
+        ready = __all_sync(0xffffffffu, mbar_test(&full[g % kStages], (g / kStages) & 1u));
       }
       if (!ok) break;
       if (elect_one()) mma_commit(&acc_full[buf]);
