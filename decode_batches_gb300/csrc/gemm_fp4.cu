@@ -132,6 +132,60 @@ MOE_DEVICE void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uin
       : "memory");
 }
 
+// The MMAs of one 128-deep stage in one block: `two` ? 8 : 4 MMAs of K = 16, D += A x B^T with A
+// in TMEM (+8 columns per step, +32 per 64-wide slice) and B in shared memory (descriptor +2 per
+// step, +kSubDesc per slice).  Only the first MMA may start a fresh accumulation (acc == 0); the
+// offsets are added inside the block, off the issuing lane's dependency chain.
+template <uint32_t kSubDesc>
+MOE_DEVICE void mma_stage_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc, bool two) {
+  if (two)
+    asm volatile(
+        "{\n\t.reg .pred p, t;\n\t.reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t"
+        ".reg .b64 b1, b2, b3, b4, b5, b6, b7;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 t, %4, %4;\n\t"
+        "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\tadd.u32 a4, %1, 32;\n\t"
+        "add.u32 a5, %1, 40;\n\tadd.u32 a6, %1, 48;\n\tadd.u32 a7, %1, 56;\n\t"
+        "add.u64 b1, %2, 2;\n\tadd.u64 b2, %2, 4;\n\tadd.u64 b3, %2, 6;\n\tadd.u64 b4, %2, %5;\n\t"
+        "add.u64 b5, b4, 2;\n\tadd.u64 b6, b4, 4;\n\tadd.u64 b7, b4, 6;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b4, %3, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], b5, %3, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b6, %3, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], b7, %3, t;\n\t}" ::"r"(d),
+        "r"(a), "l"(b), "r"(idesc), "r"(acc), "n"(static_cast<uint64_t>(kSubDesc))
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p, t;\n\t.reg .b32 a1, a2, a3;\n\t.reg .b64 b1, b2, b3;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 t, %4, %4;\n\t"
+        "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+        "add.u64 b1, %2, 2;\n\tadd.u64 b2, %2, 4;\n\tadd.u64 b3, %2, 6;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t;\n\t}" ::"r"(d),
+        "r"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// tcgen05.commit / mbarrier.test_wait on a barrier given by its shared-memory address.
+MOE_DEVICE void mma_commit_u32(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+MOE_DEVICE bool mbar_test_u32(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Pipeline.  Stage g covers K slices [2g, 2g + 2) of the unit (the last stage of an odd K/64
 // has one).  Rings:
 //   raw[p % kRawSlots]   the 4-bit blocks of stages 2p', 2p' + 1 of a unit (p' the pair within the
@@ -230,6 +284,9 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer (A from TMEM): the warp waits, one elected lane issues -------
+    const uint32_t a_base = tmem + kAStart;
+    const uint64_t b_base = smem_desc_sw128(smem_u32(ring_b));
+    const uint32_t full_u32 = smem_u32(full), empty_u32 = smem_u32(empty);
     uint32_t g = 0, j = 0;
     bool ok = true, ready = false;  // ready: full[g % kStages] already seen complete for stage g
     for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++j) {
@@ -248,22 +305,17 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
         tc_fence_after();
         int issued = 0;
         if (elect_one()) {
-          uint32_t gg = g;
+          // slot and phase advance incrementally: the lane's dependency chain per stage is the
+          // address arithmetic, the MMA block, the commit and the next barrier's test
+          uint32_t ss = static_cast<uint32_t>(s), ph = (g / kStages) & 1u;
           int k2 = kk;
           while (true) {
-            const int ss = gg % kStages;
-            const uint32_t a_tmem = tmem + kAStart + ss * kACols;
-            const uint64_t bdesc = smem_desc_sw128(smem_u32(ring_b + ss * kBBytes));
-            const int subs = min(kSubs, nsub - kSubs * k2);
-            for (int j2 = 0; j2 < subs; ++j2) {
-#pragma unroll
-              for (int ks = 0; ks < kSubK / 16; ++ks)  // K = 16 per MMA: 8 TMEM columns of A, +32 B of B
-                mma_f16_ts(d_tmem, a_tmem + 32 * j2 + 8 * ks, bdesc + (kSubBytes >> 4) * j2 + 2 * ks, idesc,
-                           (k2 | j2 | ks) != 0);
-            }
-            mma_commit(&empty[ss]);
-            ++gg, ++k2, ++issued;
-            if (k2 >= nst || !mbar_test(&full[gg % kStages], (gg / kStages) & 1u)) break;
+            mma_stage_ts<(kSubBytes >> 4)>(d_tmem, a_base + ss * kACols, b_base + ss * (kBBytes >> 4), idesc,
+                                           static_cast<uint32_t>(k2), nsub - kSubs * k2 >= kSubs);
+            mma_commit_u32(empty_u32 + 8 * ss);
+            ++k2, ++issued;
+            if (++ss == static_cast<uint32_t>(kStages)) ss = 0, ph ^= 1u;
+            if (k2 >= nst || !mbar_test_u32(full_u32 + 8 * ss, ph)) break;
             tc_fence_after();
           }
         }
