@@ -31,11 +31,9 @@ namespace fq {
 constexpr int BM = 128;
 constexpr int kSubK = 64;                        // one 128-byte-swizzled K slice / one 4-bit block
 constexpr int kSubs = 2;                         // K slices per pipeline stage (K = 128)
-constexpr int kStagesRaw = 8;                    // 4-bit stages in shared memory (~70 KB in flight)
 constexpr int kDqSets = 2;                       // dequant quartets; quartet q takes the stages kk % 2 == q
 constexpr int kRawBytes = kSubs * kFp4BlockBytes;          // 8704 B per stage
 constexpr int kRawPer = 2;                       // stages per raw bulk copy (one per quartet)
-constexpr int kRawSlots = kStagesRaw / kRawPer;  // raw ring slots of kRawPer stages
 constexpr int kRawSlotBytes = kRawPer * kRawBytes;
 constexpr int kACols = kSubs * kSubK / 2;        // 64 columns (fp16 pairs) per A stage
 constexpr int kTmemCols = 512;                   // accumulators + A stages
@@ -43,19 +41,27 @@ constexpr int kEpiStageBytes = 16 * 32 * 2;     // per epilogue warp: 16 columns
 
 // Geometry for segments of at most kN rows (128, or 64 for steps of at most 64 tokens): the two
 // accumulators take 2 kN TMEM columns and the rest of the 512 hold A stages, so small segments
-// get a deeper ring (6 stages instead of 4) with smaller activation stages.
+// get a deeper A ring (6 stages instead of 4).  With 128-row segments the activation (B) stages
+// have their own, deeper ring in shared memory: a B stage can be requested before the A slot of
+// its stage is free, so the gathered rows' L2 latency hides behind several stages of MMAs.
 template <int kN>
 struct Geo {
-  static constexpr int kStages = (kTmemCols - 2 * kN) / kACols;  // A (TMEM) + B (smem) stages, one ring
+  static constexpr int kStages = (kTmemCols - 2 * kN) / kACols;  // A stages (TMEM)
+  // 128-row activation stages get their own ring (5 stages); 64-row ones share the A ring's
+  // barriers (the second pair of barrier operations per stage costs more than it hides there)
+  static constexpr bool kSplitB = kN > 64;
+  static constexpr int kBStages = kSplitB ? 5 : kStages;         // B stages (shared memory)
+  static constexpr int kStagesRaw = kN > 64 ? 6 : 8;             // 4-bit stages in shared memory
+  static constexpr int kRawSlots = kStagesRaw / kRawPer;         // raw ring slots of kRawPer stages
   static constexpr int kSubBytes = kN * kSubK * 2;                // one K slice of up to kN rows
   static constexpr int kBBytes = kSubs * kSubBytes;
   static constexpr int kAccCols = kN;
   static constexpr int kAStart = 2 * kAccCols;                   // A stages after the accumulators
-  static constexpr int kGatherPerSlot = kN > 64 ? 2 : 1;         // gate/up B producers per slot
-  static constexpr int kGatherWarps = kGatherPerSlot * kStages;
+  static constexpr int kGatherPerSlot = kN > 64 ? 2 : 1;         // gate/up B producers per B slot
+  static constexpr int kGatherWarps = kGatherPerSlot * kBStages;
   static constexpr int kTokBytes = kGatherWarps * kN * 4;         // per gather warp: token per row
   static constexpr int kSmemBytes =
-      kStages * kBBytes + kStagesRaw * kRawBytes + 1024 + 1024 + kTokBytes + 4 * kEpiStageBytes;
+      kBStages * kBBytes + kStagesRaw * kRawBytes + 1024 + 1024 + kTokBytes + 4 * kEpiStageBytes;
   static constexpr int threads(bool gate_up) { return 32 * (gate_up ? 6 + kGatherWarps + 8 : 7 + 8); }
   static_assert(kRawPer == kDqSets && kStagesRaw % kRawPer == 0, "one stage of each raw copy per quartet");
   static_assert(kAStart + kStages * kACols <= kTmemCols, "TMEM columns");
@@ -192,10 +198,12 @@ MOE_DEVICE bool mbar_test_u32(uint32_t bar, uint32_t parity) {
 //                        unit, p counting pairs): one bulk copy per pair (a fixed cost per bulk
 //                        operation makes fewer, larger copies stream faster); quartet q reads
 //                        stage 2p' + q, and both quartets free the slot
-//   A/B[g % kStages]     dequantised weights in TMEM + activation rows in shared memory; full when
-//                        the quartet (4 arrivals) and the B producer (the slot's gather warp, or
-//                        one arrive.expect_tx for TMA) are done, empty when the MMAs reading it finish.
-// The MMA warp thus waits on one barrier and commits once per 128 K.
+//   A[g % kStages]       dequantised weights in TMEM: full when the quartet (4 arrivals) is done,
+//                        empty when the MMAs reading it finish
+//   B[g % kBStages]      activation rows in shared memory: full when the slot's gather warps (or
+//                        one arrive.expect_tx for TMA) are done, empty when the MMAs finish.
+//                        Without kSplitB the B slots are the A slots' and share their barriers.
+// The MMA lane tests one or two barriers and commits once or twice per 128 K.
 template <bool kGateUp, int kN>
 __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
     fp4_ffn_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
@@ -207,16 +215,22 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
   constexpr int kGatherPerSlot = Geo<kN>::kGatherPerSlot;
   constexpr int kGatherWarps = Geo<kN>::kGatherWarps;
   constexpr int kTokBytes = Geo<kN>::kTokBytes;
+  constexpr int kBStages = Geo<kN>::kBStages;
+  constexpr bool kSplitB = Geo<kN>::kSplitB;
+  constexpr int kStagesRaw = Geo<kN>::kStagesRaw;
+  constexpr int kRawSlots = Geo<kN>::kRawSlots;
   constexpr int kDqWarp = kGateUp ? 6 + kGatherWarps : 7;  // first dequant warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ring_b = smem;                                  // kStages x 32 KB, 1024-aligned
-  uint8_t* ring_raw = smem + kStages * kBBytes;            // kStagesRaw x 8704 B
+  uint8_t* ring_b = smem;                                  // kBStages x kBBytes, 1024-aligned
+  uint8_t* ring_raw = smem + kBStages * kBBytes;           // kStagesRaw x 8704 B
   uint64_t* raw_full = reinterpret_cast<uint64_t*>(ring_raw + kStagesRaw * kRawBytes);
-  uint64_t* raw_empty = raw_full + kStagesRaw;
-  uint64_t* full = raw_empty + kStagesRaw;
+  uint64_t* raw_empty = raw_full + kRawSlots;
+  uint64_t* full = raw_empty + kRawSlots;
   uint64_t* empty = full + kStages;
-  uint64_t* acc_full = empty + kStages;
+  uint64_t* b_full = kSplitB ? empty + kStages : full;
+  uint64_t* b_empty = kSplitB ? b_full + kBStages : empty;
+  uint64_t* acc_full = empty + kStages + 2 * kBStages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -230,10 +244,16 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
       mbar_init(&raw_full[s], 1);
       mbar_init(&raw_empty[s], 4 * kDqSets);
     }
+    const int b_arrivals = kGateUp ? kGatherPerSlot : 1;  // the slot's gather warps, or one TMA arrival
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 4 + (kGateUp ? kGatherPerSlot : 1));  // dequant quartet + B producer(s)
+      mbar_init(&full[s], 4 + (kSplitB ? 0 : b_arrivals));  // the dequant quartet (+ the B producers)
       mbar_init(&empty[s], 1);
     }
+    if (kSplitB)
+      for (int s = 0; s < kBStages; ++s) {
+        mbar_init(&b_full[s], b_arrivals);
+        mbar_init(&b_empty[s], 1);
+      }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], 4);
@@ -287,8 +307,9 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
     const uint32_t a_base = tmem + kAStart;
     const uint64_t b_base = smem_desc_sw128(smem_u32(ring_b));
     const uint32_t full_u32 = smem_u32(full), empty_u32 = smem_u32(empty);
+    const uint32_t bfull_u32 = smem_u32(b_full), bempty_u32 = smem_u32(b_empty);
     uint32_t g = 0, j = 0;
-    bool ok = true, ready = false;  // ready: full[g % kStages] already seen complete for stage g
+    bool ok = true, ready = false;  // ready: stage g's A and B barriers already seen complete
     for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++j) {
       const Unit un = decode_unit(u, a.segs, tiles);
       const uint32_t N = static_cast<uint32_t>(pad16(un.rows));
@@ -298,24 +319,30 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
       const uint32_t d_tmem = tmem + buf * kAccCols;
       const uint32_t idesc = idesc_f16_f32(BM, N);
       // The elected lane issues a run of consecutive stages that are already full (testing each
-      // next barrier itself), so the warp-wide bookkeeping is paid once per run, not per stage.
+      // next pair of barriers itself), so the warp-wide bookkeeping is paid once per run.
       for (int kk = 0; kk < nst;) {
-        const int s = g % kStages;
-        if (!ready && !(ok = mbar_wait_warp(&full[s], (g / kStages) & 1u, abort_flag, a.err))) break;
+        const uint32_t s = g % kStages, sb = g % kBStages;
+        if (!ready && !(ok = mbar_wait_warp(&full[s], (g / kStages) & 1u, abort_flag, a.err) &&
+                             (!kSplitB || mbar_wait_warp(&b_full[sb], (g / kBStages) & 1u, abort_flag, a.err))))
+          break;
         tc_fence_after();
         int issued = 0;
         if (elect_one()) {
-          // slot and phase advance incrementally: the lane's dependency chain per stage is the
-          // address arithmetic, the MMA block, the commit and the next barrier's test
-          uint32_t ss = static_cast<uint32_t>(s), ph = (g / kStages) & 1u;
+          // slots and phases advance incrementally: the lane's dependency chain per stage is the
+          // address arithmetic, the MMA block, the commits and the next barriers' tests
+          uint32_t ss = s, ph = (g / kStages) & 1u, sbb = sb, phb = (g / kBStages) & 1u;
           int k2 = kk;
           while (true) {
-            mma_stage_ts<(kSubBytes >> 4)>(d_tmem, a_base + ss * kACols, b_base + ss * (kBBytes >> 4), idesc,
+            mma_stage_ts<(kSubBytes >> 4)>(d_tmem, a_base + ss * kACols, b_base + sbb * (kBBytes >> 4), idesc,
                                            static_cast<uint32_t>(k2), nsub - kSubs * k2 >= kSubs);
             mma_commit_u32(empty_u32 + 8 * ss);
+            if (kSplitB) mma_commit_u32(bempty_u32 + 8 * sbb);
             ++k2, ++issued;
             if (++ss == static_cast<uint32_t>(kStages)) ss = 0, ph ^= 1u;
-            if (k2 >= nst || !mbar_test_u32(full_u32 + 8 * ss, ph)) break;
+            if (++sbb == static_cast<uint32_t>(kBStages)) sbb = 0, phb ^= 1u;
+            if (k2 >= nst || !mbar_test_u32(full_u32 + 8 * ss, ph) ||
+                (kSplitB && !mbar_test_u32(bfull_u32 + 8 * sbb, phb)))
+              break;
             tc_fence_after();
           }
         }
@@ -323,7 +350,8 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
         kk += issued;
         g += static_cast<uint32_t>(issued);
         // probe the next stage (possibly the next unit's first) now, use the answer next iteration
-        ready = __all_sync(0xffffffffu, mbar_test(&full[g % kStages], (g / kStages) & 1u));
+        ready = __all_sync(0xffffffffu, mbar_test(&full[g % kStages], (g / kStages) & 1u) &&
+                                            (!kSplitB || mbar_test(&b_full[g % kBStages], (g / kBStages) & 1u)));
       }
       if (!ok) break;
       if (elect_one()) mma_commit(&acc_full[buf]);
@@ -471,14 +499,14 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
         const Unit un = decode_unit(u, a.segs, tiles);
         const int nbox = (pad16(un.rows) + 31) / 32;
         for (int kk = 0; kk < nst; ++kk, ++g) {
-          const int s = g % kStages;
+          const int sb = g % kBStages;
           const int subs = min(kSubs, nsub - kSubs * kk);
-          if (!(ok = mbar_wait_warp(&empty[s], ((g / kStages) & 1u) ^ 1u, abort_flag, a.err))) break;
+          if (!(ok = mbar_wait_warp(&b_empty[sb], ((g / kBStages) & 1u) ^ 1u, abort_flag, a.err))) break;
           if (elect_one()) {
-            mbar_arrive_expect_tx(&full[s], subs * nbox * 32 * kSubK * 2);
+            mbar_arrive_expect_tx(&b_full[sb], subs * nbox * 32 * kSubK * 2);
             for (int j2 = 0; j2 < subs; ++j2)
               for (int i = 0; i < nbox; ++i)
-                tma_load_2d(ring_b + s * kBBytes + j2 * kSubBytes + i * 32 * kSubK * 2, &maps.h, &full[s],
+                tma_load_2d(ring_b + sb * kBBytes + j2 * kSubBytes + i * 32 * kSubK * 2, &maps.h, &b_full[sb],
                             (kSubs * kk + j2) * kSubK, un.row_start + 32 * i, pol_act);
           }
           __syncwarp();
@@ -487,12 +515,12 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
     }
   } else {
     // ---------------- B producer (gate/up): fp16 token rows gathered with cp.async ----------
-    // Gather warps w and w + kStages own ring slot w: they fill every stage g with
-    // g % kStages == w (each half of the rows), wait for their own copies, fence them for the
-    // tensor core and arrive.  All kStages slots can be in flight at once, and no copy waits
+    // Gather warps w and w + kBStages own B slot w: they fill every stage g with
+    // g % kBStages == w (each half of the rows), wait for their own copies, fence them for the
+    // tensor core and arrive.  All kBStages slots can be in flight at once, and no copy waits
     // behind the issue of a later stage.
     const int gw = warp - 6;
-    const int slot = gw % kStages, half = gw / kStages;
+    const int slot = gw % kBStages, half = gw / kBStages;
     int32_t* tok = tok_tab + kN * gw;           // token row of each row of this warp's unit
     const int ch = lane & 7;                    // 16-byte chunk
     const int rs = (lane >> 3) + 4 * half;      // first row; rows rs + 4 kGatherPerSlot i
@@ -503,7 +531,7 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
       const Unit un = decode_unit(u, a.segs, tiles);
       bool have_tok = false;
       for (int kk = 0; kk < nst; ++kk, ++g) {
-        const int s = g % kStages;
+        const int s = g % kBStages;
         if (s != slot) continue;
         if (!have_tok) {
           for (int n = lane; n < un.rows; n += 32) tok[n] = a.perm[un.row_start + n] / a.k;
@@ -511,7 +539,7 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
           have_tok = true;
         }
         const int subs = min(kSubs, nsub - kSubs * kk);
-        if (!(ok = mbar_wait_warp(&empty[s], ((g / kStages) & 1u) ^ 1u, abort_flag, a.err))) break;
+        if (!(ok = mbar_wait_warp(&b_empty[s], ((g / kBStages) & 1u) ^ 1u, abort_flag, a.err))) break;
         const uint32_t sb = smem_u32(ring_b + s * kBBytes);
         const int k0 = kSubs * kk * kSubK + ch * 8;
         for (int n = rs; n < un.rows; n += 4 * kGatherPerSlot) {
@@ -524,7 +552,7 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
         cp_async_wait<0>();
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&full[s]);
+        if (lane == 0) mbar_arrive(&b_full[s]);
       }
     }
   }
