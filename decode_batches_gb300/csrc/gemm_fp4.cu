@@ -62,7 +62,8 @@ struct Geo {
   static constexpr int kTokBytes = kGatherWarps * kN * 4;         // per gather warp: token per row
   static constexpr int kSmemBytes =
       kBStages * kBBytes + kStagesRaw * kRawBytes + 1024 + 1024 + kTokBytes + 4 * kEpiStageBytes;
-  static constexpr int threads(bool gate_up) { return 32 * (gate_up ? 6 + kGatherWarps + 8 : 7 + 8); }
+  static constexpr int kBProducers = 4;                           // down: warps issuing the TMA loads of h
+  static constexpr int threads(bool gate_up) { return 32 * (gate_up ? 6 + kGatherWarps + 8 : 6 + kBProducers + 8); }
   static_assert(kRawPer == kDqSets && kStagesRaw % kRawPer == 0, "one stage of each raw copy per quartet");
   static_assert(kAStart + kStages * kACols <= kTmemCols, "TMEM columns");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -219,7 +220,8 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
   constexpr bool kSplitB = Geo<kN>::kSplitB;
   constexpr int kStagesRaw = Geo<kN>::kStagesRaw;
   constexpr int kRawSlots = Geo<kN>::kRawSlots;
-  constexpr int kDqWarp = kGateUp ? 6 + kGatherWarps : 7;  // first dequant warp
+  constexpr int kBProducers = Geo<kN>::kBProducers;
+  constexpr int kDqWarp = kGateUp ? 6 + kGatherWarps : 6 + kBProducers;  // first dequant warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring_b = smem;                                  // kBStages x kBBytes, 1024-aligned
@@ -491,7 +493,10 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
     }
   } else if (!kGateUp) {
     // ---------------- B producer (down): rows of h by TMA ----------------
-    if (warp == 6) {
+    // kBProducers warps take turns (stage g: warp 6 + g % kBProducers): each stage needs up to
+    // 2 x 4 box loads, and one issuing thread would pace the whole pipeline.
+    {
+      const int bp = warp - 6;
       const uint64_t pol_act = l2_policy_evict_last();
       uint32_t g = 0;
       bool ok = true;
@@ -499,6 +504,7 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
         const Unit un = decode_unit(u, a.segs, tiles);
         const int nbox = (pad16(un.rows) + 31) / 32;
         for (int kk = 0; kk < nst; ++kk, ++g) {
+          if (static_cast<int>(g % kBProducers) != bp) continue;
           const int sb = g % kBStages;
           const int subs = min(kSubs, nsub - kSubs * kk);
           if (!(ok = mbar_wait_warp(&b_empty[sb], ((g / kBStages) & 1u) ^ 1u, abort_flag, a.err))) break;
