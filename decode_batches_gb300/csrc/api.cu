@@ -691,9 +691,11 @@ static moe_status launch_shared_gate_up_beside(moe_plan* p, const uint16_t* x, i
 // Expert FFN over grouped rows; y/y_s outputs, h/h_s in the workspace.  For the tensor-core
 // path `segs`/`n_segs` must already describe the routed segments.  shared_forked: the shared
 // expert was launched on the side stream (launch_shared_gate_up_beside); unless its down
-// projection went there too, st joins the side stream before launching it.
+// projection went there too, st joins the side stream before launching it.  x16_ready: the
+// routing already wrote the 4-bit path's fp16 copy of x.
 static moe_status run_experts(moe_plan* p, const uint16_t* x, int T, const int32_t* offsets, const int32_t* perm,
-                              uint16_t* y, uint16_t* y_s, cudaStream_t st, bool shared_forked = false) {
+                              uint16_t* y, uint16_t* y_s, cudaStream_t st, bool shared_forked = false,
+                              bool x16_ready = false) {
   if (use_tc(p)) {
     if (!p->maps_weights || !p->maps_ws) return fail(MOE_ERR_NOT_READY, "tensor maps not built");
     TcArgs a = tc_args(p, x, T, perm, y, y_s);
@@ -701,7 +703,8 @@ static moe_status run_experts(moe_plan* p, const uint16_t* x, int T, const int32
       // routed experts on the 4-bit kernels (fp16 activations), shared experts on the 16-bit
       // kernels restricted to their units
       uint16_t* x16 = ws_ptr<uint16_t>(p, p->L.x16);
-      LAUNCH(p, "x_to_f16", st, launch_x_to_f16(x, x16, static_cast<size_t>(T) * p->d, p->err, st));
+      if (!x16_ready)
+        LAUNCH(p, "x_to_f16", st, launch_x_to_f16(x, x16, static_cast<size_t>(T) * p->d, p->err, st));
       LAUNCH(p, "fp4_gateup", st, launch_fp4_gateup(&p->maps, a, p->num_sms, st));
       if (p->n_shared > 0 && !shared_forked) {
         const TcArgs sh = shared_args(p, a, T, true);
@@ -760,13 +763,13 @@ static int router_nsplit(const moe_plan* p, int T) {
 
 // Router logits + top-k (+ masks).
 static moe_status route_step(moe_plan* p, const uint16_t* x, int T, float* logits_out, int32_t* ids, float* gates,
-                             uint32_t* masks, cudaStream_t st) {
+                             uint32_t* masks, cudaStream_t st, const XConv& xc = XConv{}) {
   const float* parts = nullptr;
   const float* bias = nullptr;
   int ns = 1;
   moe_status s = router_step(p, x, T, &parts, &ns, &bias, st);
   if (s != MOE_OK) return s;
-  LAUNCH(p, "topk", st, launch_topk(parts, ns, bias, logits_out, T, p->E, p->k, ids, gates, masks, p->err, st));
+  LAUNCH(p, "topk", st, launch_topk(parts, ns, bias, logits_out, T, p->E, p->k, ids, gates, masks, p->err, st, xc));
   return MOE_OK;
 }
 
@@ -803,13 +806,22 @@ extern "C" moe_status moe_layer_forward(moe_plan* p, const void* x, int T, int n
       if (armed) cudaStreamWaitEvent(st, ev, 0);
     }
   } join{st, p->ev_join, forked};
+  // At T <= 64 the 4-bit path's fp16 copy of x is made on the side by the one routing launch
+  // that precedes the expert kernels (every thread of its grid takes a share); above, the top-k
+  // kernel would carry T·d conversions on few threads, so x_to_f16 keeps its own launch.
+  XConv xc;
+  if (tc && p->wdtype == MOE_W_MXFP4) {
+    xc.x = xb;
+    xc.x16 = ws_ptr<uint16_t>(p, p->L.x16);
+    xc.n8 = static_cast<size_t>(T) * p->d / 8;
+  }
   if (router_nsplit(p, T) == router_small_splits(p->d) && !(p->router_tc && T > kRouterTcMinT) &&
       router_route_tiny_ok(T, p->E, p->d, p->k)) {
     // tiny step: router, top-k and grouping in one launch
     LAUNCH(p, "router_route", st,
            launch_router_route_tiny(xb, p->w_router, p->b_router, T, p->E, p->d, ws_ptr<float>(p, p->L.parts), p->k,
                                     ids, gates, counts, offsets, perm, inv, segs, ws_ptr<int32_t>(p, p->L.n_segs),
-                                    p->L.max_segs, p->err + 1, p->err, st));
+                                    p->L.max_segs, p->err + 1, p->err, st, xc));
   } else if (route_small_ok(T, p->E, p->k, router_nsplit(p, T))) {
     // small step: the whole routing and grouping in one block after the router
     const float* parts = nullptr;
@@ -819,8 +831,9 @@ extern "C" moe_status moe_layer_forward(moe_plan* p, const void* x, int T, int n
     if (s != MOE_OK) return s;
     LAUNCH(p, "route_small", st,
            launch_route_small(parts, ns, bias, T, p->E, p->k, ids, gates, counts, offsets, perm, inv, segs,
-                              ws_ptr<int32_t>(p, p->L.n_segs), p->L.max_segs, p->err + 1, p->err, st));
+                              ws_ptr<int32_t>(p, p->L.n_segs), p->L.max_segs, p->err + 1, p->err, st, xc));
   } else {
+    xc = XConv{};
     s = route_step(p, xb, T, nullptr, ids, gates, masks, st);
     if (s != MOE_OK) return s;
     LAUNCH(p, "chunk_scan", st, launch_chunk_scan(masks, n_chunks, p->E, chunk_base, counts, st));
@@ -828,7 +841,7 @@ extern "C" moe_status moe_layer_forward(moe_plan* p, const void* x, int T, int n
            launch_scatter(ids, masks, chunk_base, counts, T, p->E, p->k, perm, inv, offsets, segs,
                           ws_ptr<int32_t>(p, p->L.n_segs), p->L.max_segs, p->err, st));
   }
-  s = run_experts(p, xb, T, offsets, perm, y, y_s, st, forked);
+  s = run_experts(p, xb, T, offsets, perm, y, y_s, st, forked, xc.x16 != nullptr);
   if (s != MOE_OK) return s;
   if (forked && kSharedDownBeside) MOE_CUDA_TRY(cudaStreamWaitEvent(st, p->ev_join, 0));
   join.armed = false;  // joined (before the shared down projection or here)

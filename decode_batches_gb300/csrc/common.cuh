@@ -15,6 +15,7 @@
 #include <utility>
 
 #include "../../include/moe.h"
+#include "kernels.h"
 
 #define MOE_DEVICE __device__ __forceinline__
 
@@ -328,6 +329,32 @@ MOE_DEVICE void bf16x8_to_f32(const uint4& v, float (&o)[8]) {
 // fp16 storage of the layer's intermediates (hidden vector h, expert outputs y).
 constexpr float kF16Max = 65504.0f;
 MOE_DEVICE uint16_t f32_to_f16_bits_rn(float f) { return __half_as_ushort(__float2half_rn(f)); }
+
+// Grid-stride part of an XConv: values outside the fp16 range clamp and flag MOE_DEVERR_RANGE.
+MOE_DEVICE void convert_x16(const XConv& c, uint32_t* err) {
+  if (!c.x16) return;
+  bool sat = false;
+  const size_t stride = static_cast<size_t>(gridDim.x) * gridDim.y * gridDim.z * blockDim.x;
+  const size_t b = (static_cast<size_t>(blockIdx.z) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+  for (size_t i = b * blockDim.x + threadIdx.x; i < c.n8; i += stride) {
+    const uint4 v = reinterpret_cast<const uint4*>(c.x)[i];
+    float f[8];
+    bf16x8_to_f32(v, f);
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float lo = f[2 * q], hi = f[2 * q + 1];
+      if (!(fabsf(lo) <= kF16Max) || !(fabsf(hi) <= kF16Max)) {
+        sat = true;
+        lo = fminf(fmaxf(lo, -kF16Max), kF16Max);
+        hi = fminf(fmaxf(hi, -kF16Max), kF16Max);
+      }
+      o[q] = static_cast<uint32_t>(f32_to_f16_bits_rn(lo)) | (static_cast<uint32_t>(f32_to_f16_bits_rn(hi)) << 16);
+    }
+    reinterpret_cast<uint4*>(c.x16)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (sat) set_error(err, MOE_DEVERR_RANGE);
+}
 MOE_DEVICE float f16_bits_to_f32(uint16_t b) { return __half2float(__ushort_as_half(b)); }
 
 MOE_DEVICE void f16x8_to_f32(const uint4& v, float (&o)[8]) {

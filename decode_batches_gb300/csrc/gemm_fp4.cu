@@ -607,26 +607,9 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const uint16_t* __restric
                                                        size_t n8, uint32_t* err) {
   pdl_trigger();
   pdl_wait();
-  bool sat = false;
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const uint4 v = reinterpret_cast<const uint4*>(x)[i];
-    float f[8];
-    bf16x8_to_f32(v, f);
-    uint32_t o[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float lo = f[2 * q], hi = f[2 * q + 1];
-      if (!(fabsf(lo) <= kF16Max) || !(fabsf(hi) <= kF16Max)) {
-        sat = true;
-        lo = fminf(fmaxf(lo, -kF16Max), kF16Max);
-        hi = fminf(fmaxf(hi, -kF16Max), kF16Max);
-      }
-      o[q] = static_cast<uint32_t>(f32_to_f16_bits_rn(lo)) | (static_cast<uint32_t>(f32_to_f16_bits_rn(hi)) << 16);
-    }
-    reinterpret_cast<uint4*>(x16)[i] = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-  if (sat) set_error(err, MOE_DEVERR_RANGE);
+  XConv c;
+  c.x = x, c.x16 = x16, c.n8 = n8;
+  convert_x16(c, err);
 }
 
 cudaError_t launch_x_to_f16(const uint16_t* x, uint16_t* x16, size_t n, uint32_t* err, cudaStream_t st) {

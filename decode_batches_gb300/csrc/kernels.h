@@ -12,6 +12,15 @@ namespace moe {
 // Sets the thread's moe_last_error() message and returns s (api.cu).
 moe_status fail_message(moe_status s, const char* msg);
 
+// A conversion x (bf16) -> x16 (fp16) of n8 * 8 elements that a kernel performs on the side with
+// every thread of its grid (the 4-bit path's activation copy; convert_x16 in common.cuh);
+// x16 == nullptr: none.
+struct XConv {
+  const uint16_t* x = nullptr;
+  uint16_t* x16 = nullptr;
+  size_t n8 = 0;
+};
+
 // Tokens per chunk of the grouping step: one 32-bit mask word per (chunk, expert).
 constexpr int kChunk = 32;
 // Largest number of rows one tensor-core unit handles (the MMA's N).
@@ -36,8 +45,10 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* w_router, const
 // Top-k + softmax gates per token.  The logits are sum_s parts[s][T][E] (+ bias[e]) and are
 // written to logits_out if given.  If masks != nullptr also writes the per-chunk expert masks,
 // expert-major: bit t of masks[e * n_chunks + c] <=> token c*32+t chose e.
+// xc: an x -> fp16 conversion the launch performs on the side (none by default).
 cudaError_t launch_topk(const float* parts, int nsplit, const float* bias, float* logits_out, int T, int E, int k,
-                        int32_t* ids, float* gates, uint32_t* masks, uint32_t* err, cudaStream_t st);
+                        int32_t* ids, float* gates, uint32_t* masks, uint32_t* err, cudaStream_t st,
+                        const XConv& xc = XConv{});
 
 // ---- tensor-core router (router_tc.cu) --------------------------------------------------------
 // parts[s][T][E] = x[T][k-range s] . W_r[E][k-range s]^T with W_r split into three bf16 pieces
@@ -58,12 +69,14 @@ bool router_route_tiny_ok(int T, int E, int d, int k);
 cudaError_t launch_router_route_tiny(const uint16_t* x, const float* w_router, const float* bias, int T, int E, int d,
                                      float* parts, int k, int32_t* ids, float* gates, int32_t* counts,
                                      int32_t* offsets, int32_t* perm, int32_t* inv, Seg* segs, int32_t* n_segs,
-                                     int max_segs, uint32_t* done, uint32_t* err, cudaStream_t st);
+                                     int max_segs, uint32_t* done, uint32_t* err, cudaStream_t st,
+                                     const XConv& xc = XConv{});
 
 // `done`: a device counter that is 0 between launches (the last block resets it).
 cudaError_t launch_route_small(const float* parts, int nsplit, const float* bias, int T, int E, int k, int32_t* ids,
                                float* gates, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, Seg* segs,
-                               int32_t* n_segs, int max_segs, uint32_t* done, uint32_t* err, cudaStream_t st);
+                               int32_t* n_segs, int max_segs, uint32_t* done, uint32_t* err, cudaStream_t st,
+                               const XConv& xc = XConv{});
 cudaError_t launch_router_tc(const CUtensorMap* w3, const uint16_t* x, int T, int E, int d, int nsplit, float* parts,
                              uint32_t* err, cudaStream_t st);
 cudaError_t launch_split_router(const float* w, uint16_t* w3, size_t n, cudaStream_t st);

@@ -369,10 +369,12 @@ __global__ void __launch_bounds__(topk_threads<PL>()) topk_kernel(const float* _
                                                                   float* __restrict__ logits_out, int T, int E, int k,
                                                                   int n_chunks, int32_t* __restrict__ ids,
                                                                   float* __restrict__ gates,
-                                                                  uint32_t* __restrict__ masks, uint32_t* err) {
+                                                                  uint32_t* __restrict__ masks, uint32_t* err,
+                                                                  const XConv xc) {
   extern __shared__ uint32_t smask[];  // [E]
   pdl_trigger();
   pdl_wait();
+  convert_x16(xc, err);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
   if (masks)
@@ -393,17 +395,18 @@ __global__ void __launch_bounds__(topk_threads<PL>()) topk_kernel(const float* _
 template <int PL>
 static cudaError_t launch_topk_pl(const float* parts, int nsplit, const float* bias, float* logits_out, int T, int E,
                                   int k, int n_chunks, int32_t* ids, float* gates, uint32_t* masks, uint32_t* err,
-                                  cudaStream_t st) {
+                                  const XConv& xc, cudaStream_t st) {
   return launch_pdl(topk_kernel<PL>, dim3(n_chunks), dim3(topk_threads<PL>()), masks ? E * sizeof(uint32_t) : 0, st,
-                    parts, nsplit, bias, logits_out, T, E, k, n_chunks, ids, gates, masks, err);
+                    parts, nsplit, bias, logits_out, T, E, k, n_chunks, ids, gates, masks, err, xc);
 }
 
 cudaError_t launch_topk(const float* parts, int nsplit, const float* bias, float* logits_out, int T, int E, int k,
-                        int32_t* ids, float* gates, uint32_t* masks, uint32_t* err, cudaStream_t st) {
+                        int32_t* ids, float* gates, uint32_t* masks, uint32_t* err, cudaStream_t st, const XConv& xc) {
   if (T <= 0) return cudaSuccess;
   const int n_chunks = (T + kChunk - 1) / kChunk;
   const int pl = (E + 31) / 32;
-#define MOE_TOPK(PLV) launch_topk_pl<PLV>(parts, nsplit, bias, logits_out, T, E, k, n_chunks, ids, gates, masks, err, st)
+#define MOE_TOPK(PLV) \
+  launch_topk_pl<PLV>(parts, nsplit, bias, logits_out, T, E, k, n_chunks, ids, gates, masks, err, xc, st)
   if (pl <= 1) return MOE_TOPK(1);
   if (pl <= 2) return MOE_TOPK(2);
   if (pl <= 4) return MOE_TOPK(4);
@@ -750,11 +753,12 @@ __global__ void __launch_bounds__(kRgThreads) route_group_kernel(
     const float* __restrict__ parts, int nsplit, const float* __restrict__ bias, int T, int E, int k,
     int32_t* __restrict__ ids, float* __restrict__ gates, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int32_t* __restrict__ perm, int32_t* __restrict__ inv, Seg* segs, int32_t* n_segs, int max_segs,
-    uint32_t* done, uint32_t* err) {
+    uint32_t* done, uint32_t* err, const XConv xc) {
   extern __shared__ uint32_t sm[];
   __shared__ int s_last;
   pdl_trigger();
   pdl_wait();
+  convert_x16(xc, err);
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x;
   {
@@ -816,11 +820,13 @@ __global__ void __launch_bounds__(kRgThreads) router_route_tiny_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias, int T, int E,
     int d, float* __restrict__ parts, int k, int32_t* __restrict__ ids, float* __restrict__ gates,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
-    int32_t* __restrict__ inv, Seg* segs, int32_t* n_segs, int max_segs, uint32_t* done, uint32_t* err) {
+    int32_t* __restrict__ inv, Seg* segs, int32_t* n_segs, int max_segs, uint32_t* done, uint32_t* err,
+    const XConv xc) {
   extern __shared__ __align__(16) uint32_t sm[];
   __shared__ int s_last;
   pdl_trigger();
   pdl_wait();
+  convert_x16(xc, err);
   router_parts_block<8>(x, wr, T, E, d, parts, reinterpret_cast<uint16_t*>(sm));
   __threadfence();
   __syncthreads();
@@ -874,24 +880,25 @@ template <int PL>
 static cudaError_t launch_rrt_pl(const uint16_t* x, const float* wr, const float* bias, int T, int E, int d,
                                  float* parts, int k, int32_t* ids, float* gates, int32_t* counts, int32_t* offsets,
                                  int32_t* perm, int32_t* inv, Seg* segs, int32_t* n_segs, int max_segs, uint32_t* done,
-                                 uint32_t* err, cudaStream_t st) {
+                                 uint32_t* err, const XConv& xc, cudaStream_t st) {
   const size_t xs_bytes = 8 * kRouterKS * 2;
   const size_t g_bytes = route_small_smem(T, E, k);
   dim3 grid((E + 7) / 8, router_small_splits(d));
   return launch_pdl(router_route_tiny_kernel<PL>, grid, dim3(kRgThreads), xs_bytes > g_bytes ? xs_bytes : g_bytes, st,
                     x, wr, bias, T, E, d, parts, k, ids, gates, counts, offsets, perm, inv, segs, n_segs, max_segs,
-                    done, err);
+                    done, err, xc);
 }
 
 cudaError_t launch_router_route_tiny(const uint16_t* x, const float* w_router, const float* bias, int T, int E, int d,
                                      float* parts, int k, int32_t* ids, float* gates, int32_t* counts,
                                      int32_t* offsets, int32_t* perm, int32_t* inv, Seg* segs, int32_t* n_segs,
-                                     int max_segs, uint32_t* done, uint32_t* err, cudaStream_t st) {
+                                     int max_segs, uint32_t* done, uint32_t* err, cudaStream_t st,
+                                     const XConv& xc) {
   if (!router_route_tiny_ok(T, E, d, k)) return cudaErrorInvalidValue;
   const int pl = (E + 31) / 32;
 #define MOE_RRT(PLV)                                                                                            \
   launch_rrt_pl<PLV>(x, w_router, bias, T, E, d, parts, k, ids, gates, counts, offsets, perm, inv, segs, n_segs, \
-                     max_segs, done, err, st)
+                     max_segs, done, err, xc, st)
   if (pl <= 1) return MOE_RRT(1);
   if (pl <= 2) return MOE_RRT(2);
   if (pl <= 4) return MOE_RRT(4);
@@ -911,19 +918,20 @@ template <int PL>
 static cudaError_t launch_route_small_pl(const float* parts, int nsplit, const float* bias, int T, int E, int k,
                                          int32_t* ids, float* gates, int32_t* counts, int32_t* offsets, int32_t* perm,
                                          int32_t* inv, Seg* segs, int32_t* n_segs, int max_segs, uint32_t* done,
-                                         uint32_t* err, cudaStream_t st) {
+                                         uint32_t* err, const XConv& xc, cudaStream_t st) {
   return launch_pdl(route_group_kernel<PL>, dim3(T), dim3(kRgThreads), route_small_smem(T, E, k), st, parts, nsplit,
-                    bias, T, E, k, ids, gates, counts, offsets, perm, inv, segs, n_segs, max_segs, done, err);
+                    bias, T, E, k, ids, gates, counts, offsets, perm, inv, segs, n_segs, max_segs, done, err, xc);
 }
 
 cudaError_t launch_route_small(const float* parts, int nsplit, const float* bias, int T, int E, int k, int32_t* ids,
                                float* gates, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, Seg* segs,
-                               int32_t* n_segs, int max_segs, uint32_t* done, uint32_t* err, cudaStream_t st) {
+                               int32_t* n_segs, int max_segs, uint32_t* done, uint32_t* err, cudaStream_t st,
+                               const XConv& xc) {
   if (!route_small_ok(T, E, k, nsplit)) return cudaErrorInvalidValue;
   const int pl = (E + 31) / 32;
 #define MOE_RS(PLV)                                                                                             \
   launch_route_small_pl<PLV>(parts, nsplit, bias, T, E, k, ids, gates, counts, offsets, perm, inv, segs, n_segs, \
-                             max_segs, done, err, st)
+                             max_segs, done, err, xc, st)
   if (pl <= 1) return MOE_RS(1);
   if (pl <= 2) return MOE_RS(2);
   if (pl <= 4) return MOE_RS(4);
