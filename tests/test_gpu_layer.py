@@ -144,9 +144,11 @@ def test_paths_agree():
     assert np.all(np.abs(a - b) <= 2 * _bf16_ulp(np.maximum(np.abs(a), np.abs(b))) + 1e-3 * rms)
 
 
-@pytest.mark.parametrize("T", [1, 15, 16, 17, 255, 256, 257, 1000])
+@pytest.mark.parametrize("T", [1, 8, 9, 15, 16, 17, 64, 65, 255, 256, 257, 1000])
 def test_forward_ragged_sizes(T):
-    """T around the 16-column MMA step, the 32-token chunk and the 256-row segment limit."""
+    """T around the 16-column MMA step, the 32-token chunk, the 256-row segment limit and the
+    routing front ends' switch points (one launch up to 8 tokens, tensor-core router above 16,
+    one grouping block up to 64)."""
     w = synth.custom(synth.QWEN_A3B_LIKE, T, n_prefill=T // 2, name=f"ragged{T}")
     plan = plan_for(w.spec)
     plan.set_path("auto")
@@ -300,4 +302,19 @@ def test_composed_prefill_calls_vs_oracle():
         got[n_prompt:] = out[c:]
         done += c
     compare_layer(got, ref, synth.TINY.k, TOL_BF16)
+    assert plan.device_error() == 0
+
+
+@pytest.mark.parametrize("T", [8, 9, 16, 17, 64, 65])
+def test_fp4_front_end_switch_points(T):
+    """The 384-expert 4-bit layer at the T where the routing front end, the 64-row geometry and
+    the fused fp16 conversion of x switch; every token against the oracle."""
+    base = workload("fp4_zipf", 0)
+    w = synth.custom(base.spec, T, n_prefill=T // 2, name=f"fp4switch{T}")
+    plan = plan_for(base.spec)
+    plan.set_path("tc")
+    x = to_dev(w.x(), "bf16")
+    out = bf16_tensor_to_f64(plan.forward(x, n_prefill=w.n_prefill))
+    _, ids, _ = plan.route(x, want_logits=False)
+    compare_layer(out, oracle_layer(w), base.spec.k, TOL_FP4, ids.cpu().numpy())
     assert plan.device_error() == 0
