@@ -77,10 +77,18 @@ struct Unit {
 };
 
 // Routed units only; the parts of one expert are tile-major (see gemm_tc.cu).
+// kL2: read the segment records through L2 (the down kernel's raw producer reads them before its
+// grid-dependency wait, when nothing may come from a stale L1 line).
+MOE_DEVICE Seg load_seg_l2(const Seg* p) {
+  const int4 lo = __ldcg(reinterpret_cast<const int4*>(p));
+  const int4 hi = __ldcg(reinterpret_cast<const int4*>(p) + 1);
+  return Seg{lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+}
+template <bool kL2 = false>
 MOE_DEVICE Unit decode_unit(int u, const Seg* segs, int tiles) {
-  const Seg any = segs[u / tiles];
+  const Seg any = kL2 ? load_seg_l2(segs + u / tiles) : segs[u / tiles];
   const int o = u - any.first * tiles;
-  const Seg s = segs[any.first + o % any.nparts];
+  const Seg s = kL2 ? load_seg_l2(segs + any.first + o % any.nparts) : segs[any.first + o % any.nparts];
   return Unit{s.expert, s.row_start, s.rows, o / any.nparts};
 }
 
@@ -273,25 +281,37 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_trigger();
-  pdl_wait();
+  // gate/up lets its dependents start only once its own predecessors (the routing) are complete,
+  // so the down kernel's raw producer may read the unit list -- and request its first weight
+  // stages -- before its grid-dependency wait; everything that reads h waits.
+  if (kGateUp) {
+    pdl_wait();
+    pdl_trigger();
+  } else {
+    pdl_trigger();
+    if (warp != 0) pdl_wait();
+  }
 
   const int tiles = kGateUp ? a.f / 64 : a.d / BM;
   const int nsub = (kGateUp ? a.d : a.f) / kSubK;          // K slices (4-bit blocks) per unit
   const int nst = (nsub + kSubs - 1) / kSubs;              // stages per unit
   const int npair = (nst + kRawPer - 1) / kRawPer;         // raw copies per unit
-  const int total_units = (*a.n_segs) * tiles;
+  const int total_units = __ldcg(a.n_segs) * tiles;
   const uint8_t* wq = kGateUp ? a.q_gu : a.q_down;
 
   if (warp == 0) {
     // ---------------- raw 4-bit blocks: one bulk copy per stage (the blocks are adjacent) -----
     const uint64_t pol_w = l2_policy_evict_first();
     uint32_t p = 0;
-    bool ok = true;
+    bool ok = true, waited = kGateUp;  // down: the first kRawSlots copies go out before the wait
     for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-      const Unit un = decode_unit(u, a.segs, tiles);
+      const Unit un = waited ? decode_unit(u, a.segs, tiles) : decode_unit<true>(u, a.segs, tiles);
       const uint8_t* w0 = wq + (static_cast<size_t>(un.expert) * tiles + un.tile) * nsub * kFp4BlockBytes;
       for (int kp = 0; kp < npair; ++kp, ++p) {
+        if (!waited && p >= static_cast<uint32_t>(kRawSlots)) {
+          pdl_wait();
+          waited = true;
+        }
         const int slot = p % kRawSlots;
         const int sub0 = kRawPer * kSubs * kp;
         const uint32_t bytes = static_cast<uint32_t>(min(kRawPer * kSubs, nsub - sub0)) * kFp4BlockBytes;
@@ -304,6 +324,7 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
         __syncwarp();
       }
     }
+    if (!waited) pdl_wait();
   } else if (warp == 1) {
     // ---------------- MMA issuer (A from TMEM): the warp waits, one elected lane issues -------
     const uint32_t a_base = tmem + kAStart;
