@@ -351,8 +351,7 @@ def run_gpu(args):
     counts = routing_counts(plan, x)
     bf = layer_bytes_flops(w, counts)
 
-    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv") if os.path.isdir(
-        os.path.join(ROOT, "gpurun_out")) else None)
+    clocks = ClockSampler(local, args.clocks_log)
     clocks.start()
     # timed region: K steps, nothing recorded between the layer's kernels
     ms, _, _ = time_forward(plan, x, w.n_prefill, args.steps, args.warmup, world)
@@ -617,6 +616,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the decode, 4-bit and verify workloads")
     ap.add_argument("--cpu-sample", type=int, default=256)
+    ap.add_argument("--clocks-log", default=None, help="write the nvidia-smi samples of the timed region here")
     ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--sample", type=int, default=256, help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
