@@ -32,6 +32,19 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+
+def _times_the_oracle(argv) -> bool:
+    """True for the reference arm and the CPU-baseline worker (both time the oracle on one core)."""
+    if "--cpu-worker" in argv or "--impl=reference" in argv:
+        return True
+    return any(a == "--impl" and b == "reference" for a, b in zip(argv, argv[1:]))
+
+
+# BLAS reads its thread count when it loads, so the one-core pin precedes the numpy import.
+if _times_the_oracle(sys.argv[1:]):
+    for _var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[_var] = "1"
+
 import numpy as np  # noqa: E402
 
 import synth  # noqa: E402
@@ -576,7 +589,6 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
     w = workload_from_args(args)
     rng = np.random.default_rng(7)
     # calibrate: one token, then size each step so the whole run stays within ~2 minutes
