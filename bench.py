@@ -194,25 +194,42 @@ def kernel_alg_bytes(name: str, w: synth.Workload, counts: np.ndarray):
     return table.get(name)
 
 
-def kernel_source_hash() -> str:
+# The sources a kernel's DRAM traffic depends on: its own file, the shared device helpers, the
+# plan code that picks its launch shape and the weight layouts it reads.
+_COMMON_SOURCES = ("common.cuh", "kernels.h", "api.cu", "repack.cu")
+KERNEL_SOURCES = {
+    "tc_gateup": ("gemm_tc.cu",), "tc_down": ("gemm_tc.cu",),
+    "tc_gateup_shared": ("gemm_tc.cu",), "tc_down_shared": ("gemm_tc.cu",),
+    "fp4_gateup": ("gemm_fp4.cu",), "fp4_down": ("gemm_fp4.cu",),
+    "combine": ("combine.cu",),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the sources of one kernel (KERNEL_SOURCES plus the shared ones)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_batches_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(set(KERNEL_SOURCES[kernel] + _COMMON_SOURCES)):
         with open(os.path.join(csrc, name), "rb") as fh:
             h.update(name.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
-def committed_traffic(kernel: str):
-    """dram bytes per launch from the committed ncu summary, if taken on the current sources."""
+def traffic_key(kernel: str, w: synth.Workload) -> str:
+    return f"{kernel}@{w.name}_T{w.T}"
+
+
+def committed_traffic(kernel: str, w: synth.Workload):
+    """dram bytes per launch of `kernel` on workload `w` from the committed ncu summary, if it
+    was taken on the kernel's current sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as fh:
             tr = json.load(fh)
     except (OSError, ValueError):
         return None
-    ent = tr.get(kernel)
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    ent = tr.get(traffic_key(kernel, w))
+    if not ent or kernel not in KERNEL_SOURCES or ent.get("source_hash") != kernel_source_hash(kernel):
         return None
     return ent
 
@@ -386,7 +403,7 @@ def run_gpu(args):
         if alg is None:
             alg = bf["bytes"]
         achieved = alg / per_launch_s / 1e9
-        tr = committed_traffic(name)
+        tr = committed_traffic(name, w)
         roofline = {"bound": bound, "kernel": name, "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                     "frac": round(achieved / hbm, 4), "traffic": tr["bytes_per_launch"] if tr else None,
                     "algorithmic_bytes": alg, "launch_us": round(per_launch_s * 1e6, 2),

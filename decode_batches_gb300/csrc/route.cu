@@ -295,11 +295,10 @@ MOE_DEVICE int topk_select(const float (&v)[PL], int t, int E, int k, int32_t* _
     const uint32_t win_hi = __reduce_max_sync(0xffffffffu, hi);
     const uint32_t win_lo = __reduce_max_sync(0xffffffffu, hi == win_hi ? static_cast<uint32_t>(best) : 0u);
     const int win_e = static_cast<int>(~win_lo);
-    if ((win_e & 31) == lane) {
+    // the owner lane retires the winner (a select per key: the keys stay in registers)
+    const int win_slot = (win_e & 31) == lane ? (win_e >> 5) : -1;
 #pragma unroll
-      for (int i = 0; i < PL; ++i)
-        if (i == (win_e >> 5)) key[i] = 0ull;
-    }
+    for (int i = 0; i < PL; ++i) key[i] = i == win_slot ? 0ull : key[i];
     if (lane == j) sel_i = win_e;
   }
   // gates: softmax over the k selected logits, slot 0 holds the maximum
@@ -748,6 +747,123 @@ MOE_DEVICE void group_small(int T, int E, int k, uint32_t* sm, int32_t* __restri
   }
 }
 
+// Largest step that group_tiny takes: its 64 sort keys, two per lane of one warp.
+constexpr int kTinyGroupRows = 64;
+
+// One compare-exchange stage of a bitonic network over the warp: this lane's key and the key
+// of lane ^ d; the lower lane of the pair keeps the smaller key when the run ascends.
+MOE_DEVICE uint32_t bitonic_ce_shfl(uint32_t v, int lane, int d, bool ascending) {
+  const uint32_t o = __shfl_xor_sync(0xffffffffu, v, d);
+  const bool lower = (lane & d) == 0;
+  return (lower == ascending) ? min(v, o) : max(v, o);
+}
+
+// The same grouping as group_small for steps of at most kTinyGroupRows assignments (T·k <= 64,
+// so every expert has at most 64 rows and one segment).  group_small takes about a dozen
+// block-wide steps, each a barrier apart; here one warp does the ordering in registers and the
+// block meets once.  Each valid assignment a = t·k + j becomes the key (expert << 8) | a
+// (invalid ones -- an id out of range or repeated within the token -- 0xFFFFFFFF), and a bitonic
+// network sorts the 64 keys (lane l holds positions l and l + 32).  The keys are unique, so the
+// sorted position of a key is exactly its row in the stable counting sort by expert: rows of one
+// expert ascend by a.  Segments start where the expert changes; counts and offsets come from
+// a binary search of the sorted keys by every thread of the block.  sids: the step's ids [T][k]
+// in shared memory.  Every thread of the block calls it.
+MOE_DEVICE void group_tiny(int T, int E, int k, const int32_t* sids, int32_t* __restrict__ counts,
+                           int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                           Seg* segs, int32_t* n_segs, int max_segs, uint32_t* err) {
+  constexpr uint32_t kNone = 0xFFFFFFFFu;
+  __shared__ uint32_t s_keys[kTinyGroupRows];
+  const int R = T * k;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    uint32_t key[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int a = lane + 32 * h;
+      key[h] = kNone;
+      if (a < R) {
+        const int t = a / k, j = a - t * k;
+        const int e = sids[a];
+        if (assignment_valid(sids + t * k, j, e, E))
+          key[h] = (static_cast<uint32_t>(e) << 8) | static_cast<uint32_t>(a);
+        else
+          inv[a] = -1;
+      }
+    }
+    // bitonic sort of positions p = lane + 32 h, ascending: runs of length s, partners p ^ d
+#pragma unroll
+    for (int s = 2; s <= 32; s <<= 1) {
+#pragma unroll
+      for (int d = s >> 1; d >= 1; d >>= 1) {
+        const bool asc0 = (lane & s) == 0;                 // p = lane
+        const bool asc1 = s == 32 ? false : asc0;          // p = lane + 32
+        key[0] = bitonic_ce_shfl(key[0], lane, d, asc0);
+        key[1] = bitonic_ce_shfl(key[1], lane, d, asc1);
+      }
+    }
+    {  // s = 64: the halves at distance 32 sit in one lane, then every run ascends
+      const uint32_t lo = min(key[0], key[1]), hi = max(key[0], key[1]);
+      key[0] = lo;
+      key[1] = hi;
+#pragma unroll
+      for (int d = 16; d >= 1; d >>= 1) {
+        key[0] = bitonic_ce_shfl(key[0], lane, d, true);
+        key[1] = bitonic_ce_shfl(key[1], lane, d, true);
+      }
+    }
+    s_keys[lane] = key[0];
+    s_keys[lane + 32] = key[1];
+    // segment starts: a valid key whose expert differs from the key before it
+    const uint32_t v0 = __ballot_sync(0xffffffffu, key[0] != kNone);
+    const uint32_t v1 = __ballot_sync(0xffffffffu, key[1] != kNone);
+    const int n_valid = __popc(v0) + __popc(v1);
+    const uint32_t before0 = __shfl_sync(0xffffffffu, key[0], (lane + 31) & 31);  // p - 1 for p = lane >= 1
+    const uint32_t last0 = __shfl_sync(0xffffffffu, key[0], 31);                  // p = 31
+    const uint32_t before1 = __shfl_sync(0xffffffffu, key[1], (lane + 31) & 31);  // p - 1 for p = lane + 32, lane >= 1
+    const uint32_t prev[2] = {before0, lane == 0 ? last0 : before1};
+    bool start[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      start[h] = key[h] != kNone && ((lane == 0 && h == 0) || (prev[h] >> 8) != (key[h] >> 8));
+    const uint64_t S = static_cast<uint64_t>(__ballot_sync(0xffffffffu, start[0])) |
+                       (static_cast<uint64_t>(__ballot_sync(0xffffffffu, start[1])) << 32);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (key[h] == kNone) continue;
+      const int p = lane + 32 * h;
+      const int a = static_cast<int>(key[h] & 0xFFu);
+      perm[p] = a;
+      inv[a] = p;
+      if (start[h] && segs) {
+        const int idx = __popcll(S & ((1ull << p) - 1ull));
+        const uint64_t upto = p == 63 ? ~0ull : ((2ull << p) - 1ull);  // bits 0..p
+        const uint64_t above = S & ~upto;
+        const int next = above ? __ffsll(static_cast<long long>(above)) - 1 : n_valid;
+        if (idx < max_segs)
+          segs[idx] = Seg{static_cast<int>(key[h] >> 8), p, next - p, idx, 1, 0, 0, 0};
+        else
+          set_error(err, MOE_DEVERR_SEGMENT);
+      }
+    }
+    if (lane == 0 && segs) *n_segs = min(__popcll(S), max_segs);
+  }
+  __syncthreads();
+  // offsets[e] = number of keys below expert e (the invalid keys sort above every expert)
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    int lo = 0, hi = 0;
+    const uint32_t t_lo = static_cast<uint32_t>(e) << 8, t_hi = static_cast<uint32_t>(e + 1) << 8;
+#pragma unroll
+    for (int step = kTinyGroupRows / 2; step >= 1; step >>= 1) {
+      if (s_keys[lo + step - 1] < t_lo) lo += step;
+      if (s_keys[hi + step - 1] < t_hi) hi += step;
+    }
+    lo += s_keys[lo] < t_lo ? 1 : 0;  // lo <= 63 here
+    hi += s_keys[hi] < t_hi ? 1 : 0;
+    offsets[e] = lo;
+    if (e < E) counts[e] = hi - lo;
+  }
+}
+
 template <int PL>
 __global__ void __launch_bounds__(kRgThreads) route_group_kernel(
     const float* __restrict__ parts, int nsplit, const float* __restrict__ bias, int T, int E, int k,
@@ -807,16 +923,19 @@ __global__ void __launch_bounds__(kRgThreads) route_group_kernel(
   int32_t* sids = reinterpret_cast<int32_t*>(sm) + 2 * nch * E;
   for (int i = threadIdx.x; i < T * k; i += kRgThreads) sids[i] = __ldcg(ids + i);
   __syncthreads();
-  group_small(T, E, k, sm, counts, offsets, perm, inv, segs, n_segs, max_segs, err);
+  if (T * k <= kTinyGroupRows)
+    group_tiny(T, E, k, sids, counts, offsets, perm, inv, segs, n_segs, max_segs, err);
+  else
+    group_small(T, E, k, sm, counts, offsets, perm, inv, segs, n_segs, max_segs, err);
   if (threadIdx.x == 0) *done = 0u;  // ready for the next launch (stream-ordered)
 }
 
 // Router, top-k and grouping of a step of at most 8 tokens in one launch: every block forms its
 // K-split partial logits (router_parts_block); the last block to finish adds them (split order,
 // then the bias, as the top-k kernel does), selects each token's top k with one warp per token
-// and groups the step (group_small).
+// and groups the step (group_tiny, or group_small above 64 assignments).
 template <int PL>
-__global__ void __launch_bounds__(kRgThreads) router_route_tiny_kernel(
+__global__ void __launch_bounds__(kRgThreads, 1) router_route_tiny_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias, int T, int E,
     int d, float* __restrict__ parts, int k, int32_t* __restrict__ ids, float* __restrict__ gates,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
@@ -867,7 +986,10 @@ __global__ void __launch_bounds__(kRgThreads) router_route_tiny_kernel(
     if (lane < k) sids[t * k + lane] = sel;
   }
   __syncthreads();
-  group_small(T, E, k, sm, counts, offsets, perm, inv, segs, n_segs, max_segs, err);
+  if (T * k <= kTinyGroupRows)
+    group_tiny(T, E, k, sids, counts, offsets, perm, inv, segs, n_segs, max_segs, err);
+  else
+    group_small(T, E, k, sm, counts, offsets, perm, inv, segs, n_segs, max_segs, err);
   if (threadIdx.x == 0) *done = 0u;  // ready for the next launch (stream-ordered)
 }
 
