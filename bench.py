@@ -574,13 +574,30 @@ def oracle_tokens(w: synth.Workload, rows: np.ndarray) -> float:
     return time.perf_counter() - t0
 
 
+CPU_BASELINE_SECONDS = 15.0   # oracle work the default CPU baseline aims at
+
+
 def cpu_worker(args):
-    """Child process (BLAS pinned to one thread): time the oracle on a bounded token sample."""
+    """Child process (BLAS pinned to one thread): time the oracle on a bounded token sample.
+    --sample N fixes the number of tokens; 0 sizes it to about CPU_BASELINE_SECONDS of oracle
+    work, capped at the whole step: calibration runs grow 4x from 64 tokens until one takes a
+    quarter of that (the oracle's per-expert cost amortises over the tokens, so a small
+    calibration overestimates the cost per token)."""
     w = workload_from_args(args)
     rng = np.random.default_rng(123)
-    n = min(args.sample, w.T)
-    rows = np.sort(rng.choice(w.T, size=n, replace=False))
-    oracle_tokens(w, rows[:1])             # warm (page in weights, import)
+    order = rng.permutation(w.T)
+    oracle_tokens(w, order[:1])            # warm (page in weights, import)
+    if args.sample > 0:
+        n = min(args.sample, w.T)
+    else:
+        n = min(64, w.T)
+        while True:
+            dt = oracle_tokens(w, np.sort(order[:n]))
+            if n >= w.T or dt >= CPU_BASELINE_SECONDS / 4:
+                break
+            n = min(w.T, 4 * n)
+        n = int(min(w.T, max(n, n * CPU_BASELINE_SECONDS / max(dt, 1e-6))))
+    rows = np.sort(order[:n])
     dt = oracle_tokens(w, rows)
     print(json.dumps({"value": n / dt, "seconds": dt, "tokens": n, "T": w.T}))
 
@@ -644,10 +661,11 @@ def main(argv=None):
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the decode, 4-bit and verify workloads")
-    ap.add_argument("--cpu-sample", type=int, default=256)
+    ap.add_argument("--cpu-sample", type=int, default=0,
+                    help="tokens of the CPU-baseline sample (0: about 15 s of oracle work, at most the whole step)")
     ap.add_argument("--clocks-log", default=None, help="write the nvidia-smi samples of the timed region here")
     ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
-    ap.add_argument("--sample", type=int, default=256, help=argparse.SUPPRESS)
+    ap.add_argument("--sample", type=int, default=0, help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
