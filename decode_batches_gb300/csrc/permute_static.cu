@@ -3,9 +3,8 @@
 // moe_permute needs scratch memory (per-chunk expert masks and chunk bases), which normally
 // lives in the workspace the caller allocated for a plan.  Some callers cannot allocate device
 // memory at all: engines whose memory planner owns every byte of the device and forbids a
-// component from allocating outside its pool, and code that runs while a stream is being
-// captured into a CUDA graph or on a latency-critical path, where cudaMalloc is either not
-// permitted or would synchronise the device.  moe_permute_static serves them: its scratch is a
+// component from allocating outside its pool, and code on a latency-critical path, where
+// cudaMalloc would synchronise the device.  moe_permute_static serves them: its scratch is a
 // fixed, file-scope device array that exists as soon as the library is loaded on a device.
 //
 // The array is kStaticWords 32-bit words for the masks plus the same for the chunk bases

@@ -21,8 +21,8 @@
  *     caller owns them and keeps them alive until the work queued on `stream` has finished.
  *   - Layouts are row-major with the last index contiguous.  bf16 tensors are passed as
  *     `void*` holding IEEE bfloat16 bit patterns.
- *   - Calls that take a stream only enqueue work; they never synchronise the host, never
- *     allocate device memory and are safe to capture in a CUDA graph once the plan has its
+ *   - Calls that take a plan and a stream only enqueue work; they never synchronise the host,
+ *     never allocate device memory and are safe to capture in a CUDA graph once the plan has its
  *     weights and workspace.  T == 0 is a no-op that returns MOE_OK.
  *   - A non-MOE_OK status means nothing was enqueued (argument errors are found before any
  *     launch) or, for MOE_ERR_CUDA, that a launch failed; moe_last_error() explains it.
@@ -180,8 +180,7 @@ moe_status moe_permute(moe_plan* plan, const int32_t* ids, int T, int32_t* count
  * moe_permute without a plan and without any device allocation.  The pages have no counterpart
  * to this call; it exists for callers that cannot allocate device memory: engines whose memory
  * planner owns the whole device and forbids components from allocating outside its pool, and
- * code running during CUDA-graph stream capture or on a latency-critical path, where cudaMalloc
- * is not permitted or would synchronise the device.  Same inputs and outputs as moe_permute
+ * code on a latency-critical path, where cudaMalloc would synchronise the device.  Same inputs and outputs as moe_permute
  * (ids int32 [T][k] -> counts [E], offsets [E+1], perm and inv_perm [T*k], all device
  * pointers; invalid or repeated ids are dropped with inv_perm = -1, but there is no error word).
  * Scratch is a fixed 2 MiB device array inside the library, present on every GPU that loads it

@@ -1,7 +1,7 @@
 """The allocation-free grouping call (moe_permute_static) against moe_permute.
 
 moe_permute_static is for callers that cannot allocate device memory (a memory planner that
-owns the device, graph capture, latency-critical paths): it uses a fixed scratch array inside
+owns the device, latency-critical paths where cudaMalloc would synchronise the device): it uses a fixed scratch array inside
 the library instead of a plan workspace.  This file is collected last; it must pass on its own
 in a fresh process and after every other test.  Grouping is integer work, so the comparison is
 bit-exact, on two calls in a row with different ids (the scratch keeps the previous call's
