@@ -7,7 +7,9 @@
 //                      (chunk, expert) gives counts, exclusive offsets and chunk bases; the
 //                      scatter ranks each assignment inside its chunk with one popcount, so
 //                      the permutation is a stable counting sort with no atomics-order
-//                      dependence (identical on every run).
+//                      dependence (identical on every run).  Steps of at most 64 assignments
+//                      sort unique (expert, assignment) keys in one warp instead (group_tiny):
+//                      the same permutation, with one block barrier.
 // Sources: "DeepSeek V4.1F Q4 with native DSpark MTP on M3 Ultra", Decode paragraph (the
 // 384-expert router and its top-k in one dispatch); "Why SSD-streamed MoE was slow: 8GB Jetson
 // Orin Nano, part 2", the `mul_mat_id` grouped matmul and the section on generated text
