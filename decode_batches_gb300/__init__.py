@@ -31,7 +31,8 @@ EXPORTED = (
     "moe_plan_workspace_bytes", "moe_plan_set_workspace", "moe_plan_set_path", "moe_layer_forward",
     "moe_route", "moe_route_logits", "moe_permute", "moe_experts", "moe_combine",
     "moe_plan_get_device_error", "moe_plan_enable_timing", "moe_plan_timing_report",
-    "moe_plan_last_launch_count", "moe_compose_prefill",
+    "moe_plan_last_launch_count", "moe_compose_prefill", "moe_permute_static", "moe_selftest_wait_expiry",
+    "moe_plan_resolved_path",
 )
 
 _lib = None
@@ -77,6 +78,7 @@ def load_library(path: str = LIB_PATH):
         "moe_plan_enable_timing": ([vp, i32], i32),
         "moe_plan_timing_report": ([vp, ctypes.c_char_p, sz], sz),
         "moe_plan_last_launch_count": ([vp], i32),
+        "moe_plan_resolved_path": ([vp], i32),
         "moe_compose_prefill": ([ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                  ctypes.POINTER(PrefillCall), ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)], i32),
     }
@@ -246,10 +248,10 @@ class MoePlan:
         T = gates.shape[0]
         if out is None:
             out = torch.empty((T, self.d), dtype=torch.bfloat16, device=y.device)
-        _check(self.lib.moe_combine(self._h, _dev(y, "y", torch.float16, (T * self.k, self.d)),
+        _check(self.lib.moe_combine(self._h, _dev(y, "y", torch.float32, (T * self.k, self.d)),
                                     _dev(gates, "gates", torch.float32, (T, self.k)),
                                     _dev(inv, "inv", torch.int32, (T * self.k,)),
-                                    _dev(shared_y, "shared_y", torch.float16, (T, self.d)), T,
+                                    _dev(shared_y, "shared_y", torch.float32, (T, self.d)), T,
                                     _dev(out, "out", torch.bfloat16, (T, self.d)), _stream(stream)))
         return out
 
@@ -273,6 +275,12 @@ class MoePlan:
             name, n, ms = line.split()
             rep[name] = (int(n), float(ms))
         return rep
+
+    def resolved_path(self) -> tuple:
+        """('tc' or 'simt', reason): the kernels the expert FFN runs on for this plan."""
+        code = int(self.lib.moe_plan_resolved_path(self._h))
+        name = {v: k for k, v in PATHS.items()}.get(code, "?")
+        return name, ("" if name == "tc" else self.lib.moe_last_error().decode())
 
     def last_launch_count(self) -> int:
         return int(self.lib.moe_plan_last_launch_count(self._h))

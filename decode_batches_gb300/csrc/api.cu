@@ -564,6 +564,20 @@ extern "C" moe_status moe_plan_set_path(moe_plan* p, moe_path path) {
   return MOE_OK;
 }
 
+extern "C" int moe_plan_resolved_path(const moe_plan* p) {
+  if (!p) return -1;
+  if (use_tc(p)) return MOE_PATH_TC;
+  if (p->path == MOE_PATH_SIMT) {
+    fail(MOE_OK, "the CUDA-core path was chosen with moe_plan_set_path or MOE_FORCE_PATH");
+  } else if (p->wdtype == MOE_W_MXFP4 && p->weights_set && p->fp4_tiled && !p->fp4_tc) {
+    fail(MOE_OK, "an e8m0 scale byte is outside [%d, %d]: the 4-bit weights cannot be dequantised exactly "
+                 "into fp16, so the CUDA-core path runs", kFp4ScaleMin, kFp4ScaleMax);
+  } else {
+    fail(MOE_OK, "shape without tensor-core tiles (need d_model %% 128 == 0, d_ff %% 64 == 0, d_ff_shared %% 64 == 0)");
+  }
+  return MOE_PATH_SIMT;
+}
+
 // ============================================================================================
 // step entry points
 // ============================================================================================
@@ -915,17 +929,16 @@ extern "C" moe_status moe_experts(moe_plan* p, const void* x, int T, const int32
                      p->n_shared > 0 ? static_cast<uint16_t*>(shared_y) : nullptr, st);
 }
 
-extern "C" moe_status moe_combine(moe_plan* p, const void* y, const float* gates, const int32_t* inv_perm,
-                                  const void* shared_y, int T, void* out, moe_stream_t stream) {
+extern "C" moe_status moe_combine(moe_plan* p, const float* y, const float* gates, const int32_t* inv_perm,
+                                  const float* shared_y, int T, void* out, moe_stream_t stream) {
   if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
   if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T must be >= 0");
   p->launch_count = 0;
   if (T == 0) return MOE_OK;
   if (!y || !gates || !inv_perm || !out) return fail(MOE_ERR_INVALID_ARG, "y, gates, inv_perm and out are required");
+  if (p->d % 8) return fail(MOE_ERR_UNSUPPORTED, "moe_combine needs d_model %% 8 == 0");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  LAUNCH(p, "combine", st,
-         launch_combine(static_cast<const uint16_t*>(y), gates, inv_perm, static_cast<const uint16_t*>(shared_y), T, p->k,
-                        p->d, static_cast<uint16_t*>(out), st));
+  LAUNCH(p, "combine", st, launch_combine_f32(y, gates, inv_perm, shared_y, T, p->k, p->d, static_cast<uint16_t*>(out), st));
   return MOE_OK;
 }
 

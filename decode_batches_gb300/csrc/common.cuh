@@ -7,11 +7,14 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <set>
 #include <utility>
 
 #include "../../include/moe.h"
@@ -50,6 +53,52 @@ MOE_DEVICE void set_error(uint32_t* err, uint32_t bits) {
 // ------------------------------------------------------------------------------------------
 MOE_DEVICE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 MOE_DEVICE void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Host side: the unique id of the CUDA context current on this thread (cuCtxGetId; ids are never
+// reused within a process).  With no context current yet, the runtime's primary context of the
+// current device is made current first.  Driver entry points come through the runtime, so the
+// library does not link libcuda.
+inline cudaError_t current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  if (!get_current || !get_id) {
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 4000, cudaEnableDefault, &q1);
+    if (e != cudaSuccess || q1 != cudaDriverEntryPointSuccess) return cudaErrorNotSupported;
+    e = cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2);
+    if (e != cudaSuccess || q2 != cudaDriverEntryPointSuccess) return cudaErrorNotSupported;
+    get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f1);
+    get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f2);
+  }
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  if (!ctx) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaSetDevice(dev);  // initialises and binds the primary context
+    if (e != cudaSuccess) return e;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorDeviceUninitialized;
+  }
+  return get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
+// Host side: raise the kernel's dynamic shared-memory limit to `bytes`, once per (context,
+// kernel).  The attribute belongs to the kernel's module in one context, so a plan on a second
+// device, or a context re-created after cudaDeviceReset, sets it again.
+inline cudaError_t ensure_max_dynamic_smem(const void* kern, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<unsigned long long, const void*>> done;
+  unsigned long long ctx = 0;
+  cudaError_t e = current_context_id(&ctx);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({ctx, kern})) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert({ctx, kern});
+  return e;
+}
 
 // Host side: launch `kern` with the programmatic-stream-serialization attribute.
 template <typename... KArgs, typename... Args>
@@ -118,6 +167,20 @@ MOE_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_fl
         return false;
       }
     }
+  }
+}
+
+// Teardown after an aborted pipeline (a bounded wait expired somewhere in the CTA).  A role that
+// gave up may leave bulk / TMA copies it issued still in flight into this CTA's shared memory;
+// their completion cannot be observed once the barrier phases they feed will never complete (the
+// other arrivals are missing).  Every such copy is a bounded read of device memory that lands
+// within microseconds, so the CTA waits a fixed 50 us of %globaltimer before it frees TMEM and
+// exits: no copy outlives the CTA's shared memory.  Called by every thread of the CTA after the
+// final barrier; a no-op unless the abort flag is set.
+MOE_DEVICE void abort_quiesce(volatile int* abort_flag) {
+  if (!abort_flag || !*abort_flag) return;
+  const uint64_t t0 = global_timer_ns();
+  while (global_timer_ns() - t0 < 50000ull) {
   }
 }
 

@@ -586,6 +586,7 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
 
   tc_fence_before();
   __syncthreads();
+  abort_quiesce(abort_flag);
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -598,12 +599,8 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
 template <bool kGateUp, int kN>
 static cudaError_t launch_fq_n(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st) {
   auto kern = fq::fp4_ffn_kernel<kGateUp, kN>;
-  static bool attr = false;  // one per instantiation
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, fq::Geo<kN>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), fq::Geo<kN>::kSmemBytes);
+  if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(num_sms), dim3(fq::Geo<kN>::threads(kGateUp)), fq::Geo<kN>::kSmemBytes, st, *maps, a);
 }
 

@@ -411,6 +411,7 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
 
   tc_fence_before();
   __syncthreads();
+  abort_quiesce(abort_flag);
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -420,16 +421,11 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
 
 }  // namespace tc
 
-static bool g_tc_attr_set[2] = {false, false};
-
 template <bool kGateUp>
 static cudaError_t launch_tc(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st) {
   auto kern = tc::tc_ffn_kernel<kGateUp>;
-  if (!g_tc_attr_set[kGateUp]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    g_tc_attr_set[kGateUp] = true;
-  }
+  cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), tc::kSmemBytes);
+  if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(num_sms), dim3(kGateUp ? 192 + 32 * tc::kGatherWarps : 192), tc::kSmemBytes, st,
                     *maps, a);
 }

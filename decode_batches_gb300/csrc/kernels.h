@@ -167,10 +167,12 @@ cudaError_t launch_fp4_down(const TcMaps* maps, const TcArgs& a, int num_sms, cu
 // x16 = fp16(x), n elements (multiple of 8); out-of-range values clamp and flag MOE_DEVERR_RANGE.
 cudaError_t launch_x_to_f16(const uint16_t* x, uint16_t* x16, size_t n, uint32_t* err, cudaStream_t st);
 
-// ---- combine (combine.cu): y and shared_y fp16, out bf16 ----------------------------------------
+// ---- combine (combine.cu): out bf16; y and shared_y fp16 (the layer's intermediates) or fp32 ----
 cudaError_t launch_combine(const uint16_t* y, const float* gates, const int32_t* inv,
                            const uint16_t* shared_y, int T, int k, int d, uint16_t* out,
                            cudaStream_t st);
+cudaError_t launch_combine_f32(const float* y, const float* gates, const int32_t* inv, const float* shared_y, int T,
+                               int k, int d, uint16_t* out, cudaStream_t st);
 
 // ---- weight repacking at set-up (repack.cu) --------------------------------------------------
 // dst [n][2f][K*elem] <- gate [n][f][K*elem], up [n][f][K*elem], rows interleaved by 8.

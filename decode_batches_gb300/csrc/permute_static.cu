@@ -22,23 +22,34 @@ constexpr size_t kStaticWords = size_t(1) << 18;  // per array: n_chunks * E <= 
 
 static __device__ __align__(256) uint32_t g_static_scratch[2 * kStaticWords];
 
-// Device address of g_static_scratch, looked up once per device with that device current.
+// Device address of g_static_scratch in the current CUDA context.  The module (and the array)
+// is loaded per context, so the address is cached under the context's unique id: a context that
+// was destroyed and re-created (cudaDeviceReset, a released and re-retained primary context)
+// gets a fresh lookup instead of a stale address.
 static std::mutex g_static_mu;
-static void* g_static_ptr[64] = {};
+struct StaticAddr {
+  unsigned long long ctx_id;
+  void* ptr;
+};
+static StaticAddr g_static_cache[64] = {};  // per device ordinal: the last context seen there
 
 static cudaError_t static_scratch(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  unsigned long long id = 0;
+  if ((e = current_context_id(&id)) != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(g_static_mu);
-  if (!g_static_ptr[dev]) {
+  StaticAddr& c = g_static_cache[dev];
+  if (!c.ptr || c.ctx_id != id) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_static_scratch);
     if (e != cudaSuccess) return e;
-    g_static_ptr[dev] = p;
+    c.ptr = p;
+    c.ctx_id = id;
   }
-  *out = g_static_ptr[dev];
+  *out = c.ptr;
   return cudaSuccess;
 }
 

@@ -164,6 +164,7 @@ __global__ void __launch_bounds__(320, 1)
 
   tc_fence_before();
   __syncthreads();
+  abort_quiesce(abort_flag);
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -189,17 +190,11 @@ int router_tc_splits(int T, int E, int d, int num_sms) {
   return s;
 }
 
-static bool g_rt_attr = false;
-
 cudaError_t launch_router_tc(const CUtensorMap* w3, const uint16_t* x, int T, int E, int d, int nsplit, float* parts,
                              uint32_t* err, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
-  if (!g_rt_attr) {
-    cudaError_t e = cudaFuncSetAttribute(rt::router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         rt::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    g_rt_attr = true;
-  }
+  cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(rt::router_tc_kernel), rt::kSmemBytes);
+  if (e != cudaSuccess) return e;
   dim3 grid(E / rt::BM, (T + rt::BN - 1) / rt::BN, nsplit);
   return launch_pdl(rt::router_tc_kernel, grid, dim3(320), rt::kSmemBytes, st, *w3, x, T, E, d, nsplit, parts, err);
 }

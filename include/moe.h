@@ -86,21 +86,29 @@ typedef enum {
 
 /*
  * Create a plan for E routed experts, top-k, model width d_model, expert hidden width d_ff,
- * n_shared always-on shared experts (0 allowed; their width is set by moe_plan_set_shared)
- * and routed-weight format weight_dtype.  Host-side only; no device memory is touched.
+ * n_shared always-on shared experts (0 allowed; their width is set by moe_plan_set_shared) and
+ * routed-weight format weight_dtype.  Source: the layer shapes of "moe-prefill-quantum" (cause
+ * section: 256 experts, k chosen per token) and "DeepSeek V4.1F Q4 with native DSpark MTP on M3
+ * Ultra" (Decode paragraph: a 384-expert router and an always-run shared expert).
+ * Host-side only; no device memory is touched.
  * Limits: 1 <= k <= E <= 1024, k <= 32, d_model and d_ff multiples of 8 (multiples of 32
  * for MOE_W_MXFP4).  Returns NULL on bad arguments (moe_last_error() says why).
  */
 moe_plan* moe_plan_create(int E, int k, int d_model, int d_ff, int n_shared, moe_wdtype weight_dtype);
 
 /* Free the plan and the device memory it owns (its weight copies).  NULL is a no-op.
-   Synchronises the device first so no queued work still reads the plan's memory. */
+   Synchronises the device first so no queued work still reads the plan's memory.  (No
+   counterpart on the pages: resource management of this library.) */
 void moe_plan_destroy(moe_plan* plan);
 
-/* Message for the most recent failing call on this host thread ("" if none). */
+/* Message for the most recent failing call on this host thread ("" if none).  (No counterpart
+   on the pages: error reporting of this library.) */
 const char* moe_last_error(void);
 
 /*
+ * Source: the expert FFN weights gate, up, down of "Why SSD-streamed MoE was slow: 8GB Jetson
+ * Orin Nano, part 2" (section re-checking part 1) and their block-scaled 4-bit form ("moe-prefill-
+ * quantum", hardware-check paragraph: MXFP4 unpack times scale).
  * Copy the layer's weights into plan-owned device memory (repacked for the kernels); the
  * caller's buffers may be freed when this returns.  Synchronous.  All pointers are device
  * pointers.  bf16 down-projection weights are held as fp16 (the down GEMM multiplies them with
@@ -120,6 +128,8 @@ moe_status moe_plan_set_weights(moe_plan* plan, const float* w_router, const flo
                                 const uint8_t* s_gate, const uint8_t* s_up, const uint8_t* s_down);
 
 /*
+ * Source: "DeepSeek V4.1F Q4 with native DSpark MTP on M3 Ultra", Decode paragraph (the shared
+ * expert's gate+up+SwiGLU runs for every token).
  * Shared experts (bf16), added to every token with weight 1:
  *   w_gate, w_up [n_shared][d_ff_shared][d_model],  w_down [n_shared][d_model][d_ff_shared].
  * Required before forward when n_shared > 0 (and before moe_plan_set_workspace, whose size
@@ -128,10 +138,12 @@ moe_status moe_plan_set_weights(moe_plan* plan, const float* w_router, const flo
 moe_status moe_plan_set_shared(moe_plan* plan, int d_ff_shared, const void* w_gate,
                                const void* w_up, const void* w_down);
 
-/* Bytes of device workspace forward/route/permute/experts need for up to T_max tokens. */
+/* Bytes of device workspace forward/route/permute/experts need for up to T_max tokens (no
+   counterpart on the pages: the library's memory contract, so that no call allocates). */
 size_t moe_plan_workspace_bytes(const moe_plan* plan, int T_max);
 
 /*
+ * (No counterpart on the pages: the library's memory contract.)
  * Give the plan a caller-owned device workspace of `bytes` (>= moe_plan_workspace_bytes(T_max),
  * 256-byte aligned).  The plan keeps the pointer until the next call or destroy; it never
  * allocates device memory itself after this point.
@@ -139,11 +151,26 @@ size_t moe_plan_workspace_bytes(const moe_plan* plan, int T_max);
 moe_status moe_plan_set_workspace(moe_plan* plan, void* dev_ptr, size_t bytes, int T_max);
 
 /* Choose the expert-FFN kernels (default MOE_PATH_AUTO; env MOE_FORCE_PATH=simt|tc overrides
-   the default at plan creation). */
+   the default at plan creation).  No counterpart on the pages: a testing and debugging switch. */
 moe_status moe_plan_set_path(moe_plan* plan, moe_path path);
 
 /*
- * The whole layer.  x bf16 [T][d_model] -> out bf16 [T][d_model]:
+ * The kernels the expert FFN will actually run on (no counterpart on the pages): MOE_PATH_TC
+ * or MOE_PATH_SIMT, as MOE_PATH_AUTO (or a forced path) resolves for the plan's shapes and
+ * weights -- the tensor-core path needs d_model % 128 == 0, d_ff % 64 == 0, d_ff_shared % 64
+ * == 0 and, for MOE_W_MXFP4, every e8m0 scale byte in [104, 140] (where e2m1 x 2^(s-127) is exact
+ * in fp16).  MOE_PATH_SIMT is the CUDA-core reference path, orders of magnitude slower; a caller
+ * that must not run it checks this after moe_plan_set_weights / moe_plan_set_shared, and
+ * moe_last_error() then names the reason.  Returns -1 for a NULL plan.
+ */
+int moe_plan_resolved_path(const moe_plan* plan);
+
+/*
+ * The whole layer on one serving step.  Source: "moe-prefill-quantum", the cause section and
+ * Table 9 (a step's batch is a prefill chunk of `quantum` rows plus the decode rows of the
+ * generating sessions, and every row goes through the MoE layer) and "DeepSeek V4.1F Q4 with
+ * native DSpark MTP on M3 Ultra", Decode and DSpark paragraphs (decode and 6-row verify steps).
+ * x bf16 [T][d_model] -> out bf16 [T][d_model]:
  *   out[t] = sum_j g[t,j] * FFN_{ids[t,j]}(x[t]) + sum_s FFN_shared_s(x[t]),
  * the sum taken in fp32 in slot order j = 0..k-1, then the shared term, then one
  * round-to-nearest-even to bf16.  Rows [0, n_prefill) are prefill rows and the rest decode or
@@ -154,7 +181,10 @@ moe_status moe_layer_forward(moe_plan* plan, const void* x, int T, int n_prefill
                              moe_stream_t stream);
 
 /*
- * Router + top-k.  logits fp32 [T][E] (may be NULL: then kept in the workspace),
+ * Router + top-k.  Source: "DeepSeek V4.1F Q4 with native DSpark MTP on M3 Ultra", Decode
+ * paragraph (router logits and top-k selection, one dispatch); "moe-prefill-quantum", cause
+ * section (k of E experts per token).  The tie rule (lower index first) is this library's.
+ * logits fp32 [T][E] (may be NULL: then kept in the workspace),
  * ids int32 [T][k], gates fp32 [T][k].  Slot j holds the (j+1)-th largest logit under the
  * order (value desc, index asc; +0 == -0; NaN lowest); gates are the softmax of the k
  * selected logits, computed in fp32.
@@ -162,16 +192,23 @@ moe_status moe_layer_forward(moe_plan* plan, const void* x, int T, int n_prefill
 moe_status moe_route(moe_plan* plan, const void* x, int T, float* logits, int32_t* ids,
                      float* gates, moe_stream_t stream);
 
-/* Top-k and gates from given fp32 logits [T][E] (the same selection code as moe_route). */
+/* Top-k and gates from given fp32 logits [T][E] (the same selection code as moe_route; the
+   Decode paragraph's top-k step of "DeepSeek V4.1F Q4 with native DSpark MTP on M3 Ultra").
+   Exists so that selection can be compared bit for bit on identical logits. */
 moe_status moe_route_logits(moe_plan* plan, const float* logits, int T, int32_t* ids,
                             float* gates, moe_stream_t stream);
 
 /*
- * Grouping of the T*k assignments a = t*k + j by expert:
+ * Grouping of the T*k assignments a = t*k + j by expert.  Source: "Why SSD-streamed MoE was
+ * slow: 8GB Jetson Orin Nano, part 2" -- the grouped expert matmul (`mul_mat_id`, first-cache
+ * section) needs the rows of each expert together, and the section on generated text changing
+ * between runs requires every chosen expert to be computed exactly once (a bijection here):
  *   counts int32 [E], offsets int32 [E+1] (exclusive scan, offsets[E] = T*k),
  *   perm int32 [T*k] (perm[r] = a, a stable counting sort: rows of one expert ascend by a),
  *   inv_perm int32 [T*k] (inv_perm[perm[r]] = r).
- * ids outside [0, E) set MOE_DEVERR_EXPERT_RANGE and are dropped from counts and perm.
+ * An id outside [0, E), or one that repeats an earlier slot of the same token, sets
+ * MOE_DEVERR_EXPERT_RANGE and is dropped: it is not counted, gets no row, and its inv_perm entry
+ * is -1; perm then holds offsets[E] < T*k rows and its tail is left untouched.
  */
 moe_status moe_permute(moe_plan* plan, const int32_t* ids, int T, int32_t* counts,
                        int32_t* offsets, int32_t* perm, int32_t* inv_perm, moe_stream_t stream);
@@ -185,9 +222,10 @@ moe_status moe_permute(moe_plan* plan, const int32_t* ids, int T, int32_t* count
  * pointers; invalid or repeated ids are dropped with inv_perm = -1, but there is no error word).
  * Scratch is a fixed 2 MiB device array inside the library, present on every GPU that loads it
  * until the process exits; ceil(T / 32) * E must not exceed 262144 (T <= 32768 at E = 256),
- * else MOE_ERR_WORKSPACE and nothing is enqueued.  The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress); make that first call before any stream
- * capture.  All calls share the array: two calls that may run at the same time on the GPU
+ * else MOE_ERR_WORKSPACE and nothing is enqueued.  The first call in a CUDA context (the first
+ * on a device, and the first after that device's context was destroyed and re-created, e.g. by
+ * cudaDeviceReset) looks up the array's device address (cudaGetSymbolAddress); make that first
+ * call before any stream capture.  All calls share the array: two calls that may run at the same time on the GPU
  * (unordered streams) race; calls ordered on one stream do not.  Every scratch word a call
  * reads is rewritten by that call, so no clearing is needed between calls.
  */
@@ -195,7 +233,24 @@ moe_status moe_permute_static(int E, int k, const int32_t* ids, int T, int32_t* 
                               int32_t* offsets, int32_t* perm, int32_t* inv_perm, moe_stream_t stream);
 
 /*
- * Expert FFNs on grouped rows (testing entry point for the grouped GEMMs):
+ * Self-test of the bounded waits' expiry path (failure detection; the pages have no counterpart).
+ * Launches one CTA whose first warp waits on an mbarrier phase nothing completes, with the same
+ * bounded wait the layer's kernels use, while its second warp holds a TMEM allocation: after
+ * about one second (the kernels' wait limit) the wait gives up, sets MOE_DEVERR_TIMEOUT in *err
+ * and raises the CTA's abort flag, and the CTA takes the GEMM kernels' abort teardown (waits out
+ * in-flight copies, frees TMEM) and returns, leaving the context usable.
+ *   err     device uint32, OR-ed with the error bits (the caller clears it first);
+ *   result  device uint32 [3]: [0] = 2 when the wait expired (1 if it completed), [1] = the
+ *           milliseconds it waited, [2] = 1 if the abort flag was raised.
+ * Returns MOE_ERR_INVALID_ARG for NULL pointers, MOE_ERR_CUDA if the launch fails.
+ */
+moe_status moe_selftest_wait_expiry(uint32_t* err, uint32_t* result, moe_stream_t stream);
+
+/*
+ * Expert FFNs on grouped rows (testing entry point for the grouped GEMMs).  Source: "Why
+ * SSD-streamed MoE was slow: 8GB Jetson Orin Nano, part 2", section re-checking part 1 (gate ->
+ * up -> down, SwiGLU(gate, up)); "DeepSeek V4.1F Q4 with native DSpark MTP on M3 Ultra", Decode
+ * paragraph (intermediates rounded inside the producing kernel):
  *   y[r] = FFN_e(x[perm[r] / k]) for r in [offsets[e], offsets[e+1]),  fp16 [T*k][d_model],
  *   shared_y[t] = sum_s FFN_shared_s(x[t]) fp16 [T][d_model] (may be NULL if n_shared == 0).
  * FFN(x) = W_d (silu(W_g x) * (W_u x)) with fp32 accumulation; the hidden vector is rounded to
@@ -207,23 +262,28 @@ moe_status moe_experts(moe_plan* plan, const void* x, int T, const int32_t* offs
                        const int32_t* perm, void* y, void* shared_y, moe_stream_t stream);
 
 /*
- * Gate-weighted unpermute-combine:
+ * Gate-weighted unpermute-combine.  Source: the combine is implicit in the pages -- every token's
+ * output is the gate-weighted sum of its chosen experts' outputs ("moe-prefill-quantum", cause
+ * section: each token is sent to k of the E experts; "Why SSD-streamed MoE was slow", part 2,
+ * the section on generated text changing between runs: each chosen expert counted exactly once).
  *   out[t] = sum_{j<k} gates[t,j] * y[inv_perm[t*k+j]]  (+ shared_y[t]),
- * fp32 accumulation in slot order, one round-to-nearest-even to bf16.
- *   y fp16 [T*k][d_model] in grouped (permuted) row order; gates fp32 [T][k];
- *   inv_perm int32 [T*k] (entries < 0 are skipped); shared_y fp16 [T][d_model] or NULL;
- *   out bf16 [T][d_model].
- * Needs no workspace.
+ * fp32 accumulation in slot order, then the shared term, one round-to-nearest-even to bf16.
+ *   y         fp32 [T*k][d_model] in grouped (permuted) row order (device);
+ *   gates     fp32 [T][k];  inv_perm int32 [T*k] (entries < 0 are skipped);
+ *   shared_y  fp32 [T][d_model] or NULL;  out bf16 [T][d_model].
+ * Needs no workspace and no weights (only the plan's k and d_model).  d_model % 8 != 0 gives
+ * MOE_ERR_UNSUPPORTED.  (moe_layer_forward runs the same kernel on its own fp16 intermediates.)
  */
-moe_status moe_combine(moe_plan* plan, const void* y, const float* gates, const int32_t* inv_perm,
-                       const void* shared_y, int T, void* out, moe_stream_t stream);
+moe_status moe_combine(moe_plan* plan, const float* y, const float* gates, const int32_t* inv_perm,
+                       const float* shared_y, int T, void* out, moe_stream_t stream);
 
 /* Synchronise the device, return the device error word in *code (host pointer) and clear
-   it.  Returns MOE_ERR_DEVICE when *code != 0. */
+   it.  Returns MOE_ERR_DEVICE when *code != 0.  No counterpart on the pages (failure detection
+   of this library: device-side problems never trap). */
 moe_status moe_plan_get_device_error(moe_plan* plan, uint32_t* code);
 
 /*
- * Per-kernel timing for profiling.  When enabled, every kernel launched by the calls above
+ * Per-kernel timing for profiling (no counterpart on the pages).  When enabled, every kernel launched by the calls above
  * is bracketed by CUDA events recorded on the launching stream (a few microseconds of
  * overhead per launch).  moe_plan_timing_report synchronises, writes one line per kernel
  * name, "name launches total_ms\n", into buf (host memory, NUL-terminated, truncated to
@@ -232,7 +292,9 @@ moe_status moe_plan_get_device_error(moe_plan* plan, uint32_t* code);
 moe_status moe_plan_enable_timing(moe_plan* plan, int enable);
 size_t moe_plan_timing_report(moe_plan* plan, char* buf, size_t len);
 
-/* Number of kernels the most recent moe_layer_forward call launched. */
+/* Number of kernels the most recent moe_layer_forward call launched (no counterpart on the
+   pages; the Decode paragraph of "DeepSeek V4.1F Q4 with native DSpark MTP on M3 Ultra" counts
+   dispatches per layer the same way). */
 int moe_plan_last_launch_count(const moe_plan* plan);
 
 /*

@@ -30,6 +30,38 @@ def test_header_declares_the_layer_entry_points():
         assert required in names
 
 
+def _params(name):
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    m = re.search(r"\b" + name + r"\s*\(([^)]*)\)\s*;", text)
+    assert m, name
+    return [" ".join(p.split()) for p in m.group(1).split(",")]
+
+
+def test_combine_takes_fp32_expert_outputs():
+    """The boundary's combine call takes y and shared_y as fp32 (the layer keeps its own
+    intermediates in fp16 and calls the kernel internally)."""
+    params = _params("moe_combine")
+    assert params[1] == "const float* y" and params[4] == "const float* shared_y", params
+    assert params[2] == "const float* gates" and params[3] == "const int32_t* inv_perm"
+
+
+def test_every_declaration_cites_its_source_or_says_it_has_none():
+    """Each entry point's comment names the page passage it implements, or states that the pages
+    have no counterpart."""
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    for name in declared_functions():
+        m = re.search(r"\n[a-z_ *]*\b" + name + r"\s*\(", text)
+        assert m, name
+        lines = text[:m.start()].split("\n")
+        i = len(lines)                         # back to the end of the previous declaration
+        while i > 0 and not (lines[i - 1].rstrip().endswith(");") and not lines[i - 1].lstrip().startswith("*")
+                             and "/*" in "\n".join(lines[i:])):
+            i -= 1                             # (declarations that share one comment share its citation)
+        doc = "\n".join(lines[i:])
+        assert ('"' in doc) or ("no counterpart" in " ".join(doc.lower().replace("*", " ").split())), name
+
+
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), f"libmoe.so does not export {name}"

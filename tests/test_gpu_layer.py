@@ -18,7 +18,8 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 FULL = [("tiny", 0), ("decode", 0), ("mixed", 128), ("verify", 0)]
-SAMPLED = [("mixed", 2048), ("mixed", 8192), ("fp4_zipf", 0)]
+# every quantum of the mixed-step sweep goes through the whole layer against the oracle
+SAMPLED = [("mixed", 512), ("mixed", 1024), ("mixed", 2048), ("mixed", 4096), ("mixed", 8192), ("fp4_zipf", 0)]
 
 
 @functools.lru_cache(maxsize=None)
@@ -51,6 +52,7 @@ def test_forward_full_vs_oracle(name, q, path):
     w = workload(name, q)
     plan = plan_for(w.spec)
     plan.set_path(path)
+    assert plan.resolved_path()[0] == path
     x = to_dev(w.x(), "bf16")
     out = bf16_tensor_to_f64(plan.forward(x, n_prefill=w.n_prefill))
     _, ids, _ = plan.route(x, want_logits=False)
@@ -101,8 +103,8 @@ def test_combine_vs_oracle(T, k, d, shared):
     from decode_batches_gb300 import MoePlan
     plan = MoePlan(16, k, d, 64, 0, "bf16")
     rng = np.random.default_rng(T)
-    y = rng.normal(size=(T * k, d)).astype(np.float16)
-    ys = rng.normal(size=(T, d)).astype(np.float16) if shared else None
+    y = rng.normal(size=(T * k, d)).astype(np.float32)
+    ys = rng.normal(size=(T, d)).astype(np.float32) if shared else None
     g = rng.random((T, k)).astype(np.float32)
     g /= g.sum(1, keepdims=True)
     inv = rng.permutation(T * k).astype(np.int32)
@@ -154,9 +156,11 @@ def test_forward_ragged_sizes(T):
     plan.set_path("auto")
     x = to_dev(w.x(), "bf16")
     out = bf16_tensor_to_f64(plan.forward(x, n_prefill=w.n_prefill))
+    _, ids, _ = plan.route(x, want_logits=False)
     rows = sample_rows(w, 48)
     ref = oracle_layer(w, rows)
-    compare_layer(out[rows], ref, w.spec.k, TOL_BF16)
+    compare_layer(out[rows], ref, w.spec.k, TOL_BF16, ids.cpu().numpy()[rows])
+    assert plan.device_error() == 0
 
 
 # odd tile counts everywhere (gate/up 3, down 3, shared gate/up 5): with T = 4000 the 16-bit
@@ -171,9 +175,10 @@ def test_odd_tile_counts(T):
     plan.set_path("tc")
     x = to_dev(w.x(), "bf16")
     out = bf16_tensor_to_f64(plan.forward(x, n_prefill=w.n_prefill))
+    _, ids, _ = plan.route(x, want_logits=False)
     rows = sample_rows(w, 64)
     ref = oracle_layer(w, rows)
-    compare_layer(out[rows], ref, w.spec.k, TOL_BF16)
+    compare_layer(out[rows], ref, w.spec.k, TOL_BF16, ids.cpu().numpy()[rows])
     assert plan.device_error() == 0
 
 
@@ -209,6 +214,8 @@ def test_untiled_shape_runs_the_reference_path():
     from decode_batches_gb300 import MoeError
     with pytest.raises(MoeError):
         plan.set_path("tc")
+    path, why = plan.resolved_path()
+    assert path == "simt" and "tensor-core tiles" in why
     x = to_dev(w.x(), "bf16")
     out = bf16_tensor_to_f64(plan.forward(x, n_prefill=w.n_prefill))
     _, ids, _ = plan.route(x, want_logits=False)
@@ -273,6 +280,8 @@ def test_fp4_scales_outside_fp16_range_use_the_reference_path():
     plan.allocate_workspace(w.T)
     with pytest.raises(MoeError):
         plan.set_path("tc")
+    path, why = plan.resolved_path()
+    assert path == "simt" and "scale byte" in why
     x = to_dev(w.x(), "bf16")
     out = bf16_tensor_to_f64(plan.forward(x, n_prefill=w.n_prefill))
     ref = oracle.moe_layer(w.x(), w.router_weight(), None, s.k,
