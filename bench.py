@@ -200,6 +200,8 @@ def kernel_alg_bytes(name: str, w: synth.Workload, counts: np.ndarray):
         "tc_gateup_shared": sh_gu + x + h_s,
         "tc_down_shared": sh_dn + h_s + y_s,
         "combine": y_r + y_s + x + R * 8.0,
+        # the one-launch small step: the whole layer (router, touched and shared weights, x, out)
+        "layer_small": touched * 3.0 * s.d * s.f * wb + sh_gu + sh_dn + s.d * s.E * 4.0 + 2.0 * x + R * 8.0,
     }
     return table.get(name)
 
@@ -212,6 +214,7 @@ KERNEL_SOURCES = {
     "tc_gateup_shared": ("gemm_tc.cu",), "tc_down_shared": ("gemm_tc.cu",),
     "fp4_gateup": ("gemm_fp4.cu",), "fp4_down": ("gemm_fp4.cu",),
     "combine": ("combine.cu",),
+    "layer_small": ("layer_small.cu", "topk.cuh"),
 }
 
 

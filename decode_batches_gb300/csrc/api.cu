@@ -53,6 +53,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
   size_t logits, parts, ids, gates, masks, chunk_base, counts, offsets, perm, inv, segs, n_segs, h, h_s, y, y_s, x16;
+  size_t touched, y32;  // the one-launch small-step layer: touched-expert list, fp32 expert outputs
   size_t total;
   int max_segs;
 };
@@ -82,6 +83,7 @@ struct moe_plan {
   uint16_t* w_gu_s = nullptr;
   uint16_t* w_down_s = nullptr;
   uint32_t* err = nullptr;
+  uint32_t* ls_sync = nullptr;  // launch-wide words of the one-launch small-step layer (zero between launches)
   bool weights_set = false, shared_set = false;
   bool tiled = false, tiled_s = false;  // weights stored in the tile-contiguous layouts
   bool fp4_tiled = false;  // 4-bit routed weights in the tile-contiguous layout
@@ -147,6 +149,9 @@ static WsLayout layout_for(const moe_plan* p, int T_max) {
   L.y = take(R * p->d * 2);
   L.y_s = take(T * p->d * 2);
   L.x16 = take(p->wdtype == MOE_W_MXFP4 ? T * p->d * 2 : 0);
+  const size_t T8 = T < static_cast<size_t>(kLsTMax) ? T : static_cast<size_t>(kLsTMax);
+  L.touched = take((p->E + 1) * sizeof(int32_t));
+  L.y32 = take(p->wdtype == MOE_W_BF16 ? T8 * (p->k + 1) * p->d * sizeof(float) : 0);
   L.total = o;
   return L;
 }
@@ -167,6 +172,14 @@ static bool tc_shape_ok(const moe_plan* p) {
 static bool use_tc(const moe_plan* p) {
   if (p->path == MOE_PATH_SIMT) return false;
   return tc_shape_ok(p);
+}
+
+// The one-launch small-step layer (layer_small.cu): MOE_PATH_AUTO at T <= 8 with bf16 routed
+// weights in the tensor-core tile layout (the kernel streams those tiles).
+static bool use_small_layer(const moe_plan* p, int T) {
+  return p->path == MOE_PATH_AUTO && p->wdtype == MOE_W_BF16 && tc_shape_ok(p) && p->tiled &&
+         (p->n_shared == 0 || p->tiled_s) && p->ls_sync &&
+         layer_small_ok(T, p->E, p->k, p->d, p->f, p->n_shared, p->f_s);
 }
 
 // ---- timing -----------------------------------------------------------------------------------
@@ -327,6 +340,7 @@ extern "C" void moe_plan_destroy(moe_plan* p) {
   cudaFree(p->w_gu_s);
   cudaFree(p->w_down_s);
   cudaFree(p->err);
+  cudaFree(p->ls_sync);
   for (auto& t : p->timed) {
     cudaEventDestroy(t.start);
     cudaEventDestroy(t.stop);
@@ -551,6 +565,10 @@ extern "C" moe_status moe_plan_set_workspace(moe_plan* p, void* dev_ptr, size_t 
   moe_status s = ensure_err_word(p);
   if (s != MOE_OK) return s;
   if ((s = ensure_side_stream(p)) != MOE_OK) return s;
+  if (!p->ls_sync) {
+    MOE_CUDA_TRY(cudaMalloc(&p->ls_sync, kLsSyncWords * sizeof(uint32_t)));
+    MOE_CUDA_TRY(cudaMemset(p->ls_sync, 0, kLsSyncWords * sizeof(uint32_t)));
+  }
   return build_ws_maps(p);
 }
 
@@ -797,6 +815,35 @@ extern "C" moe_status moe_layer_forward(moe_plan* p, const void* x, int T, int n
   if (!x || !out) return fail(MOE_ERR_INVALID_ARG, "x and out are required");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const uint16_t* xb = static_cast<const uint16_t*>(x);
+  if (use_small_layer(p, T)) {
+    LsArgs a;
+    a.x = xb;
+    a.w_router = p->w_router;
+    a.b_router = p->b_router;
+    a.w_gu = reinterpret_cast<const uint16_t*>(p->w_gu);
+    a.w_down = reinterpret_cast<const uint16_t*>(p->w_down);
+    a.w_gu_s = p->w_gu_s;
+    a.w_down_s = p->w_down_s;
+    a.logits = ws_ptr<float>(p, p->L.logits);
+    a.ids = ws_ptr<int32_t>(p, p->L.ids);
+    a.gates = ws_ptr<float>(p, p->L.gates);
+    a.counts = ws_ptr<int32_t>(p, p->L.counts);
+    a.offsets = ws_ptr<int32_t>(p, p->L.offsets);
+    a.perm = ws_ptr<int32_t>(p, p->L.perm);
+    a.inv = ws_ptr<int32_t>(p, p->L.inv);
+    a.touched = ws_ptr<int32_t>(p, p->L.touched);
+    a.n_touched = a.touched + p->E;
+    a.h = ws_ptr<uint16_t>(p, p->L.h);
+    a.h_s = ws_ptr<uint16_t>(p, p->L.h_s);
+    a.y32 = ws_ptr<float>(p, p->L.y32);
+    a.ys32 = a.y32 + static_cast<size_t>(T) * p->k * p->d;
+    a.out = static_cast<uint16_t*>(out);
+    a.sync = p->ls_sync;
+    a.err = p->err;
+    a.T = T, a.E = p->E, a.k = p->k, a.d = p->d, a.f = p->f, a.n_shared = p->n_shared, a.f_s = p->f_s;
+    LAUNCH(p, "layer_small", st, launch_layer_small(a, p->num_sms, st));
+    return MOE_OK;
+  }
   int32_t* ids = ws_ptr<int32_t>(p, p->L.ids);
   float* gates = ws_ptr<float>(p, p->L.gates);
   uint32_t* masks = ws_ptr<uint32_t>(p, p->L.masks);
@@ -895,8 +942,9 @@ extern "C" moe_status moe_permute(moe_plan* p, const int32_t* ids, int T, int32_
   if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T must be >= 0");
   if (!p->ws) return fail(MOE_ERR_NOT_READY, "workspace not set");
   if (T > p->T_max) return fail(MOE_ERR_WORKSPACE, "T=%d exceeds the workspace's T_max=%d", T, p->T_max);
-  if (!counts || !offsets || !perm || !inv_perm || (T > 0 && !ids))
-    return fail(MOE_ERR_INVALID_ARG, "ids, counts, offsets, perm and inv_perm are required");
+  if (!counts || !offsets || (T > 0 && (!ids || !perm || !inv_perm)))
+    return fail(MOE_ERR_INVALID_ARG, "ids, counts, offsets, perm and inv_perm are required (ids, perm, inv_perm "
+                                     "may be NULL when T == 0)");
   moe_status s = ensure_err_word(p);
   if (s != MOE_OK) return s;
   p->launch_count = 0;

@@ -167,6 +167,40 @@ cudaError_t launch_fp4_down(const TcMaps* maps, const TcArgs& a, int num_sms, cu
 // x16 = fp16(x), n elements (multiple of 8); out-of-range values clamp and flag MOE_DEVERR_RANGE.
 cudaError_t launch_x_to_f16(const uint16_t* x, uint16_t* x16, size_t n, uint32_t* err, cudaStream_t st);
 
+// ---- one-launch layer of a small step (layer_small.cu) ------------------------------------------
+constexpr int kLsTMax = 8;                  // tokens per step
+constexpr int kLsUnionBytes = 72 * 1024;    // x (bf16) and then h (fp16) of the step in shared memory
+constexpr int kLsMaxGroups = 512;           // d_model / 32
+constexpr int kLsSyncWords = 8 + kLsMaxGroups;
+struct LsArgs {
+  const uint16_t* x = nullptr;
+  const float* w_router = nullptr;
+  const float* b_router = nullptr;
+  const uint16_t* w_gu = nullptr;      // tile-contiguous layouts of the tensor-core path
+  const uint16_t* w_down = nullptr;
+  const uint16_t* w_gu_s = nullptr;
+  const uint16_t* w_down_s = nullptr;
+  float* logits = nullptr;             // [T][E]
+  int32_t* ids = nullptr;              // [T][k]
+  float* gates = nullptr;              // [T][k]
+  int32_t* counts = nullptr;           // [E]
+  int32_t* offsets = nullptr;          // [E + 1]
+  int32_t* perm = nullptr;             // [T k]
+  int32_t* inv = nullptr;              // [T k]
+  int32_t* touched = nullptr;          // [E]: touched experts, ascending
+  int32_t* n_touched = nullptr;        // 1 word
+  uint16_t* h = nullptr;               // fp16 [T k][f] grouped rows
+  uint16_t* h_s = nullptr;             // fp16 [T][n_s f_s]
+  float* y32 = nullptr;                // fp32 [T k][d] per assignment t k + j
+  float* ys32 = nullptr;               // fp32 [T][d]
+  uint16_t* out = nullptr;             // bf16 [T][d]
+  uint32_t* sync = nullptr;            // kLsSyncWords plan-owned words, zero between launches
+  uint32_t* err = nullptr;
+  int T = 0, E = 0, k = 0, d = 0, f = 0, n_shared = 0, f_s = 0;
+};
+bool layer_small_ok(int T, int E, int k, int d, int f, int n_shared, int f_s);
+cudaError_t launch_layer_small(const LsArgs& a, int num_sms, cudaStream_t st);
+
 // ---- combine (combine.cu): out bf16; y and shared_y fp16 (the layer's intermediates) or fp32 ----
 cudaError_t launch_combine(const uint16_t* y, const float* gates, const int32_t* inv,
                            const uint16_t* shared_y, int T, int k, int d, uint16_t* out,

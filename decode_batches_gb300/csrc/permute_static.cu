@@ -59,7 +59,7 @@ extern "C" moe_status moe_permute_static(int E, int k, const int32_t* ids, int T
                                          int32_t* perm, int32_t* inv_perm, moe_stream_t stream) {
   using namespace moe;
   if (E < 1 || E > 1024 || k < 1 || k > 32 || k > E || T < 0) return MOE_ERR_INVALID_ARG;
-  if (!counts || !offsets || !perm || !inv_perm || (T > 0 && !ids)) return MOE_ERR_INVALID_ARG;
+  if (!counts || !offsets || (T > 0 && (!ids || !perm || !inv_perm))) return MOE_ERR_INVALID_ARG;
   const size_t n_chunks = (static_cast<size_t>(T) + kChunk - 1) / kChunk;
   if (n_chunks * static_cast<size_t>(E) > kStaticWords) return MOE_ERR_WORKSPACE;
   void* base = nullptr;

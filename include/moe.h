@@ -71,9 +71,12 @@ typedef enum {
 
 /* Which kernels run the expert FFN (gate/up + SwiGLU + down). */
 typedef enum {
-  MOE_PATH_AUTO = 0, /* tensor-core path where the shape allows it */
+  MOE_PATH_AUTO = 0, /* chosen by T: a step of at most 8 tokens with bf16 routed weights runs the
+                        whole layer in one launch that streams the weights (a GEMV on the CUDA
+                        cores); larger steps, and 4-bit weights, the tensor-core path where the
+                        shape allows it */
   MOE_PATH_SIMT = 1, /* plain CUDA-core grouped FFN (debug/reference path, slow) */
-  MOE_PATH_TC = 2    /* tcgen05/TMEM grouped GEMM (requires d % 128 == 0, d_ff % 64 == 0) */
+  MOE_PATH_TC = 2    /* tcgen05/TMEM grouped GEMM at every T (requires d % 128 == 0, d_ff % 64 == 0) */
 } moe_path;
 
 /* Device error bits (moe_plan_get_device_error). */
@@ -208,7 +211,8 @@ moe_status moe_route_logits(moe_plan* plan, const float* logits, int T, int32_t*
  *   inv_perm int32 [T*k] (inv_perm[perm[r]] = r).
  * An id outside [0, E), or one that repeats an earlier slot of the same token, sets
  * MOE_DEVERR_EXPERT_RANGE and is dropped: it is not counted, gets no row, and its inv_perm entry
- * is -1; perm then holds offsets[E] < T*k rows and its tail is left untouched.
+ * is -1; perm then holds offsets[E] < T*k rows and its tail is left untouched.  With T == 0,
+ * counts and offsets are zeroed and ids, perm, inv_perm may be NULL.
  */
 moe_status moe_permute(moe_plan* plan, const int32_t* ids, int T, int32_t* counts,
                        int32_t* offsets, int32_t* perm, int32_t* inv_perm, moe_stream_t stream);

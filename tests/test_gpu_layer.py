@@ -327,3 +327,29 @@ def test_fp4_front_end_switch_points(T):
     _, ids, _ = plan.route(x, want_logits=False)
     compare_layer(out, oracle_layer(w), base.spec.k, TOL_FP4, ids.cpu().numpy())
     assert plan.device_error() == 0
+
+
+@pytest.mark.parametrize("spec_name,T", [("decode", 1), ("decode", 2), ("decode", 4), ("decode", 7), ("decode", 8),
+                                         ("tiny", 1), ("tiny", 5), ("tiny", 8)])
+def test_small_step_one_launch_vs_oracle(spec_name, T):
+    """Steps of at most 8 tokens on bf16 weights run the whole layer in one launch (router, top-k,
+    grouping, weight-streaming gate/up + SwiGLU and down, combine).  Every token against the
+    oracle, the same answer twice (bit for bit), and close to the tensor-core path's."""
+    spec = workload(spec_name, 0).spec
+    w = synth.custom(spec, T, n_prefill=T // 2, name=f"small{spec_name}{T}")
+    plan = plan_for(spec)
+    plan.set_path("auto")
+    x = to_dev(w.x(), "bf16")
+    a = plan.forward(x, n_prefill=w.n_prefill).clone()
+    assert plan.last_launch_count() == 1
+    b = plan.forward(x, n_prefill=w.n_prefill).clone()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    _, ids, _ = plan.route(x, want_logits=False)
+    got = bf16_tensor_to_f64(a)
+    compare_layer(got, oracle_layer(w), spec.k, TOL_BF16, ids.cpu().numpy())
+    plan.set_path("tc")
+    c = bf16_tensor_to_f64(plan.forward(x, n_prefill=w.n_prefill))
+    plan.set_path("auto")
+    rms = np.sqrt(np.mean(got ** 2))
+    assert np.abs(got - c).max() <= 1e-2 * rms
+    assert plan.device_error() == 0
