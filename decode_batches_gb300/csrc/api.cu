@@ -54,6 +54,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 struct WsLayout {
   size_t logits, parts, ids, gates, masks, chunk_base, counts, offsets, perm, inv, segs, n_segs, h, h_s, y, y_s, x16;
   size_t touched, y32;  // the one-launch small-step layer: touched-expert list, fp32 expert outputs
+  size_t xq, xs;        // the block-scaled 4-bit gate/up: x as two e4m3 terms and their e8m0 scales
   size_t total;
   int max_segs;
 };
@@ -88,6 +89,9 @@ struct moe_plan {
   bool tiled = false, tiled_s = false;  // weights stored in the tile-contiguous layouts
   bool fp4_tiled = false;  // 4-bit routed weights in the tile-contiguous layout
   bool fp4_tc = false;     // ... and every scale in the fp16-exact range: tensor-core path allowed
+  // 4-bit gate/up on the block-scaled MMA (e2m1 weights x two e4m3 terms of x) instead of the
+  // dequantising kernel; env MOE_FP4_GATEUP=dequant selects the latter at plan creation
+  bool fp4_mx = true;
   // workspace (caller-owned)
   uint8_t* ws = nullptr;
   size_t ws_bytes = 0;
@@ -151,6 +155,8 @@ static WsLayout layout_for(const moe_plan* p, int T_max) {
   L.x16 = take(p->wdtype == MOE_W_MXFP4 ? T * p->d * 2 : 0);
   const size_t T8 = T < static_cast<size_t>(kLsTMax) ? T : static_cast<size_t>(kLsTMax);
   L.touched = take((p->E + 1) * sizeof(int32_t));
+  L.xq = take(p->wdtype == MOE_W_MXFP4 ? T * 2 * p->d : 0);
+  L.xs = take(p->wdtype == MOE_W_MXFP4 ? T * 2 * (p->d / 32) : 0);
   L.y32 = take(p->wdtype == MOE_W_BF16 ? T8 * (p->k + 1) * p->d * sizeof(float) : 0);
   L.total = o;
   return L;
@@ -310,6 +316,7 @@ extern "C" moe_plan* moe_plan_create(int E, int k, int d_model, int d_ff, int n_
   cudaGetDevice(&p->device);
   cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
   if (p->num_sms <= 0) p->num_sms = 1;
+  if (const char* env = getenv("MOE_FP4_GATEUP")) p->fp4_mx = strcmp(env, "dequant") != 0;
   if (const char* env = getenv("MOE_FORCE_PATH")) {
     if (!strcmp(env, "simt")) p->path = MOE_PATH_SIMT;
     else if (!strcmp(env, "tc")) p->path = MOE_PATH_TC;
@@ -352,12 +359,15 @@ extern "C" void moe_plan_destroy(moe_plan* p) {
   delete p;
 }
 
-// Plan-owned device words: [0] the error bits, [1] the small-step routing counter (0 between
+// Plan-owned device words: [0] the error bits, [1] the small-step routing counter, [2..3] and
+// [4..5] the unit hand-out words of the 4-bit gate/up and down kernels (all counters 0 between
 // launches), kept out of the caller's workspace, whose contents may change between calls.
+constexpr int kPlanWords = 6;
+constexpr int kSchedFp4GateUp = 2, kSchedFp4Down = 4;
 static moe_status ensure_err_word(moe_plan* p) {
   if (p->err) return MOE_OK;
-  MOE_CUDA_TRY(cudaMalloc(&p->err, 2 * sizeof(uint32_t)));
-  MOE_CUDA_TRY(cudaMemset(p->err, 0, 2 * sizeof(uint32_t)));
+  MOE_CUDA_TRY(cudaMalloc(&p->err, kPlanWords * sizeof(uint32_t)));
+  MOE_CUDA_TRY(cudaMemset(p->err, 0, kPlanWords * sizeof(uint32_t)));
   return MOE_OK;
 }
 
@@ -735,13 +745,22 @@ static moe_status run_experts(moe_plan* p, const uint16_t* x, int T, const int32
       // routed experts on the 4-bit kernels (fp16 activations), shared experts on the 16-bit
       // kernels restricted to their units
       uint16_t* x16 = ws_ptr<uint16_t>(p, p->L.x16);
-      if (!x16_ready)
-        LAUNCH(p, "x_to_f16", st, launch_x_to_f16(x, x16, static_cast<size_t>(T) * p->d, p->err, st));
-      LAUNCH(p, "fp4_gateup", st, launch_fp4_gateup(&p->maps, a, p->num_sms, st));
+      a.sched = p->err + kSchedFp4GateUp;
+      if (p->fp4_mx) {
+        a.xq = ws_ptr<uint8_t>(p, p->L.xq);
+        a.xs = ws_ptr<uint8_t>(p, p->L.xs);
+        LAUNCH(p, "x_to_mx", st, launch_x_to_mx(x, ws_ptr<uint8_t>(p, p->L.xq), ws_ptr<uint8_t>(p, p->L.xs), T, p->d, st));
+        LAUNCH(p, "mx_gateup", st, launch_mx_gateup(a, p->num_sms, st));
+      } else {
+        if (!x16_ready)
+          LAUNCH(p, "x_to_f16", st, launch_x_to_f16(x, x16, static_cast<size_t>(T) * p->d, p->err, st));
+        LAUNCH(p, "fp4_gateup", st, launch_fp4_gateup(&p->maps, a, p->num_sms, st));
+      }
       if (p->n_shared > 0 && !shared_forked) {
         const TcArgs sh = shared_args(p, a, T, true);
         LAUNCH(p, "tc_gateup_shared", st, launch_tc_gateup(&p->maps, sh, p->num_sms, st));
       }
+      a.sched = p->err + kSchedFp4Down;
       LAUNCH(p, "fp4_down", st, launch_fp4_down(&p->maps, a, p->num_sms, st));
       if (p->n_shared > 0 && !(shared_forked && kSharedDownBeside)) {
         if (shared_forked) MOE_CUDA_TRY(cudaStreamWaitEvent(st, p->ev_join, 0));
@@ -871,7 +890,7 @@ extern "C" moe_status moe_layer_forward(moe_plan* p, const void* x, int T, int n
   // that precedes the expert kernels (every thread of its grid takes a share); above, the top-k
   // kernel would carry T·d conversions on few threads, so x_to_f16 keeps its own launch.
   XConv xc;
-  if (tc && p->wdtype == MOE_W_MXFP4) {
+  if (tc && p->wdtype == MOE_W_MXFP4 && !p->fp4_mx) {
     xc.x = xb;
     xc.x16 = ws_ptr<uint16_t>(p, p->L.x16);
     xc.n8 = static_cast<size_t>(T) * p->d / 8;

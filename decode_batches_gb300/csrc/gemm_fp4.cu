@@ -72,6 +72,25 @@ struct Geo {
 
 MOE_DEVICE int pad16(int rows) { return rows <= 16 ? 16 : ((rows + 15) & ~15); }
 
+// Units are handed out at run time: each CTA's first unit is blockIdx.x, later ones come from a
+// per-launch counter (gridDim.x + the counter's old value), so a CTA that starts late -- its SM
+// still busy with another kernel -- does fewer units instead of holding the end of the launch.
+// Warp 0 fetches them and publishes each CTA's sequence in a ring of kUnitRing slots; every
+// other warp reads the same sequence from the ring.  An index >= the unit count ends it.
+constexpr int kUnitRing = 8;
+
+// Unit i of this CTA for a consumer warp (converged): waits for ring slot i, reads it and
+// releases the slot.  -1 when the wait gave up.
+MOE_DEVICE int ring_unit(const int32_t* ring, uint64_t* unit_full, uint64_t* unit_empty, uint32_t i,
+                         volatile int* abort_flag, uint32_t* err) {
+  const uint32_t s = i % kUnitRing;
+  if (!mbar_wait_warp(&unit_full[s], (i / kUnitRing) & 1u, abort_flag, err)) return -1;
+  const int u = ring[s];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&unit_empty[s]);
+  return u;
+}
+
 struct Unit {
   int expert, row_start, rows, tile;
 };
@@ -245,6 +264,11 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* unit_full = reinterpret_cast<uint64_t*>(tmem_slot + 2);
+  uint64_t* unit_empty = unit_full + kUnitRing;
+  int32_t* unit_ring = reinterpret_cast<int32_t*>(unit_empty + kUnitRing);
+  static_assert((2 * kRawSlots + 2 * kStages + 2 * kBStages + 5) * 8 + 8 + kUnitRing * 20 <= 1024,
+                "barriers, TMEM slot, abort flag and unit ring fit the 1 KB area");
   int32_t* tok_tab = reinterpret_cast<int32_t*>(ring_raw + kStagesRaw * kRawBytes + 1024);
   uint16_t* epi_stage = reinterpret_cast<uint16_t*>(ring_raw + kStagesRaw * kRawBytes + 1024 + kTokBytes);
 
@@ -269,6 +293,10 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
       mbar_init(&acc_empty[b], 4);
     }
     mbar_init(drain, 1);
+    for (int s = 0; s < kUnitRing; ++s) {
+      mbar_init(&unit_full[s], 1);                                    // warp 0 publishes
+      mbar_init(&unit_empty[s], static_cast<int>(blockDim.x / 32) - 1);  // every other warp reads
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -301,10 +329,28 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
 
   if (warp == 0) {
     // ---------------- raw 4-bit blocks: one bulk copy per stage (the blocks are adjacent) -----
+    // ---------------- also the unit hand-out: publishes this CTA's units in the ring ----------
     const uint64_t pol_w = l2_policy_evict_first();
     uint32_t p = 0;
     bool ok = true, waited = kGateUp;  // down: the first kRawSlots copies go out before the wait
-    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+    int u = static_cast<int>(blockIdx.x);
+    for (uint32_t i = 0; ok; ++i) {
+      const uint32_t rs = i % kUnitRing;
+      if (!(ok = mbar_wait_warp(&unit_empty[rs], ((i / kUnitRing) & 1u) ^ 1u, abort_flag, a.err))) break;
+      if (lane == 0) {
+        unit_ring[rs] = u;
+        mbar_arrive(&unit_full[rs]);
+      }
+      __syncwarp();
+      if (u >= total_units) break;
+      // the next unit's ticket is requested now and read once this unit's copies are out (the
+      // counter is only touched after the grid-dependency wait: it is reset by the previous launch)
+      uint32_t ticket = 0;
+      bool requested = false;
+      if (waited) {
+        if (lane == 0) ticket = atomicAdd(a.sched, 1u);
+        requested = true;
+      }
       const Unit un = waited ? decode_unit(u, a.segs, tiles) : decode_unit<true>(u, a.segs, tiles);
       const uint8_t* w0 = wq + (static_cast<size_t>(un.expert) * tiles + un.tile) * nsub * kFp4BlockBytes;
       for (int kp = 0; kp < npair; ++kp, ++p) {
@@ -323,6 +369,12 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
         }
         __syncwarp();
       }
+      if (!waited) {
+        pdl_wait();
+        waited = true;
+      }
+      if (!requested && lane == 0) ticket = atomicAdd(a.sched, 1u);
+      u = static_cast<int>(gridDim.x + __shfl_sync(0xffffffffu, ticket, 0));
     }
     if (!waited) pdl_wait();
   } else if (warp == 1) {
@@ -333,7 +385,13 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
     const uint32_t bfull_u32 = smem_u32(b_full), bempty_u32 = smem_u32(b_empty);
     uint32_t g = 0, j = 0;
     bool ok = true, ready = false;  // ready: stage g's A and B barriers already seen complete
-    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++j) {
+    for (uint32_t ui = 0; ok; ++ui, ++j) {
+      const int u = ring_unit(unit_ring, unit_full, unit_empty, ui, abort_flag, a.err);
+      if (u < 0) {
+        ok = false;
+        break;
+      }
+      if (u >= total_units) break;
       const Unit un = decode_unit(u, a.segs, tiles);
       const uint32_t N = static_cast<uint32_t>(pad16(un.rows));
       const uint32_t buf = j & 1u, use_acc = j >> 1;
@@ -387,7 +445,9 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
     // ---------------- epilogue (as in gemm_tc.cu) ----------------
     const int q = warp & 3;
     uint32_t j = 0;
-    for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x, ++j) {
+    for (uint32_t ui = 0; !*abort_flag; ++ui, ++j) {
+      const int u = ring_unit(unit_ring, unit_full, unit_empty, ui, abort_flag, a.err);
+      if (u < 0 || u >= total_units) break;
       const Unit un = decode_unit(u, a.segs, tiles);
       const uint32_t buf = j & 1u, use_acc = j >> 1;
       if (!mbar_wait(&acc_full[buf], use_acc & 1u, abort_flag, a.err)) break;
@@ -472,7 +532,13 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
     const uint32_t trow = tmem + (static_cast<uint32_t>(32 * q) << 16) + kAStart;
     uint32_t p = 0, uidx = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++uidx) {
+    for (uint32_t ui = 0; ok; ++ui, ++uidx) {
+      const int u = ring_unit(unit_ring, unit_full, unit_empty, ui, abort_flag, a.err);
+      if (u < 0) {
+        ok = false;
+        break;
+      }
+      if (u >= total_units) break;
       for (int kp = 0; kp < npair; ++kp, ++p) {
         const int kk = kRawPer * kp + static_cast<int>(set);
         const bool have = kk < nst;  // the last pair of an odd stage count has one stage
@@ -521,7 +587,13 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
       const uint64_t pol_act = l2_policy_evict_last();
       uint32_t g = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+      for (uint32_t ui = 0; ok; ++ui) {
+        const int u = ring_unit(unit_ring, unit_full, unit_empty, ui, abort_flag, a.err);
+        if (u < 0) {
+          ok = false;
+          break;
+        }
+        if (u >= total_units) break;
         const Unit un = decode_unit(u, a.segs, tiles);
         const int nbox = (pad16(un.rows) + 31) / 32;
         for (int kk = 0; kk < nst; ++kk, ++g) {
@@ -554,7 +626,13 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
     const uint64_t pol_x = l2_policy_evict_last();
     uint32_t g = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+    for (uint32_t ui = 0; ok; ++ui) {
+      const int u = ring_unit(unit_ring, unit_full, unit_empty, ui, abort_flag, a.err);
+      if (u < 0) {
+        ok = false;
+        break;
+      }
+      if (u >= total_units) break;
       const Unit un = decode_unit(u, a.segs, tiles);
       bool have_tok = false;
       for (int kk = 0; kk < nst; ++kk, ++g) {
@@ -592,6 +670,16 @@ __global__ void __launch_bounds__(Geo<kN>::threads(kGateUp), 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // The last CTA to leave resets the hand-out words for the next launch: every CTA's tickets
+  // were taken by its thread 0 before this point.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
+      a.sched[0] = 0u;
+      a.sched[1] = 0u;
+      __threadfence();
+    }
+  }
 }
 
 }  // namespace fq
@@ -607,6 +695,7 @@ static cudaError_t launch_fq_n(const TcMaps* maps, const TcArgs& a, int num_sms,
 // Steps of at most 64 tokens have segments of at most 64 rows: the deeper-ring geometry.
 template <bool kGateUp>
 static cudaError_t launch_fq(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st) {
+  if (!a.sched) return cudaErrorInvalidValue;  // the unit hand-out words are required
   if (a.T <= 64) return launch_fq_n<kGateUp, 64>(maps, a, num_sms, st);
   return launch_fq_n<kGateUp, 128>(maps, a, num_sms, st);
 }

@@ -142,6 +142,9 @@ struct TcArgs {
   const uint8_t* q_gu = nullptr;     // [E][f/64][d/64] blocks of kFp4BlockBytes
   const uint8_t* q_down = nullptr;   // [E][d/128][f/64] blocks
   const uint16_t* x16 = nullptr;     // fp16 copy of x (4-bit path's B operand)
+  const uint8_t* xq = nullptr;       // x as two e4m3 terms [T][2][d] (block-scaled gate/up's B operand)
+  const uint8_t* xs = nullptr;       // their e8m0 scales [T][2][d / 32]
+  uint32_t* sched = nullptr;         // persistent 4-bit kernels: the launch's unit hand-out words
   int routed = 1;                    // 0: the 16-bit kernels run the shared-expert units only
   const Seg* segs = nullptr;
   const int32_t* n_segs = nullptr;
@@ -166,12 +169,17 @@ cudaError_t launch_fp4_gateup(const TcMaps* maps, const TcArgs& a, int num_sms, 
 cudaError_t launch_fp4_down(const TcMaps* maps, const TcArgs& a, int num_sms, cudaStream_t st);
 // x16 = fp16(x), n elements (multiple of 8); out-of-range values clamp and flag MOE_DEVERR_RANGE.
 cudaError_t launch_x_to_f16(const uint16_t* x, uint16_t* x16, size_t n, uint32_t* err, cudaStream_t st);
+// ---- 4-bit gate/up on the block-scaled MMA (gemm_mx.cu) ------------------------------------------
+// xq [T][2][d] e4m3 (hi, lo) and xs [T][2][d / 32] e8m0 from x (bf16); requires d % 128 == 0.
+cudaError_t launch_x_to_mx(const uint16_t* x, uint8_t* xq, uint8_t* xs, int T, int d, cudaStream_t st);
+// h = SwiGLU of the routed units (a.q_gu tiled 4-bit weights, a.xq / a.xs, a.sched: zeroed words
+// [0] units handed out, [1] CTAs exited; the last CTA resets them).
+cudaError_t launch_mx_gateup(const TcArgs& a, int num_sms, cudaStream_t st);
 
 // ---- one-launch layer of a small step (layer_small.cu) ------------------------------------------
 constexpr int kLsTMax = 8;                  // tokens per step
-constexpr int kLsUnionBytes = 72 * 1024;    // x (bf16) and then h (fp16) of the step in shared memory
-constexpr int kLsMaxGroups = 512;           // d_model / 32
-constexpr int kLsSyncWords = 8 + kLsMaxGroups;
+constexpr int kLsUnionBytes = 76 * 1024;    // x (bf16) and then h (fp16) of the step in shared memory
+constexpr int kLsSyncWords = 8;            // launch-wide counters and flags
 struct LsArgs {
   const uint16_t* x = nullptr;
   const float* w_router = nullptr;

@@ -9,28 +9,33 @@
 // the weights through shared memory with bulk copies and multiplies on the CUDA cores (fp32
 // accumulation), the weight-streaming GEMV of the small-T regime.
 //
-// Persistent CTAs, one per SM.  Warp 0 is the producer: it takes tasks from two launch-wide
-// counters (gate/up tasks first, then down tasks) and streams each task's weight rows into a
-// ring of kSlots shared-memory slots (one 32 KB piece per slot; bulk copies of whole 128-byte
-// rows of the tile-contiguous weight layout).  Warps 1..16 consume the pieces in ring order.
+// Persistent CTAs, one per SM, 16 warps (warp 0 also routes the step).  Each warp streams
+// the weight rows it will itself multiply into its own ring of kSlots 2 KB shared-memory slots
+// with 16-byte cp.async (16 rows x 128 bytes of one K chunk of the tile-contiguous weight layout
+// per slot), kSlots - 1 pieces ahead of its arithmetic: no producer, no barrier on the data path,
+// and 16 x kSlots x 2 KB of every SM's weights in flight.  Tasks have equal sizes and are dealt
+// round-robin (gate/up task i to CTA i mod G, down task j to CTA G - 1 - j mod G, so CTAs with one
+// gate/up task more get one down task less); every warp of a CTA walks the same piece sequence.
 //
-//   router  every CTA computes the logits of experts blockIdx.x, blockIdx.x + gridDim.x, ...
-//           (full K, so no partial sums); the last CTA to finish selects the top k of each token
-//           (topk.cuh, the same selection as every other front end), groups the assignments
-//           (counts, offsets, the stable permutation) and raises the routed flag.
+//   router  every CTA computes the logits of experts blockIdx.x, blockIdx.x + G, ... (full K, so
+//           no partial sums).  Once every CTA's logits are written (a launch-wide counter), the
+//           warp 0 of every CTA selects the top k of each token (topk.cuh, the same
+//           selection as every other front end) and groups the assignments (counts, offsets, the
+//           stable permutation, the touched experts) into shared memory: the same result in every
+//           CTA, with no further hop.  Shared-expert gate/up tasks need no routing and stream
+//           from the start.
 //   gate/up task = one matrix (an expert, or the shared experts) x 8 features: its 16
 //           interleaved rows (8 gate, 8 up) over the whole K; consumer warp w takes K chunk w of
 //           each 16-chunk piece, the 16 warps' partial sums are added in warp order, SwiGLU, h
 //           rounded to fp16 (as the tensor-core path does) into the workspace.
 //   down    task = one matrix x 32 output features (32 rows of W_d over the whole K); after every
-//           gate/up task is done (a launch-wide counter) each CTA copies all of h into shared
-//           memory once; y (fp32) goes to the workspace.  The last down task of a 32-feature
-//           group (a per-group counter) combines those features of every token:
-//           out[t] = sum_j g[t,j] y[t,j] + y_s[t] in fp32, slot order, one rounding to bf16.
-// Shared-expert gate/up tasks come first and need no routing, so they stream while the router
-// finishes.  Every sum has a fixed order: the result does not depend on which CTA did what.
-// Every wait is bounded (1 s); an expired wait sets MOE_DEVERR_TIMEOUT and the CTA stops.  The
-// last CTA to leave resets the launch-wide counters for the next launch.
+//           CTA's gate/up tasks are done (a launch-wide counter, one addition per CTA) each CTA
+//           copies all of h into shared memory once; y (fp32) goes to the workspace.
+//   combine after every down task (one addition per CTA), out[t] = sum_j g[t,j] y[t,j] + y_s[t]
+//           in fp32, slot order, one rounding to bf16, 8-column chunks spread over the CTAs.
+// Every sum has a fixed order: the result does not depend on which CTA did what.  Every wait is
+// bounded (1 s); an expired wait sets MOE_DEVERR_TIMEOUT and the CTA stops.  The last CTA to leave
+// resets the launch-wide counters for the next launch.
 #include "common.cuh"
 #include "kernels.h"
 #include "topk.cuh"
@@ -39,34 +44,42 @@ namespace moe {
 namespace ls {
 
 constexpr int kConsumerWarps = 16;
-constexpr int kThreads = 32 * (1 + kConsumerWarps);
+constexpr int kThreads = 32 * kConsumerWarps;  // every warp computes; warp 0 also routes
 constexpr int kConsumers = 32 * kConsumerWarps;
-constexpr int kSlots = 4;
-constexpr int kSlotBytes = 32 * 1024;   // one piece: 16 rows x 16 K chunks (gate/up), 32 x 8 (down)
+constexpr int kSlots = 4;               // per compute warp
+constexpr int kSlotBytes = 2 * 1024;    // one warp's part of a piece: 16 rows x one 128-byte K chunk
 constexpr int kRowBytes = 128;          // 64 bf16 / fp16 elements of one row in one K chunk
 constexpr int kUnionBytes = kLsUnionBytes;
 constexpr int kMaxR = 256;              // T * k
 constexpr int kEMax = 1024;
-constexpr int kSmemBytes = kSlots * kSlotBytes + kUnionBytes + kConsumerWarps * 16 * kLsTMax * 4 /*red*/ +
-                           32 * kLsTMax * 4 /*sums*/ + (kEMax + 1) * 4 + 2 * kMaxR * 4 + (kEMax + 1) * 4 /*touched*/ +
-                           1024 /*barriers, descriptors, flags*/;
+constexpr int kSmemBytes = kConsumerWarps * kSlots * kSlotBytes + kUnionBytes + kConsumerWarps * 16 * kLsTMax * 4 /*red*/ +
+                           32 * kLsTMax * 4 /*sums*/ + (kEMax + 1) * 4 /*off*/ + 3 * kMaxR * 4 /*perm, gates, ids*/ +
+                           (kEMax + 1) * 4 /*touched*/ + 256 /*flags*/;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 enum Kind : int { kEnd = -1, kGuShared = 0, kGuRouted = 1, kDnShared = 2, kDnRouted = 3 };
 
+// A piece: K chunks [kc0, kc0 + nkc) of one task's rows (16 chunks of 16 rows for gate/up, 8
+// chunks of 32 rows for down), one chunk per compute warp (down: warps w and w + 8 take the two
+// 16-row halves of chunk w).
 struct Piece {
   int kind;      // Kind
   int m;         // routed expert (kinds 1, 3), else -1
   int group;     // 8-feature group (gate/up) or 32-feature group (down)
   int kc0, nkc;  // K chunks of this piece
   int last;      // 1 on the task's last piece
-  int pad0, pad1;
 };
 
-// Launch-wide words (plan-owned, zero between launches): see kLsSyncWords.
+// A compute warp's walk over its CTA's pieces (every warp of the CTA walks the same sequence).
+struct Walk {
+  int gu_i, dn_i;      // next gate/up / down task of this CTA
+  Piece cur;           // the piece the walk is on
+  int npieces, pc;     // pieces of the current task, index of the current one
+};
+
+// Launch-wide words (plan-owned, zero between launches; kLsSyncWords of them).
 struct Sync {
-  uint32_t gu_next, dn_next, router_done, routed, gu_done, exited, pad0, pad1;
-  uint32_t fg_done[1];  // [d / 32]
+  uint32_t router_done, gu_done, dn_done, exited, pad0, pad1, pad2, pad3;
 };
 
 struct Smem {
@@ -74,22 +87,20 @@ struct Smem {
   uint16_t* uni;  // x (bf16 [T][d]) during gate/up, then h (fp16) during down
   float* red;     // [kConsumerWarps][16][kLsTMax]
   float* sums;    // [32][kLsTMax]
-  int32_t* off;   // [E + 1]
-  int32_t* perm;  // [T k]
-  float* gates;   // [T k]
-  int32_t* touched;  // producer's copy: [E] (+ count in touched[E])
-  uint64_t* full;
-  uint64_t* empty;
-  Piece* desc;
-  volatile int* flags;  // [0] abort, [3] last router CTA, [4] routing published, [5] h complete,
-                        // [6] last task of a down group (each written by one thread, read after a barrier)
+  int32_t* off;      // [E + 1] offsets of the grouping (counts while it is built)
+  int32_t* perm;     // [T k]
+  float* gates;      // [T k]
+  int32_t* ids;      // [T k]
+  int32_t* touched;  // [E] touched experts, ascending; touched[E] = their number
+  volatile int* flags;  // [0] abort, [4] routing ready (set by warp 0), [5] h complete, [6] down complete
+                        // (each written by one thread and read after a barrier)
 };
 
 MOE_DEVICE Smem carve(uint8_t* base) {
   Smem s;
   uint8_t* p = base;
   s.ring = p;
-  p += kSlots * kSlotBytes;
+  p += kConsumerWarps * kSlots * kSlotBytes;
   s.uni = reinterpret_cast<uint16_t*>(p);
   p += kUnionBytes;
   s.red = reinterpret_cast<float*>(p);
@@ -102,16 +113,15 @@ MOE_DEVICE Smem carve(uint8_t* base) {
   p += kMaxR * 4;
   s.gates = reinterpret_cast<float*>(p);
   p += kMaxR * 4;
+  s.ids = reinterpret_cast<int32_t*>(p);
+  p += kMaxR * 4;
   s.touched = reinterpret_cast<int32_t*>(p);
   p += (kEMax + 1) * 4;
-  s.full = reinterpret_cast<uint64_t*>(p);
-  s.empty = s.full + kSlots;
-  s.desc = reinterpret_cast<Piece*>(s.empty + kSlots);
-  s.flags = reinterpret_cast<volatile int*>(s.desc + kSlots);
+  s.flags = reinterpret_cast<volatile int*>(p);
   return s;
 }
 
-// Named barrier of the consumer warps only (the producer never joins it).
+// Barrier of the CTA's compute warps (all of its warps).
 MOE_DEVICE void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
 
 // The same barrier returning the AND of every consumer thread's predicate.
@@ -168,9 +178,52 @@ MOE_DEVICE float dot8_f16(const uint4& w, const uint4& h, float acc) {
   return acc;
 }
 
-// Top k and gates of token t by one warp, from the logits the CTAs wrote (read through L2).
+// Warp-level tensor-core fragments (mma.sync m16n8k16, fp32 accumulate): 16 weight rows x 16 K
+// (A, row-major in the slot) times 16 K x 8 tokens (B, token rows of x or h).  At this T the MMA
+// replaces a few CUDA-core instructions per weight; the weights still stream once.
+MOE_DEVICE void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+MOE_DEVICE void ldsm_x2(uint32_t addr, uint32_t (&r)[2]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
+}
+template <bool kBf16>
+MOE_DEVICE void mma_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  if (kBf16)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// Bounded wait until the shared-memory flag is set (one thread).
+MOE_DEVICE bool wait_flag(volatile int* flag, volatile int* abort_flag, uint32_t* err) {
+  if (*flag) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (*flag) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > MOE_WAIT_LIMIT_NS) {
+      set_error(err, MOE_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// Top k and gates of token t by one warp, from the logits every CTA wrote (read through L2), into
+// the shared-memory ids / gates.
 template <int PL>
-MOE_DEVICE void select_token(const LsArgs& a, int t) {
+MOE_DEVICE void select_token(const LsArgs& a, int t, int32_t* ids, float* gates) {
   const int lane = threadIdx.x & 31;
   float v[PL];
 #pragma unroll
@@ -178,7 +231,60 @@ MOE_DEVICE void select_token(const LsArgs& a, int t) {
     const int e = lane + 32 * i;
     v[i] = e < a.E ? __ldcg(a.logits + static_cast<size_t>(t) * a.E + e) : 0.f;
   }
-  topk_select<PL>(v, t, a.E, a.k, a.ids, a.gates, a.err);
+  topk_select<PL>(v, t, a.E, a.k, ids, gates, a.err);
+}
+
+// The routing of the step by one warp (warp 0), into shared memory: ids and gates (top k of
+// every token), counts -> offsets, the stable permutation (rows of an expert ascend by assignment
+// index) and the touched experts in ascending order.  Returns the number of touched experts.
+MOE_DEVICE int route_step(const LsArgs& a, const Smem& S) {
+  const int lane = threadIdx.x & 31;
+  const int T = a.T, E = a.E, R = a.T * a.k;
+  for (int t = 0; t < T; ++t) {
+    if (E <= 256)
+      select_token<8>(a, t, S.ids, S.gates);
+    else if (E <= 512)
+      select_token<16>(a, t, S.ids, S.gates);
+    else
+      select_token<32>(a, t, S.ids, S.gates);
+  }
+  __syncwarp();
+  int32_t* cnt = S.off;  // counts first, then turned into offsets
+  for (int e = lane; e <= E; e += 32) cnt[e] = 0;
+  __syncwarp();
+  for (int q = lane; q < R; q += 32) atomicAdd(&cnt[S.ids[q]], 1);
+  __syncwarp();
+  int run = 0, trun = 0;
+  for (int e0 = 0; e0 < E; e0 += 32) {
+    const int e = e0 + lane;
+    const int c = e < E ? cnt[e] : 0;
+    const unsigned used = __ballot_sync(0xffffffffu, c > 0);
+    int inc = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int up = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += up;
+    }
+    if (e < E) {
+      if (c > 0) S.touched[trun + __popc(used & ((1u << lane) - 1u))] = e;
+      cnt[e] = run + inc - c;  // the exclusive offset
+    }
+    run += __shfl_sync(0xffffffffu, inc, 31);
+    trun += __popc(used);
+  }
+  if (lane == 0) {
+    cnt[E] = run;
+    S.touched[E] = trun;
+  }
+  __syncwarp();
+  for (int q = lane; q < R; q += 32) {
+    const int e = S.ids[q];
+    int r = cnt[e];
+    for (int q2 = 0; q2 < q; ++q2) r += S.ids[q2] == e ? 1 : 0;
+    S.perm[r] = q;
+  }
+  __syncwarp();
+  return trun;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) layer_small_kernel(const LsArgs a) {
@@ -188,136 +294,146 @@ __global__ void __launch_bounds__(kThreads, 1) layer_small_kernel(const LsArgs a
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = a.T, E = a.E, k = a.k, d = a.d, f = a.f;
   const int R = T * k;
+  const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
   const int fs_all = a.n_shared * a.f_s;                     // shared experts' hidden width, concatenated
-  const int n_gu_s = fs_all / 8;                             // shared gate/up tasks
+  const int n_gu_s = fs_all / 8;                             // shared gate/up tasks (they come first)
   const int nk_gu = d / 64;                                  // K chunks of a gate/up row
   const int n_dn_groups = d / 32;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kSlots; ++s) {
-      mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], kConsumerWarps);
-    }
+  if (threadIdx.x == 0)
     for (int i = 0; i < 8; ++i) S.flags[i] = 0;
-    fence_mbar_init();
-  }
   __syncthreads();
   pdl_wait();
   pdl_trigger();
   volatile int* abort_flag = S.flags;
 
-  if (warp == 0) {
-    // ================================ producer ================================
-    const uint64_t pol = l2_policy_evict_first();
-    int n_touched = -1;  // known once the routing is published
-    bool gu_phase = true, ok = true;
-    uint32_t slot = 0, phase = 0;
-    while (ok) {
-      // ---- next task ----
-      int kind = kEnd, m = -1, group = 0;
-      if (gu_phase) {
-        uint32_t id = 0;
-        if (lane == 0) id = atomicAdd(&sy->gu_next, 1u);
-        id = __shfl_sync(0xffffffffu, id, 0);
-        if (static_cast<int>(id) < n_gu_s) {
-          kind = kGuShared, group = static_cast<int>(id);
-        } else {
-          if (n_touched < 0) {
-            bool okw = true;
-            if (lane == 0) okw = wait_counter(&sy->routed, 1u, abort_flag, a.err);
-            if (!__shfl_sync(0xffffffffu, okw, 0)) break;
-            ld_acquire(&sy->routed);  // every lane's own acquire of the published routing
-            n_touched = static_cast<int>(__ldcg(a.n_touched));
-            for (int i = lane; i < n_touched; i += 32) S.touched[i] = __ldcg(a.touched + i);
-            __syncwarp();
-          }
-          const int v = static_cast<int>(id) - n_gu_s;
-          if (v < n_touched * (f / 8)) {
-            kind = kGuRouted, m = S.touched[v / (f / 8)], group = v % (f / 8);
-          } else {
-            gu_phase = false;
-          }
-        }
-      }
-      if (!gu_phase) {
-        if (n_touched < 0) {  // no gate/up task reached the routed ones: wait for the routing here
-          bool okw = true;
-          if (lane == 0) okw = wait_counter(&sy->routed, 1u, abort_flag, a.err);
-          if (!__shfl_sync(0xffffffffu, okw, 0)) break;
-          ld_acquire(&sy->routed);
-          n_touched = static_cast<int>(__ldcg(a.n_touched));
-          for (int i = lane; i < n_touched; i += 32) S.touched[i] = __ldcg(a.touched + i);
-          __syncwarp();
-        }
-        const int nmat = n_touched + (a.n_shared > 0 ? 1 : 0);
-        uint32_t id = 0;
-        if (lane == 0) id = atomicAdd(&sy->dn_next, 1u);
-        id = __shfl_sync(0xffffffffu, id, 0);
-        if (static_cast<int>(id) < nmat * n_dn_groups) {
-          group = static_cast<int>(id) / nmat;  // feature-group major: groups complete one by one
-          const int mi = static_cast<int>(id) % nmat;
-          if (a.n_shared > 0 && mi == 0) {
-            kind = kDnShared;
-          } else {
-            kind = kDnRouted, m = S.touched[mi - (a.n_shared > 0 ? 1 : 0)];
-          }
-        }
-      }
-      // ---- its pieces ----
-      const bool gu = kind == kGuShared || kind == kGuRouted;
-      int nk = 1, tiles = 1, tile = 0, r0 = 0, rows = 0;
-      const uint16_t* base = nullptr;
-      if (kind == kGuShared || kind == kGuRouted) {
-        tiles = (kind == kGuShared ? fs_all : f) / 64;
-        nk = nk_gu;
-        tile = group / 8, r0 = 16 * (group % 8), rows = 16;
-        base = kind == kGuShared ? a.w_gu_s : a.w_gu + static_cast<size_t>(m) * tiles * nk * kTileElems;
-      } else if (kind == kDnShared || kind == kDnRouted) {
-        tiles = d / 128;
-        nk = (kind == kDnShared ? fs_all : f) / 64;
-        tile = group / 4, r0 = 32 * (group % 4), rows = 32;
-        base = kind == kDnShared ? a.w_down_s : a.w_down + static_cast<size_t>(m) * tiles * nk * kTileElems;
-      }
-      const int per_piece = gu ? 16 : 8;  // K chunks per 32 KB piece
-      const int npieces = kind == kEnd ? 1 : (nk + per_piece - 1) / per_piece;
-      for (int pc = 0; pc < npieces; ++pc) {
-        if (!(ok = mbar_wait_warp(&S.empty[slot], phase ^ 1u, abort_flag, a.err))) break;
-        const int kc0 = pc * per_piece;
-        const int nkc = kind == kEnd ? 0 : min(per_piece, nk - kc0);
-        if (lane == 0) {
-          S.desc[slot] = Piece{kind, m, group, kc0, nkc, pc == npieces - 1 ? 1 : 0, 0, 0};
-          mbar_arrive_expect_tx(&S.full[slot], static_cast<uint32_t>(nkc * rows * kRowBytes));
-        }
-        __syncwarp();
-        if (lane < nkc) {  // one bulk copy per K chunk: `rows` consecutive 128-byte rows
-          const uint16_t* src = base + tile_chunk_offset(tile, kc0 + lane, tiles, nk) + static_cast<size_t>(r0) * 64;
-          bulk_load(S.ring + slot * kSlotBytes + lane * rows * kRowBytes, src, rows * kRowBytes, &S.full[slot], pol);
-        }
-        __syncwarp();
-        if (++slot == kSlots) slot = 0, phase ^= 1u;
-      }
-      if (kind == kEnd) break;
-    }
-    if (!ok || *abort_flag) {
-      // wake the consumers so that they see the abort (their waits also give up on the flag)
-      *abort_flag = 1;
-    }
-  } else {
-    // ================================ consumers ================================
-    const int cw = warp - 1;              // consumer warp 0..15
-    const int ct = threadIdx.x - 32;      // consumer thread 0..511
+  {
+    // ========================= compute warps =========================
+    const int cw = warp;                  // compute warp 0..15
+    const int ct = threadIdx.x;           // compute thread 0..511
     bool ok = true;
-    // ---- x into shared memory ----
+    uint8_t* ring = S.ring + cw * kSlots * kSlotBytes;
+    // ---- the CTA's piece sequence ----
+    int n_touched = -1;
+    auto routing_ready = [&](bool wait) -> bool {
+      if (n_touched >= 0) return true;
+      if (!wait && !S.flags[4]) return false;
+      bool okw = true;
+      if (lane == 0) okw = wait_flag(&S.flags[4], abort_flag, a.err);
+      okw = __shfl_sync(0xffffffffu, okw, 0);
+      __syncwarp();
+      if (!okw) return false;
+      n_touched = S.touched[E];
+      return true;
+    };
+    // piece state for issuing (ahead) and computing (behind)
+    struct Seq {
+      int gu_i, dn_i, pc, npieces, nk;
+      Piece cur;
+    };
+    auto start_task = [&](Seq& q, bool wait) -> int {  // 1: a task, 0: end, -1: routing not ready
+      if (q.gu_i < n_gu_s) {
+        q.cur = Piece{kGuShared, -1, q.gu_i, 0, 0, 0};
+        q.gu_i += G;
+      } else {
+        if (!routing_ready(wait)) return -1;
+        const int n_gu = n_gu_s + n_touched * (f / 8);
+        const int nmat = n_touched + (a.n_shared > 0 ? 1 : 0);
+        if (q.gu_i < n_gu) {
+          const int v = q.gu_i - n_gu_s;
+          q.cur = Piece{kGuRouted, S.touched[v / (f / 8)], v % (f / 8), 0, 0, 0};
+          q.gu_i += G;
+        } else if (q.dn_i < nmat * n_dn_groups) {
+          const int g = q.dn_i / nmat, mi = q.dn_i % nmat;  // feature-group major
+          if (a.n_shared > 0 && mi == 0)
+            q.cur = Piece{kDnShared, -1, g, 0, 0, 0};
+          else
+            q.cur = Piece{kDnRouted, S.touched[mi - (a.n_shared > 0 ? 1 : 0)], g, 0, 0, 0};
+          q.dn_i += G;
+        } else {
+          q.cur = Piece{kEnd, -1, 0, 0, 0, 1};
+          return 0;
+        }
+      }
+      const bool gu = q.cur.kind == kGuShared || q.cur.kind == kGuRouted;
+      q.nk = gu ? nk_gu : ((q.cur.kind == kDnShared ? fs_all : f) / 64);
+      const int per = gu ? 16 : 8;
+      q.npieces = (q.nk + per - 1) / per;
+      q.pc = 0;
+      q.cur.kc0 = 0;
+      q.cur.nkc = min(per, q.nk);
+      q.cur.last = q.npieces == 1 ? 1 : 0;
+      return 1;
+    };
+    // advance q to its next piece; 1: a piece, 0: end, -1: routing not ready (q unchanged)
+    auto advance = [&](Seq& q, bool wait) -> int {
+      if (q.cur.kind == kEnd) return 0;
+      if (q.pc >= 0 && q.pc + 1 < q.npieces) {
+        const int per = (q.cur.kind == kGuShared || q.cur.kind == kGuRouted) ? 16 : 8;
+        q.pc += 1;
+        q.cur.kc0 += per;
+        q.cur.nkc = min(per, q.nk - q.cur.kc0);
+        q.cur.last = q.pc + 1 == q.npieces ? 1 : 0;
+        return 1;
+      }
+      Seq save = q;
+      const int r = start_task(q, wait);
+      if (r < 0) q = save;
+      return r;
+    };
+    // this warp's 16 rows x 128 bytes of a piece into ring slot `sl` (nothing past the task's K)
+    auto issue = [&](const Piece& pc, int sl) {
+      const bool gu = pc.kind == kGuShared || pc.kind == kGuRouted;
+      const int kci = gu ? cw : (cw & 7);
+      if (pc.kind != kEnd && kci < pc.nkc) {
+        int nk, tiles, tile, r0;
+        const uint16_t* base;
+        if (gu) {
+          tiles = (pc.kind == kGuShared ? fs_all : f) / 64;
+          nk = nk_gu;
+          tile = pc.group / 8, r0 = 16 * (pc.group % 8);
+          base = pc.kind == kGuShared ? a.w_gu_s : a.w_gu + static_cast<size_t>(pc.m) * tiles * nk * kTileElems;
+        } else {
+          tiles = d / 128;
+          nk = (pc.kind == kDnShared ? fs_all : f) / 64;
+          tile = pc.group / 4, r0 = 32 * (pc.group % 4) + 16 * (cw >> 3);
+          base = pc.kind == kDnShared ? a.w_down_s : a.w_down + static_cast<size_t>(pc.m) * tiles * nk * kTileElems;
+        }
+        const uint16_t* src = base + tile_chunk_offset(tile, pc.kc0 + kci, tiles, nk) + static_cast<size_t>(r0) * 64;
+        const uint32_t dst = smem_u32(ring + sl * kSlotBytes);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {  // 16 rows x 8 chunks of 16 bytes: 4 per lane
+          const int v = lane + 32 * i;
+          cp_async_16(dst + v * 16, src + v * 8);
+        }
+      }
+      cp_async_commit();  // one group per piece, empty or not: the group count stays in step
+    };
+
+    // ---- x into shared memory, then the router logits of this CTA's experts (full K) ----
     {
       const uint4* src = reinterpret_cast<const uint4*>(a.x);
-      uint4* dst = reinterpret_cast<uint4*>(S.uni);
-      for (int i = ct; i < T * d / 8; i += kConsumers) dst[i] = __ldg(src + i);
+      for (int i = ct; i < T * d / 8; i += kConsumers) {  // rows padded by 16 bytes (ldmatrix banks)
+        const int t = i / (d / 8), c = i % (d / 8);
+        reinterpret_cast<uint4*>(S.uni + static_cast<size_t>(t) * (d + 8))[c] = __ldg(src + i);
+      }
+    }
+    // the first pieces that need no routing stream while the logits are computed
+    Seq iq{b, (G - 1) - b, -1, 0, 0, Piece{kGuShared, -1, 0, 0, 0, 0}};  // issue cursor
+    int issued = 0;
+    Piece pend[kSlots];  // the pieces in the ring, by slot
+    while (issued < kSlots) {
+      const int r = advance(iq, false);
+      if (r < 0) break;
+      pend[issued % kSlots] = iq.cur;
+      issue(iq.cur, issued % kSlots);
+      ++issued;
+      if (r == 0) break;
     }
     consumers_sync();
-    // ---- router logits of this CTA's experts (full K: no partial sums) ----
     {
       const int ks = d / kConsumerWarps;  // K slice per warp (a multiple of 8)
-      for (int e = blockIdx.x; e < E; e += gridDim.x) {
+      for (int e = b; e < E; e += G) {
         float acc[kLsTMax];
 #pragma unroll
         for (int t = 0; t < kLsTMax; ++t) acc[t] = 0.f;
@@ -327,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_small_kernel(const LsArgs a
 #pragma unroll
           for (int t = 0; t < kLsTMax; ++t) {
             if (t < T) {
-              const uint16_t* xr = S.uni + static_cast<size_t>(t) * d + cw * ks + i;
+              const uint16_t* xr = S.uni + static_cast<size_t>(t) * (d + 8) + cw * ks + i;
               const uint2 xv = *reinterpret_cast<const uint2*>(xr);
               acc[t] = fmaf(w4.x, __uint_as_float(xv.x << 16), acc[t]);
               acc[t] = fmaf(w4.y, __uint_as_float(xv.x & 0xFFFF0000u), acc[t]);
@@ -352,116 +468,67 @@ __global__ void __launch_bounds__(kThreads, 1) layer_small_kernel(const LsArgs a
         consumers_sync();
       }
     }
-    // ---- the last CTA to finish its logits routes and groups the step ----
     if (ct == 0) {
       __threadfence();
-      const uint32_t prev = atomicAdd(&sy->router_done, 1u);
-      S.flags[3] = prev == gridDim.x - 1 ? 1 : 0;
+      atomicAdd(&sy->router_done, 1u);
+    }
+    // ---- warp 0 routes the step once every CTA's logits are written (a launch-wide counter) ----
+    if (warp == 0) {
+      bool okw = true;
+      if (lane == 0) okw = wait_counter(&sy->router_done, static_cast<uint32_t>(G), abort_flag, a.err);
+      if (__shfl_sync(0xffffffffu, okw, 0)) {
+        ld_acquire(&sy->router_done);  // every lane's own acquire of the logits
+        route_step(a, S);
+        __threadfence_block();
+        if (lane == 0) S.flags[4] = 1;
+      }
     }
     consumers_sync();
-    if (S.flags[3]) {
-      __threadfence();
-      int32_t* cnt = S.off;  // counts first, then turned into offsets
-      for (int e = ct; e <= E; e += kConsumers) cnt[e] = 0;
-      consumers_sync();
-      for (int t = cw; t < T; t += kConsumerWarps) {  // one warp per token: logits -> top k + gates
-        if (E <= 256)
-          select_token<8>(a, t);
-        else if (E <= 512)
-          select_token<16>(a, t);
-        else
-          select_token<32>(a, t);
+    ok = S.flags[4] != 0;
+    // ---- the pieces: wait for this warp's copies of piece p, compute, refill the slot ----
+    while (ok && issued < kSlots && iq.cur.kind != kEnd) {  // the rest of the prologue
+      const int r = advance(iq, true);
+      if (r < 0) {
+        ok = false;
+        break;
       }
-      __threadfence_block();
-      consumers_sync();
-      // counts (order-independent), then offsets, the stable permutation and the touched list
-      for (int q = ct; q < R; q += kConsumers) {
-        S.perm[q] = a.ids[q];
-        atomicAdd(&cnt[a.ids[q]], 1);
-      }
-      consumers_sync();
-      if (cw == 0) {  // one warp scans E counts: exclusive offsets and touched-expert positions
-        int run = 0, trun = 0;
-        for (int e0 = 0; e0 < E; e0 += 32) {
-          const int e = e0 + lane;
-          const int c = e < E ? cnt[e] : 0;
-          int inc = c;
-          const unsigned used = __ballot_sync(0xffffffffu, c > 0);
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int up = __shfl_up_sync(0xffffffffu, inc, o);
-            if (lane >= o) inc += up;
-          }
-          if (e < E) {
-            a.counts[e] = c;
-            const int ex = run + inc - c;
-            if (c > 0) a.touched[trun + __popc(used & ((1u << lane) - 1u))] = e;
-            cnt[e] = ex;  // now the exclusive offset
-          }
-          run += __shfl_sync(0xffffffffu, inc, 31);
-          trun += __popc(used);
-        }
-        if (lane == 0) {
-          cnt[E] = run;
-          *a.n_touched = trun;
-        }
-      }
-      consumers_sync();
-      for (int e = ct; e <= E; e += kConsumers) a.offsets[e] = cnt[e];
-      for (int q = ct; q < R; q += kConsumers) {  // row of assignment q: stable by assignment index
-        const int e = S.perm[q];
-        int r = cnt[e];
-        for (int q2 = 0; q2 < q; ++q2) r += S.perm[q2] == e ? 1 : 0;
-        a.perm[r] = q;
-        a.inv[q] = r;
-      }
-      __threadfence();
-      consumers_sync();
-      if (ct == 0) {
-        __threadfence();
-        atomicExch(&sy->routed, 1u);
-      }
+      pend[issued % kSlots] = iq.cur;
+      issue(iq.cur, issued % kSlots);
+      ++issued;
     }
-    // ---- pieces ----
-    float acc[4][kLsTMax];
-    int tok[kLsTMax];  // per task: x row (gate/up) or h row (down) of each of its tokens
+    float dacc[4];     // this warp's 16 rows x 8 token columns (mma.sync accumulator fragment)
+    int brow = 0;      // per task: the x row (gate/up) or h row (down) of token lane % 8
     int n_tok = 0;
-    bool routing = false, h_loaded = false;
-    uint32_t slot = 0, phase = 0;
-    const int hr_ld = f, hs_ld = fs_all;                   // h row strides in shared memory
-    uint16_t* h_r = S.uni;                                 // routed h rows [R][f]
-    uint16_t* h_s = S.uni + static_cast<size_t>(R) * f;    // shared h rows [T][n_s f_s]
-    while (ok) {
-      // every consumer warp waits for the piece, then all agree (a warp whose wait gave up still
-      // reaches this barrier, so no consumer is left waiting at a later one)
-      ok = consumers_all(mbar_wait_warp(&S.full[slot], phase, abort_flag, a.err));
-      if (!ok) break;
-      const Piece pc = S.desc[slot];
+    bool h_loaded = false, gu_signalled = false;
+    uint32_t n_gu_mine = 0, n_dn_mine = 0;  // tasks this CTA finished
+    const int hr_ld = f + 8, hs_ld = fs_all + 8;           // h row strides in shared memory (padded)
+    uint16_t* h_r = S.uni;                                 // routed h rows [R][f + 8]
+    uint16_t* h_s = S.uni + static_cast<size_t>(R) * hr_ld;  // shared h rows [T][n_s f_s + 8]
+    for (int p = 0; ok && p < issued; ++p) {
+      const int sl = p % kSlots;
+      const Piece pc = pend[sl];
       if (pc.kind == kEnd) break;
+      // groups committed after piece p's: issued - p - 1 (at most kSlots - 1)
+      switch (issued - p - 1) {
+        case 0: cp_async_wait<0>(); break;
+        case 1: cp_async_wait<1>(); break;
+        case 2: cp_async_wait<2>(); break;
+        default: cp_async_wait<3>(); break;
+      }
+      __syncwarp();
       const bool gu = pc.kind == kGuShared || pc.kind == kGuRouted;
       const bool routed = pc.kind == kGuRouted || pc.kind == kDnRouted;
-      if ((routed || !gu) && !routing) {
-        // the routing: offsets, permutation and gates into shared memory (once)
-        if (ct == 0) S.flags[4] = wait_counter(&sy->routed, 1u, abort_flag, a.err) ? 1 : 0;
-        consumers_sync();
-        if (!S.flags[4]) {
-          ok = false;
-          break;
-        }
-        for (int e = ct; e <= E; e += kConsumers) S.off[e] = __ldcg(a.offsets + e);
-        for (int q = ct; q < R; q += kConsumers) {
-          S.perm[q] = __ldcg(a.perm + q);
-          S.gates[q] = __ldcg(a.gates + q);
-        }
-        consumers_sync();
-        routing = true;
-      }
       if (!gu && !h_loaded) {
-        // every gate/up task of the launch is done: all of h into shared memory (x is no longer needed)
+        // this CTA's gate/up tasks are done (pieces come in task order): count them, then wait for
+        // every CTA's; all of h then goes into shared memory (x is no longer needed)
+        consumers_sync();
         if (ct == 0) {
-          const uint32_t n_gu = static_cast<uint32_t>(n_gu_s + static_cast<int>(__ldcg(a.n_touched)) * (f / 8));
+          __threadfence();
+          atomicAdd(&sy->gu_done, n_gu_mine);
+          const uint32_t n_gu = static_cast<uint32_t>(n_gu_s + S.touched[E] * (f / 8));
           S.flags[5] = wait_counter(&sy->gu_done, n_gu, abort_flag, a.err) ? 1 : 0;
         }
+        gu_signalled = true;
         consumers_sync();
         if (!S.flags[5]) {
           ok = false;
@@ -469,76 +536,73 @@ __global__ void __launch_bounds__(kThreads, 1) layer_small_kernel(const LsArgs a
         }
         __threadfence();
         const uint4* src_r = reinterpret_cast<const uint4*>(a.h);
-        uint4* dst_r = reinterpret_cast<uint4*>(h_r);
-        for (int i = ct; i < R * f / 8; i += kConsumers) dst_r[i] = __ldcg(src_r + i);
+        for (int i = ct; i < R * f / 8; i += kConsumers)
+          reinterpret_cast<uint4*>(h_r + static_cast<size_t>(i / (f / 8)) * hr_ld)[i % (f / 8)] = __ldcg(src_r + i);
         const uint4* src_s = reinterpret_cast<const uint4*>(a.h_s);
-        uint4* dst_s = reinterpret_cast<uint4*>(h_s);
-        for (int i = ct; i < T * fs_all / 8; i += kConsumers) dst_s[i] = __ldcg(src_s + i);
+        for (int i = ct; i < T * fs_all / 8; i += kConsumers)
+          reinterpret_cast<uint4*>(h_s + static_cast<size_t>(i / (fs_all / 8)) * hs_ld)[i % (fs_all / 8)] =
+              __ldcg(src_s + i);
         consumers_sync();
         h_loaded = true;
       }
       if (pc.kc0 == 0) {  // a new task: its tokens, and fresh accumulators
+        const int n = lane & 7;  // the B row (token) whose address this lane gives ldmatrix
         if (routed) {
           const int r0 = S.off[pc.m];
           n_tok = S.off[pc.m + 1] - r0;
-#pragma unroll
-          for (int t = 0; t < kLsTMax; ++t) tok[t] = t < n_tok ? (gu ? S.perm[r0 + t] / k : r0 + t) : 0;
+          const int nn = n < n_tok ? n : 0;  // columns past the task's tokens repeat its first (ignored)
+          brow = gu ? S.perm[r0 + nn] / k : r0 + nn;
         } else {
           n_tok = T;
-#pragma unroll
-          for (int t = 0; t < kLsTMax; ++t) tok[t] = t;
+          brow = n < T ? n : 0;
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int t = 0; t < kLsTMax; ++t) acc[i][t] = 0.f;
+        dacc[0] = dacc[1] = dacc[2] = dacc[3] = 0.f;
       }
-      // ---- this warp's K chunk of the piece: 16 rows x 128 bytes, 4 vectors per lane ----
-      const int rows = gu ? 16 : 32;
+      // ---- this warp's K chunk of the piece: 16 rows x 64 K on the tensor core (4 x m16n8k16) ----
       const int kci = gu ? cw : (cw & 7);           // K chunk within the piece
-      const int rb = gu ? 0 : 16 * (cw >> 3);       // first row of this warp's 16
       if (kci < pc.nkc) {
         const int kc = pc.kc0 + kci;
-        const uint8_t* base = S.ring + slot * kSlotBytes + kci * rows * kRowBytes;
-        const int p = lane & 7;
+        const uint32_t slot_a = smem_u32(ring + sl * kSlotBytes);
+        // A: lane i gives row (i % 8) + 8 ((i / 8) % 2), K half (i / 16) of each 16-K step; the rows
+        // keep the weight layout's 16-byte chunk swizzle (chunk c of row r at c ^ (r % 8))
+        const int ar = (lane & 7) + 8 * ((lane >> 3) & 1), ah = lane >> 4;
+        // B: lane i (< 16) gives token row i % 8, K half i / 8
+        const uint16_t* bb = gu ? S.uni + static_cast<size_t>(brow) * (d + 8)
+                                : (pc.kind == kDnRouted ? h_r + static_cast<size_t>(brow) * hr_ld
+                                                        : h_s + static_cast<size_t>(brow) * hs_ld);
+        const uint32_t b_addr = smem_u32(bb + kc * 64 + 8 * ((lane >> 3) & 1));
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int rho = rb + (lane >> 3) + 4 * i;            // row within the task's rows
-          const uint4 w = *reinterpret_cast<const uint4*>(base + rho * kRowBytes + p * 16);
-          const int c = p ^ (rho & 7);                          // logical 8-element chunk of the row
-          const int k0 = kc * 64 + c * 8;
-          if (gu) {
-#pragma unroll
-            for (int t = 0; t < kLsTMax; ++t)
-              if (t < n_tok)
-                acc[i][t] = dot8_bf16(w, *reinterpret_cast<const uint4*>(S.uni + static_cast<size_t>(tok[t]) * d + k0),
-                                      acc[i][t]);
-          } else {
-            const uint16_t* hb = pc.kind == kDnRouted ? h_r : h_s;
-            const int ld = pc.kind == kDnRouted ? hr_ld : hs_ld;
-#pragma unroll
-            for (int t = 0; t < kLsTMax; ++t)
-              if (t < n_tok)
-                acc[i][t] = dot8_f16(w, *reinterpret_cast<const uint4*>(hb + static_cast<size_t>(tok[t]) * ld + k0),
-                                     acc[i][t]);
-          }
+        for (int ks = 0; ks < 4; ++ks) {
+          uint32_t af[4], bf[2];
+          ldsm_x4(slot_a + ar * kRowBytes + ((((2 * ks + ah) ^ (ar & 7))) << 4), af);
+          ldsm_x2(b_addr + ks * 32, bf);
+          if (gu)
+            mma_16816<true>(dacc, af, bf);
+          else
+            mma_16816<false>(dacc, af, bf);
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.empty[slot]);
-      if (++slot == kSlots) slot = 0, phase ^= 1u;
-      if (!pc.last) continue;
-      // ---- end of task: add the 8 lanes of each row, then the warps in K order ----
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int t = 0; t < kLsTMax; ++t) {
-          float v = acc[i][t];
-          v += __shfl_xor_sync(0xffffffffu, v, 1);
-          v += __shfl_xor_sync(0xffffffffu, v, 2);
-          v += __shfl_xor_sync(0xffffffffu, v, 4);
-          if ((lane & 7) == 0) S.red[(cw * 16 + (lane >> 3) + 4 * i) * kLsTMax + t] = v;
+      __syncwarp();  // every lane is done with the slot: refill it with the piece kSlots ahead
+      if (iq.cur.kind != kEnd) {
+        const int r = advance(iq, true);  // the routing is in shared memory by now: never waits
+        if (r < 0) {
+          ok = false;
+          break;
         }
+        pend[issued % kSlots] = iq.cur;
+        issue(iq.cur, issued % kSlots);
+        ++issued;
+      }
+      if (!pc.last) continue;
+      // ---- end of task: each warp's 16 x 8 fragment to shared memory, then the warps in K order ----
+      {
+        const int gr = lane >> 2, tc = 2 * (lane & 3);  // fragment row, token column
+        float* rw = S.red + cw * 16 * kLsTMax;
+        rw[gr * kLsTMax + tc] = dacc[0];
+        rw[gr * kLsTMax + tc + 1] = dacc[1];
+        rw[(gr + 8) * kLsTMax + tc] = dacc[2];
+        rw[(gr + 8) * kLsTMax + tc + 1] = dacc[3];
+      }
       consumers_sync();
       if (gu) {
         if (ct < 16 * kLsTMax) {  // (row, token): the 16 warps' partial sums in K order
@@ -563,11 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_small_kernel(const LsArgs a
               a.h_s[static_cast<size_t>(t) * fs_all + feat] = f32_to_f16_bits_rn(hv);
           }
         }
-        consumers_sync();
-        if (ct == 0) {
-          __threadfence();
-          atomicAdd(&sy->gu_done, 1u);
-        }
+        ++n_gu_mine;  // counted once, when this CTA is done with gate/up
       } else {
         if (ct < 32 * kLsTMax) {  // (row, token): the 8 warps of the row's half in K order
           const int rho = ct / kLsTMax, t = ct % kLsTMax;
@@ -582,45 +642,88 @@ __global__ void __launch_bounds__(kThreads, 1) layer_small_kernel(const LsArgs a
               a.ys32[static_cast<size_t>(t) * d + feat] = v;
           }
         }
-        consumers_sync();
-        if (ct == 0) {
-          __threadfence();
-          const uint32_t nmat = static_cast<uint32_t>(__ldcg(a.n_touched)) + (a.n_shared > 0 ? 1u : 0u);
-          S.flags[6] = atomicAdd(&sy->fg_done[pc.group], 1u) == nmat - 1 ? 1 : 0;
+        ++n_dn_mine;
+        consumers_sync();  // the next task's reduction reuses S.red
+      }
+      if (gu) consumers_sync();  // S.sums / S.red are reused by the next task
+    }
+    cp_async_wait<0>();  // nothing of this warp's is still in flight
+    ok = consumers_all(ok);
+    // ---- after the last piece: the gate/up count if not given yet, then the down count; once
+    // every CTA's down tasks are done, this CTA combines its share of the outputs ----
+    if (ok && !gu_signalled) {
+      if (ct == 0) {
+        __threadfence();
+        atomicAdd(&sy->gu_done, n_gu_mine);
+      }
+      gu_signalled = true;
+    }
+    if (ok) {
+      consumers_sync();  // this CTA's y writes precede its count
+      if (ct == 0) {
+        __threadfence();
+        if (n_dn_mine) atomicAdd(&sy->dn_done, n_dn_mine);
+        const uint32_t nmat = static_cast<uint32_t>(S.touched[E]) + (a.n_shared > 0 ? 1u : 0u);
+        S.flags[6] = wait_counter(&sy->dn_done, nmat * static_cast<uint32_t>(n_dn_groups), abort_flag, a.err) ? 1 : 0;
+      }
+      consumers_sync();
+      ok = S.flags[6] != 0;
+    }
+    if (ok) {
+      // out[t][8c .. 8c + 7] for the 8-column chunks c of this CTA: slot order, then the shared term
+      __threadfence();
+      const int n8 = T * d / 8;
+      for (int c = b + G * ct; c < n8; c += G * kConsumers) {
+        const int t = (8 * c) / d, j = (8 * c) % d;
+        float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int sl = 0; sl < k; ++sl) {
+          const float g = S.gates[t * k + sl];
+          const float4* yp = reinterpret_cast<const float4*>(a.y32 + static_cast<size_t>(t * k + sl) * d + j);
+          const float4 y0 = __ldcg(yp), y1 = __ldcg(yp + 1);
+          o[0] = fmaf(g, y0.x, o[0]), o[1] = fmaf(g, y0.y, o[1]), o[2] = fmaf(g, y0.z, o[2]), o[3] = fmaf(g, y0.w, o[3]);
+          o[4] = fmaf(g, y1.x, o[4]), o[5] = fmaf(g, y1.y, o[5]), o[6] = fmaf(g, y1.z, o[6]), o[7] = fmaf(g, y1.w, o[7]);
         }
-        consumers_sync();
-        if (S.flags[6]) {  // the group's last task: combine its 32 features of every token
-          __threadfence();
-          if (ct < 32 * T) {
-            const int t = ct / 32, j = 32 * pc.group + (ct & 31);
-            float o = 0.f;
-            for (int s = 0; s < k; ++s)
-              o = fmaf(S.gates[t * k + s], __ldcg(a.y32 + static_cast<size_t>(t * k + s) * d + j), o);
-            if (a.n_shared > 0) o += __ldcg(a.ys32 + static_cast<size_t>(t) * d + j);
-            a.out[static_cast<size_t>(t) * d + j] = f32_to_bf16_bits_rn(o);
-          }
+        if (a.n_shared > 0) {
+          const float4* sp = reinterpret_cast<const float4*>(a.ys32 + static_cast<size_t>(t) * d + j);
+          const float4 s0 = __ldcg(sp), s1 = __ldcg(sp + 1);
+          o[0] += s0.x, o[1] += s0.y, o[2] += s0.z, o[3] += s0.w;
+          o[4] += s1.x, o[5] += s1.y, o[6] += s1.z, o[7] += s1.w;
         }
+        uint4 v;
+        v.x = pack_bf16x2(o[0], o[1]);
+        v.y = pack_bf16x2(o[2], o[3]);
+        v.z = pack_bf16x2(o[4], o[5]);
+        v.w = pack_bf16x2(o[6], o[7]);
+        *reinterpret_cast<uint4*>(a.out + static_cast<size_t>(t) * d + j) = v;
       }
     }
     if (!ok) *abort_flag = 1;
   }
 
-  // ---- leave; the last CTA out resets the launch-wide words ----
+  // ---- leave: CTA 0 leaves the routing in the workspace; the last CTA out resets the counters ----
   __syncthreads();
+  if (b == 0 && S.flags[4]) {
+    for (int q = threadIdx.x; q < R; q += kThreads) {
+      a.ids[q] = S.ids[q];
+      a.gates[q] = S.gates[q];
+      a.perm[q] = S.perm[q];
+      a.inv[S.perm[q]] = q;
+    }
+    for (int e = threadIdx.x; e <= E; e += kThreads) {
+      a.offsets[e] = S.off[e];
+      if (e < E) a.counts[e] = S.off[e + 1] - S.off[e];
+    }
+  }
   if (threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(&sy->exited, 1u) == gridDim.x - 1) {
-      sy->gu_next = 0u;
-      sy->dn_next = 0u;
       sy->router_done = 0u;
-      sy->routed = 0u;
       sy->gu_done = 0u;
-      for (int g = 0; g < n_dn_groups; ++g) sy->fg_done[g] = 0u;
+      sy->dn_done = 0u;
       sy->exited = 0u;
       __threadfence();
     }
   }
-  abort_quiesce(abort_flag);
 }
 
 }  // namespace ls
@@ -628,9 +731,9 @@ __global__ void __launch_bounds__(kThreads, 1) layer_small_kernel(const LsArgs a
 bool layer_small_ok(int T, int E, int k, int d, int f, int n_shared, int f_s) {
   if (T < 1 || T > kLsTMax || E > ls::kEMax || T * k > ls::kMaxR) return false;
   if (d % 128 || f % 64 || (n_shared > 0 && (n_shared * f_s) % 64)) return false;
-  const size_t x_bytes = static_cast<size_t>(T) * d * 2;
-  const size_t h_bytes = (static_cast<size_t>(T) * k * f + static_cast<size_t>(T) * n_shared * f_s) * 2;
-  return x_bytes <= ls::kUnionBytes && h_bytes <= ls::kUnionBytes && d / 32 <= kLsMaxGroups;
+  const size_t x_bytes = static_cast<size_t>(T) * (d + 8) * 2;  // rows padded by 16 bytes
+  const size_t h_bytes = (static_cast<size_t>(T) * k * (f + 8) + static_cast<size_t>(T) * (n_shared * f_s + 8)) * 2;
+  return x_bytes <= ls::kUnionBytes && h_bytes <= ls::kUnionBytes;
 }
 
 cudaError_t launch_layer_small(const LsArgs& a, int num_sms, cudaStream_t st) {
