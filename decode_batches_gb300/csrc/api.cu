@@ -55,6 +55,7 @@ struct WsLayout {
   size_t logits, parts, ids, gates, masks, chunk_base, counts, offsets, perm, inv, segs, n_segs, h, h_s, y, y_s, x16;
   size_t touched, y32;  // the one-launch small-step layer: touched-expert list, fp32 expert outputs
   size_t xq, xs;        // the block-scaled 4-bit gate/up: x as two e4m3 terms and their e8m0 scales
+  size_t hq, hs;        // ... and down: h as two e4m3 terms and their e8m0 scales
   size_t total;
   int max_segs;
 };
@@ -89,9 +90,13 @@ struct moe_plan {
   bool tiled = false, tiled_s = false;  // weights stored in the tile-contiguous layouts
   bool fp4_tiled = false;  // 4-bit routed weights in the tile-contiguous layout
   bool fp4_tc = false;     // ... and every scale in the fp16-exact range: tensor-core path allowed
-  // 4-bit gate/up on the block-scaled MMA (e2m1 weights x two e4m3 terms of x) instead of the
-  // dequantising kernel; env MOE_FP4_GATEUP=dequant selects the latter at plan creation
-  bool fp4_mx = true;
+  // 4-bit gate/up and down on the block-scaled MMA (e2m1 weights x two e4m3 terms of x or h)
+  // instead of the dequantising kernels (the default, faster as measured); env MOE_FP4_GATEUP /
+  // MOE_FP4_DOWN = mx selects the former at plan creation
+  bool fp4_mx = false, fp4_mx_down = false;
+  // steps of at most 8 tokens with bf16 weights: the one-launch layer (layer_small.cu) instead of
+  // the routing launch + tensor-core GEMMs + combine; env MOE_SMALL_STEP = fused | multi
+  bool small_fused = false;
   // workspace (caller-owned)
   uint8_t* ws = nullptr;
   size_t ws_bytes = 0;
@@ -157,6 +162,8 @@ static WsLayout layout_for(const moe_plan* p, int T_max) {
   L.touched = take((p->E + 1) * sizeof(int32_t));
   L.xq = take(p->wdtype == MOE_W_MXFP4 ? T * 2 * p->d : 0);
   L.xs = take(p->wdtype == MOE_W_MXFP4 ? T * 2 * (p->d / 32) : 0);
+  L.hq = take(p->wdtype == MOE_W_MXFP4 ? R * 2 * p->f : 0);
+  L.hs = take(p->wdtype == MOE_W_MXFP4 ? R * 2 * static_cast<size_t>(mx_scale_bytes(p->f)) : 0);
   L.y32 = take(p->wdtype == MOE_W_BF16 ? T8 * (p->k + 1) * p->d * sizeof(float) : 0);
   L.total = o;
   return L;
@@ -183,7 +190,7 @@ static bool use_tc(const moe_plan* p) {
 // The one-launch small-step layer (layer_small.cu): MOE_PATH_AUTO at T <= 8 with bf16 routed
 // weights in the tensor-core tile layout (the kernel streams those tiles).
 static bool use_small_layer(const moe_plan* p, int T) {
-  return p->path == MOE_PATH_AUTO && p->wdtype == MOE_W_BF16 && tc_shape_ok(p) && p->tiled &&
+  return p->small_fused && p->path == MOE_PATH_AUTO && p->wdtype == MOE_W_BF16 && tc_shape_ok(p) && p->tiled &&
          (p->n_shared == 0 || p->tiled_s) && p->ls_sync &&
          layer_small_ok(T, p->E, p->k, p->d, p->f, p->n_shared, p->f_s);
 }
@@ -316,7 +323,9 @@ extern "C" moe_plan* moe_plan_create(int E, int k, int d_model, int d_ff, int n_
   cudaGetDevice(&p->device);
   cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
   if (p->num_sms <= 0) p->num_sms = 1;
-  if (const char* env = getenv("MOE_FP4_GATEUP")) p->fp4_mx = strcmp(env, "dequant") != 0;
+  if (const char* env = getenv("MOE_FP4_GATEUP")) p->fp4_mx = strcmp(env, "mx") == 0;
+  if (const char* env = getenv("MOE_FP4_DOWN")) p->fp4_mx_down = strcmp(env, "mx") == 0;
+  if (const char* env = getenv("MOE_SMALL_STEP")) p->small_fused = strcmp(env, "fused") == 0;
   if (const char* env = getenv("MOE_FORCE_PATH")) {
     if (!strcmp(env, "simt")) p->path = MOE_PATH_SIMT;
     else if (!strcmp(env, "tc")) p->path = MOE_PATH_TC;
@@ -761,7 +770,18 @@ static moe_status run_experts(moe_plan* p, const uint16_t* x, int T, const int32
         LAUNCH(p, "tc_gateup_shared", st, launch_tc_gateup(&p->maps, sh, p->num_sms, st));
       }
       a.sched = p->err + kSchedFp4Down;
-      LAUNCH(p, "fp4_down", st, launch_fp4_down(&p->maps, a, p->num_sms, st));
+      if (p->fp4_mx_down) {
+        const int R = T * p->k;
+        uint8_t* hq = ws_ptr<uint8_t>(p, p->L.hq);
+        uint8_t* hs = ws_ptr<uint8_t>(p, p->L.hs);
+        LAUNCH(p, "h_to_mx", st, launch_h_to_mx(ws_ptr<uint16_t>(p, p->L.h), hq, hs, R, p->f, st));
+        TcArgs ad = a;
+        ad.xq = hq;
+        ad.xs = hs;
+        LAUNCH(p, "mx_down", st, launch_mx_down(ad, p->num_sms, st));
+      } else {
+        LAUNCH(p, "fp4_down", st, launch_fp4_down(&p->maps, a, p->num_sms, st));
+      }
       if (p->n_shared > 0 && !(shared_forked && kSharedDownBeside)) {
         if (shared_forked) MOE_CUDA_TRY(cudaStreamWaitEvent(st, p->ev_join, 0));
         const TcArgs sh = shared_args(p, a, T, false);

@@ -41,14 +41,15 @@ namespace mx {
 constexpr int BM = 128;
 constexpr int kStageK = 128;                      // K per stage: two 64-K raw blocks
 constexpr int kRawBytes = 2 * kFp4BlockBytes;     // 8704 B per stage
-constexpr int kRawSlots = 4;
-constexpr int kStages = 5;                        // A / B / scale-factor ring
+constexpr int kRawSlots = 10;                    // 87 KB of 4-bit weights in flight per SM
+constexpr int kAStages = 3;                       // expanded A tiles + their scale factors (TMEM)
+constexpr int kStages = 5;                        // B (activation) ring
 constexpr int kTokMax = 64;                       // tokens per unit
 constexpr int kNMax = 2 * kTokMax;                // B rows (hi / lo) per unit
 constexpr int kABytes = BM * kStageK;             // 16 KB
 constexpr int kBBytes = kNMax * kStageK;          // 16 KB
 constexpr int kGatherPerSlot = 2;
-constexpr int kGatherWarps = kGatherPerSlot * kStages;   // 10
+constexpr int kGatherWarps = kGatherPerSlot * kStages;   // 10 (two per B slot)
 constexpr int kFirstGather = 6;
 constexpr int kFirstExpand = kFirstGather + kGatherWarps;  // 16: warps 16..23, two quartets
 constexpr int kExpandSets = 2;                             // quartet e takes the stages g % 2 == e
@@ -60,9 +61,9 @@ constexpr int kTmemCols = 512;
 constexpr int kEpiStageBytes = 16 * 32 * 2;       // per epilogue warp: 16 columns x 32 fp16 rows
 constexpr int kUnitRing = 8;
 constexpr int kTokBytes = kGatherWarps * kTokMax * 4;
-constexpr int kSmemBytes = kStages * (kABytes + kBBytes) + kStages * kNMax * 4 /*SFB words*/ +
+constexpr int kSmemBytes = kAStages * kABytes + kStages * kBBytes + kStages * kNMax * 4 /*SFB words*/ +
                            kRawSlots * kRawBytes + 1024 /*barriers*/ + 1024 /*align*/ + kTokBytes + 4 * kEpiStageBytes;
-static_assert(kSfBase + kStages * kSfCols <= kTmemCols, "TMEM columns");
+static_assert(kSfBase + kAStages * kSfCols <= kTmemCols, "TMEM columns");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 static_assert(kFirstExpand % 4 == 0, "expander warps cover lane quarters 0..3 in order");
 
@@ -88,6 +89,10 @@ MOE_DEVICE Unit decode_unit(int u, const Seg* segs, int tiles) {
 }
 
 MOE_DEVICE int pad16(int n) { return n <= 16 ? 16 : ((n + 15) & ~15); }
+
+// Scale bytes per quantised row of K elements: K / 32, rounded up to a multiple of 4 so that a
+// stage's four block scales are one aligned 32-bit word.
+__host__ __device__ inline int mx_scale_stride(int K) { return ((K / 32) + 3) & ~3; }
 
 // Instruction descriptor of kind::mxf8f6f4 with block scaling: A e2m1 (5), B e4m3 (0), K-major
 // both, N >> 3 at bit 17, e8m0 scale factors (bit 23), M >> 4 at bit 24, scale-factor byte ids of
@@ -143,19 +148,24 @@ MOE_DEVICE int ring_unit(const int32_t* ring, uint64_t* unit_full, uint64_t* uni
   return u;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) mx_gateup_kernel(const TcArgs a) {
+// kGateUp: gate/up (A = W_gate|W_up interleaved, B = x in two e4m3 terms gathered by token, SwiGLU
+// epilogue, h fp16); else down (A = W_down, B = h in two e4m3 terms, grouped rows, y fp16).  In both
+// the B operand comes as xq [rows][2][K] e4m3 and xs [rows][2][sstride] e8m0.
+template <bool kGateUp>
+__global__ void __launch_bounds__(kThreads, 1) mx_ffn_kernel(const TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ring_a = smem;                                        // kStages x 16 KB (1024-aligned)
-  uint8_t* ring_b = ring_a + kStages * kABytes;                  // kStages x 16 KB
+  uint8_t* ring_a = smem;                                        // kAStages x 16 KB (1024-aligned)
+  uint8_t* ring_b = ring_a + kAStages * kABytes;                 // kStages x 16 KB
   uint32_t* sfb_words = reinterpret_cast<uint32_t*>(ring_b + kStages * kBBytes);  // [kStages][kNMax]
   uint8_t* ring_raw = reinterpret_cast<uint8_t*>(sfb_words + kStages * kNMax);   // kRawSlots x 8704 B
   uint64_t* raw_full = reinterpret_cast<uint64_t*>(ring_raw + kRawSlots * kRawBytes);
   uint64_t* raw_empty = raw_full + kRawSlots;
   uint64_t* a_full = raw_empty + kRawSlots;
-  uint64_t* b_full = a_full + kStages;
-  uint64_t* st_empty = b_full + kStages;
-  uint64_t* acc_full = st_empty + kStages;
+  uint64_t* a_empty = a_full + kAStages;
+  uint64_t* b_full = a_empty + kAStages;
+  uint64_t* b_empty = b_full + kStages;
+  uint64_t* acc_full = b_empty + kStages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
   uint64_t* unit_full = drain + 1;
@@ -172,10 +182,13 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gateup_kernel(const TcArgs a) 
       mbar_init(&raw_full[s], 1);
       mbar_init(&raw_empty[s], 4);
     }
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kAStages; ++s) {
       mbar_init(&a_full[s], 4);
+      mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&b_full[s], kGatherPerSlot);
-      mbar_init(&st_empty[s], 1);
+      mbar_init(&b_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -200,9 +213,12 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gateup_kernel(const TcArgs a) 
   pdl_wait();
   pdl_trigger();
 
-  const int tiles = a.f / 64;
-  const int nblk = a.d / 64;                 // 64-K raw blocks per unit
-  const int nst = a.d / kStageK;             // stages per unit (d % 128 == 0)
+  const int K = kGateUp ? a.d : a.f;         // reduction length
+  const int tiles = kGateUp ? a.f / 64 : a.d / BM;
+  const int nblk = K / 64;                   // 64-K raw blocks per unit
+  const int nst = (nblk + 1) / 2;            // stages per unit (the last one may hold one block)
+  const int sstride = mx_scale_stride(K);    // scale bytes per B-source row
+  const uint8_t* wq = kGateUp ? a.q_gu : a.q_down;
   const int total_units = 2 * __ldcg(a.n_segs) * tiles;
 
   if (warp == 0) {
@@ -231,13 +247,14 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gateup_kernel(const TcArgs a) 
       if (u >= total_units) break;
       uint32_t ticket = 0;
       if (lane == 0) ticket = atomicAdd(a.sched, 1u);  // the next unit's, read after this unit's copies
-      const uint8_t* w0 = a.q_gu + (static_cast<size_t>(un.expert) * tiles + un.tile) * nblk * kFp4BlockBytes;
+      const uint8_t* w0 = wq + (static_cast<size_t>(un.expert) * tiles + un.tile) * nblk * kFp4BlockBytes;
       for (int kk = 0; kk < nst; ++kk, ++p) {
         const int slot = p % kRawSlots;
+        const uint32_t bytes = static_cast<uint32_t>(min(2, nblk - 2 * kk)) * kFp4BlockBytes;
         if (!(ok = mbar_wait_warp(&raw_empty[slot], ((p / kRawSlots) & 1u) ^ 1u, abort_flag, a.err))) break;
         if (elect_one()) {
-          mbar_arrive_expect_tx(&raw_full[slot], kRawBytes);
-          bulk_load(ring_raw + slot * kRawBytes, w0 + static_cast<size_t>(2 * kk) * kFp4BlockBytes, kRawBytes,
+          mbar_arrive_expect_tx(&raw_full[slot], bytes);
+          bulk_load(ring_raw + slot * kRawBytes, w0 + static_cast<size_t>(2 * kk) * kFp4BlockBytes, bytes,
                     &raw_full[slot], pol_w);
         }
         __syncwarp();
@@ -264,16 +281,18 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gateup_kernel(const TcArgs a) 
       tc_fence_after();
       const uint32_t d_tmem = tmem + buf * kAccCols;
       for (int kk = 0; kk < nst; ++kk, ++g) {
-        const uint32_t s = g % kStages;
-        if (!(ok = mbar_wait_warp(&a_full[s], (g / kStages) & 1u, abort_flag, a.err))) break;
+        // a_full of the stage implies its B rows (the expander waited for them before its arrival)
+        const uint32_t sa = g % kAStages, sb = g % kStages;
+        if (!(ok = mbar_wait_warp(&a_full[sa], (g / kAStages) & 1u, abort_flag, a.err))) break;
         tc_fence_after();
         if (elect_one()) {
-          const uint64_t ad = a_base + s * (kABytes >> 4), bd = b_base + s * (kBBytes >> 4);
-          const uint32_t sf = tmem + kSfBase + s * kSfCols;
-#pragma unroll
-          for (uint32_t kb = 0; kb < 4; ++kb)  // K = 32 per MMA: +32 bytes = +2 in the address field
+          const uint64_t ad = a_base + sa * (kABytes >> 4), bd = b_base + sb * (kBBytes >> 4);
+          const uint32_t sf = tmem + kSfBase + sa * kSfCols;
+          const uint32_t nkb = 2u * static_cast<uint32_t>(min(2, nblk - 2 * kk));  // 32-K blocks of the stage
+          for (uint32_t kb = 0; kb < nkb; ++kb)  // K = 32 per MMA: +32 bytes = +2 in the address field
             mma_mx(d_tmem, ad + 2 * kb, bd + 2 * kb, idesc_mx(N, kb), sf, sf + 4, (kk | kb) != 0);
-          mma_commit(&st_empty[s]);
+          mma_commit(&a_empty[sa]);
+          mma_commit(&b_empty[sb]);
         }
         __syncwarp();
       }
@@ -285,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gateup_kernel(const TcArgs a) 
     __syncwarp();
     mbar_wait_warp(drain, 0, nullptr, a.err);
   } else if (warp < 6) {
-    // ---------------- epilogue: hi + lo columns, SwiGLU, h (fp16) ----------------
+    // ---------------- epilogue: hi + lo columns; gate/up: SwiGLU, h (fp16); down: y (fp16) ----------------
     const int q = warp & 3;
     uint32_t j = 0;
     for (uint32_t ui = 0; !*abort_flag; ++ui, ++j) {
@@ -299,6 +318,39 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gateup_kernel(const TcArgs a) 
       const int L = 32 * q + lane;
       uint16_t* stg = epi_stage + (warp - 2) * (kEpiStageBytes / 2);
       bool sat = false;
+      if (!kGateUp) {
+        const int feat0 = un.tile * BM + 32 * q;
+        for (int c0 = 0; c0 < un.rows; c0 += 16) {
+          uint32_t rr[32];
+          tmem_ld_32x32b_x32(tbase + 2 * c0, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            float v = __uint_as_float(rr[2 * c]) + __uint_as_float(rr[2 * c + 1]);
+            if (c0 + c < un.rows && !(fabsf(v) <= kF16Max)) {
+              sat = true;
+              v = fminf(fmaxf(v, -kF16Max), kF16Max);
+            }
+            stg[c * 32 + lane] = f32_to_f16_bits_rn(v);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int pass = 0; pass < 2; ++pass) {  // column (16 pass + lane) / 4, features 8 (lane % 4) .. + 7
+            const int idx = 32 * pass + lane;
+            const int cl = idx >> 2, g4 = idx & 3;
+            if (c0 + cl < un.rows) {
+              const uint4 v = *reinterpret_cast<const uint4*>(stg + cl * 32 + 8 * g4);
+              *reinterpret_cast<uint4*>(a.y + static_cast<size_t>(un.row_start + c0 + cl) * a.d + feat0 + 8 * g4) = v;
+            }
+          }
+          __syncwarp();
+        }
+        if (__any_sync(0xffffffffu, sat) && lane == 0) set_error(a.err, MOE_DEVERR_RANGE);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        continue;
+      }
       const int w16 = L & 15;
       const bool is_gate = w16 < 8;
       const int fl = 8 * ((L >> 4) & 1) + (w16 & 7);
@@ -347,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gateup_kernel(const TcArgs a) 
     const int ch = lane & 7;
     const int rs0 = (lane >> 3) + 4 * half;  // B rows rs0 + 8 i
     const uint64_t pol_x = l2_policy_evict_last();
-    const int dbytes = a.d, sbytes = a.d / 32;  // per x-quant row: e4m3 bytes, scale bytes
+    const int dbytes = K;  // per B-source row: e4m3 bytes (scale bytes: sstride)
     uint32_t g = 0;
     bool ok = true;
     for (uint32_t ui = 0; ok; ++ui) {
@@ -363,21 +415,23 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gateup_kernel(const TcArgs a) 
       for (int kk = 0; kk < nst; ++kk, ++g) {
         const int s = g % kStages;
         if (s != slot) continue;
-        if (!have_tok) {
-          for (int n = lane; n < un.rows; n += 32) tok[n] = a.perm[un.row_start + n] / a.k;
+        if (!have_tok) {  // gate/up: the token of each row; down: the grouped row itself
+          for (int n = lane; n < un.rows; n += 32) tok[n] = kGateUp ? a.perm[un.row_start + n] / a.k : un.row_start + n;
           __syncwarp();
           have_tok = true;
         }
-        if (!(ok = mbar_wait_warp(&st_empty[s], ((g / kStages) & 1u) ^ 1u, abort_flag, a.err))) break;
+        const int nch = min(2, nblk - 2 * kk) * 4;  // 16-byte chunks of this stage's K
+        if (!(ok = mbar_wait_warp(&b_empty[s], ((g / kStages) & 1u) ^ 1u, abort_flag, a.err))) break;
         const uint32_t sb = smem_u32(ring_b + s * kBBytes);
-        for (int n = rs0; n < nrow; n += 8) {
-          const int qrow = 2 * tok[n >> 1] + (n & 1);  // row of the quantised x: token, hi / lo
-          const uint8_t* src = a.xq + static_cast<size_t>(qrow) * dbytes + kk * kStageK + ch * 16;
-          cp_async_16_hint(sb + n * 128 + ((ch ^ (n & 7)) << 4), src, pol_x);
-        }
+        if (ch < nch)
+          for (int n = rs0; n < nrow; n += 8) {
+            const int qrow = 2 * tok[n >> 1] + (n & 1);  // row of the quantised source: token / row, hi / lo
+            const uint8_t* src = a.xq + static_cast<size_t>(qrow) * dbytes + kk * kStageK + ch * 16;
+            cp_async_16_hint(sb + n * 128 + ((ch ^ (n & 7)) << 4), src, pol_x);
+          }
         for (int n = half * 64 + lane; n < min(nrow, half * 64 + 64); n += 32) {
           const int qrow = 2 * tok[n >> 1] + (n & 1);
-          cp_async_4(smem_u32(sfb_words + s * kNMax + n), a.xs + static_cast<size_t>(qrow) * sbytes + kk * 4);
+          cp_async_4(smem_u32(sfb_words + s * kNMax + n), a.xs + static_cast<size_t>(qrow) * sstride + kk * 4);
         }
         cp_async_commit();
         cp_async_wait<0>();
@@ -402,33 +456,37 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gateup_kernel(const TcArgs a) 
       if (u >= total_units) break;
       for (int kk = 0; kk < nst; ++kk, ++g, ++p) {
         if (g % kExpandSets != set) continue;
-        const int rsl = p % kRawSlots, s = g % kStages;
+        const int rsl = p % kRawSlots, s = g % kStages, sa = g % kAStages;
         if (!(ok = mbar_wait_warp(&raw_full[rsl], (p / kRawSlots) & 1u, abort_flag, a.err))) break;
         const uint8_t* raw = ring_raw + rsl * kRawBytes;
+        const int nb = min(2, nblk - 2 * kk);  // raw blocks in this stage
         uint4 c[2][2];
-        uint32_t sc[2];
+        uint32_t sc[2] = {0u, 0u};
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
-          const uint8_t* blk = raw + b * kFp4BlockBytes;
-          c[b][0] = *reinterpret_cast<const uint4*>(blk + r * 16);
-          c[b][1] = *reinterpret_cast<const uint4*>(blk + 2048 + r * 16);
-          sc[b] = *reinterpret_cast<const uint16_t*>(blk + 4096 + 2 * r);
+          if (b < nb) {
+            const uint8_t* blk = raw + b * kFp4BlockBytes;
+            c[b][0] = *reinterpret_cast<const uint4*>(blk + r * 16);
+            c[b][1] = *reinterpret_cast<const uint4*>(blk + 2048 + r * 16);
+            sc[b] = *reinterpret_cast<const uint16_t*>(blk + 4096 + 2 * r);
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&raw_empty[rsl]);
-        if (!(ok = mbar_wait_warp(&st_empty[s], ((g / kStages) & 1u) ^ 1u, abort_flag, a.err))) break;
+        if (!(ok = mbar_wait_warp(&a_empty[sa], ((g / kAStages) & 1u) ^ 1u, abort_flag, a.err))) break;
         // row r: logical 16-element chunk j = 4 b + 2 half + sub holds the codes in its low 8 bytes
-        uint8_t* arow = ring_a + s * kABytes + r * 128;
+        uint8_t* arow = ring_a + sa * kABytes + r * 128;
 #pragma unroll
         for (int b = 0; b < 2; ++b)
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
+            if (b >= nb) continue;  // a one-block stage: the MMAs read chunks 0..3 only
             const int j0 = 4 * b + 2 * hf;
             *reinterpret_cast<uint4*>(arow + ((j0 ^ (r & 7)) << 4)) = make_uint4(c[b][hf].x, c[b][hf].y, 0u, 0u);
             *reinterpret_cast<uint4*>(arow + (((j0 + 1) ^ (r & 7)) << 4)) = make_uint4(c[b][hf].z, c[b][hf].w, 0u, 0u);
           }
         fence_proxy_async_smem();
-        const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16) + kSfBase + s * kSfCols;
+        const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16) + kSfBase + sa * kSfCols;
         tmem_st_x1(tq + q, sc[0] | (sc[1] << 16));  // SFA: row r's four block scales, column + r / 32
         if (!(ok = mbar_wait_warp(&b_full[s], (g / kStages) & 1u, abort_flag, a.err))) break;
         const uint32_t* w = sfb_words + s * kNMax;  // SFB: B row n at column 4 + n / 32, lane n % 32
@@ -436,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) mx_gateup_kernel(const TcArgs a) 
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[s]);
+        if (lane == 0) mbar_arrive(&a_full[sa]);
       }
     }
   }
@@ -485,11 +543,12 @@ MOE_DEVICE float2 e4m3x2_to_f32(uint32_t v) {  // low byte -> .x
   return __half22float2(*reinterpret_cast<const __half2*>(&h2));
 }
 
-__global__ void __launch_bounds__(256) x_to_mx_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ xq,
-                                                     uint8_t* __restrict__ xs, int T, int d) {
+template <bool kBf16>
+__global__ void __launch_bounds__(256) to_mx_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ xq,
+                                                   uint8_t* __restrict__ xs, int T, int d) {
   pdl_wait();
   pdl_trigger();
-  const int nb = d / 32;
+  const int nb = d / 32, ss = mx_scale_stride(d);
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T * nb; i += gridDim.x * blockDim.x) {
     const int t = i / nb, j = i % nb;
     float v[32];
@@ -497,7 +556,10 @@ __global__ void __launch_bounds__(256) x_to_mx_kernel(const uint16_t* __restrict
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       float f8[8];
-      bf16x8_to_f32(src[q], f8);
+      if (kBf16)
+        bf16x8_to_f32(src[q], f8);
+      else
+        f16x8_to_f32(src[q], f8);
 #pragma unroll
       for (int e = 0; e < 8; ++e) v[8 * q + e] = f8[e];
     }
@@ -528,25 +590,39 @@ __global__ void __launch_bounds__(256) x_to_mx_kernel(const uint16_t* __restrict
     dh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
     dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-    xs[static_cast<size_t>(2 * t) * nb + j] = static_cast<uint8_t>(s1);
-    xs[static_cast<size_t>(2 * t + 1) * nb + j] = static_cast<uint8_t>(s2);
+    xs[static_cast<size_t>(2 * t) * ss + j] = static_cast<uint8_t>(s1);
+    xs[static_cast<size_t>(2 * t + 1) * ss + j] = static_cast<uint8_t>(s2);
   }
 }
 
 }  // namespace mx
 
-cudaError_t launch_mx_gateup(const TcArgs& a, int num_sms, cudaStream_t st) {
+template <bool kGateUp>
+static cudaError_t launch_mx(const TcArgs& a, int num_sms, cudaStream_t st) {
   if (!a.sched || !a.xq || !a.xs) return cudaErrorInvalidValue;
-  cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(mx::mx_gateup_kernel), mx::kSmemBytes);
+  auto kern = mx::mx_ffn_kernel<kGateUp>;
+  cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), mx::kSmemBytes);
   if (e != cudaSuccess) return e;
-  return launch_pdl(mx::mx_gateup_kernel, dim3(num_sms), dim3(mx::kThreads), mx::kSmemBytes, st, a);
+  return launch_pdl(kern, dim3(num_sms), dim3(mx::kThreads), mx::kSmemBytes, st, a);
 }
+
+cudaError_t launch_mx_gateup(const TcArgs& a, int num_sms, cudaStream_t st) { return launch_mx<true>(a, num_sms, st); }
+cudaError_t launch_mx_down(const TcArgs& a, int num_sms, cudaStream_t st) { return launch_mx<false>(a, num_sms, st); }
 
 cudaError_t launch_x_to_mx(const uint16_t* x, uint8_t* xq, uint8_t* xs, int T, int d, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
   const int n = T * (d / 32);
   const int blocks = (n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024;
-  return launch_pdl(mx::x_to_mx_kernel, dim3(blocks), dim3(256), 0, st, x, xq, xs, T, d);
+  return launch_pdl(mx::to_mx_kernel<true>, dim3(blocks), dim3(256), 0, st, x, xq, xs, T, d);
 }
+
+cudaError_t launch_h_to_mx(const uint16_t* h, uint8_t* hq, uint8_t* hs, int R, int f, cudaStream_t st) {
+  if (R <= 0) return cudaSuccess;
+  const int n = R * (f / 32);
+  const int blocks = (n + 255) / 256 < 2048 ? (n + 255) / 256 : 2048;
+  return launch_pdl(mx::to_mx_kernel<false>, dim3(blocks), dim3(256), 0, st, h, hq, hs, R, f);
+}
+
+int mx_scale_bytes(int K) { return mx::mx_scale_stride(K); }
 
 }  // namespace moe

@@ -175,6 +175,13 @@ cudaError_t launch_x_to_mx(const uint16_t* x, uint8_t* xq, uint8_t* xs, int T, i
 // h = SwiGLU of the routed units (a.q_gu tiled 4-bit weights, a.xq / a.xs, a.sched: zeroed words
 // [0] units handed out, [1] CTAs exited; the last CTA resets them).
 cudaError_t launch_mx_gateup(const TcArgs& a, int num_sms, cudaStream_t st);
+// y (fp16) of the routed units from W_down (a.q_down) and h in two e4m3 terms: a.xq = hq
+// [R][2][f], a.xs = hs [R][2][mx_scale_bytes(f)] (launch_h_to_mx), a.sched as above.
+cudaError_t launch_mx_down(const TcArgs& a, int num_sms, cudaStream_t st);
+// hq / hs from h (fp16 [R][f]); f % 64 == 0.
+cudaError_t launch_h_to_mx(const uint16_t* h, uint8_t* hq, uint8_t* hs, int R, int f, cudaStream_t st);
+// scale bytes per quantised row of K elements (K / 32 rounded up to a multiple of 4)
+int mx_scale_bytes(int K);
 
 // ---- one-launch layer of a small step (layer_small.cu) ------------------------------------------
 constexpr int kLsTMax = 8;                  // tokens per step

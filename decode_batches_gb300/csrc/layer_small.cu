@@ -9,13 +9,13 @@
 // the weights through shared memory with bulk copies and multiplies on the CUDA cores (fp32
 // accumulation), the weight-streaming GEMV of the small-T regime.
 //
-// Persistent CTAs, one per SM, 16 warps (warp 0 also routes the step).  Each warp streams
-// the weight rows it will itself multiply into its own ring of kSlots 2 KB shared-memory slots
-// with 16-byte cp.async (16 rows x 128 bytes of one K chunk of the tile-contiguous weight layout
-// per slot), kSlots - 1 pieces ahead of its arithmetic: no producer, no barrier on the data path,
-// and 16 x kSlots x 2 KB of every SM's weights in flight.  Tasks have equal sizes and are dealt
-// round-robin (gate/up task i to CTA i mod G, down task j to CTA G - 1 - j mod G, so CTAs with one
-// gate/up task more get one down task less); every warp of a CTA walks the same piece sequence.
+// Persistent CTAs, one per SM, 16 warps (warp 0 also routes the step).  Each warp streams the
+// weight rows of its own tasks into its own ring of kSlots 2 KB shared-memory slots with 16-byte
+// cp.async (16 rows x 128 bytes of one K chunk of the tile-contiguous weight layout per slot),
+// kSlots - 1 pieces ahead of its arithmetic: no producer, no barrier on the data path, and
+// 16 x kSlots x 2 KB of every SM's weights in flight.  Tasks have equal sizes and are dealt
+// round-robin over all the launch's warps (gate/up task i to warp i mod NW, down task j to warp
+// NW - 1 - j mod NW, so warps with one gate/up task more get one down task less).
 //
 //   router  every CTA computes the logits of experts blockIdx.x, blockIdx.x + G, ... (full K, so
 //           no partial sums).  Once every CTA's logits are written (a launch-wide counter), the
@@ -25,12 +25,13 @@
 //           CTA, with no further hop.  Shared-expert gate/up tasks need no routing and stream
 //           from the start.
 //   gate/up task = one matrix (an expert, or the shared experts) x 8 features: its 16
-//           interleaved rows (8 gate, 8 up) over the whole K; consumer warp w takes K chunk w of
-//           each 16-chunk piece, the 16 warps' partial sums are added in warp order, SwiGLU, h
-//           rounded to fp16 (as the tensor-core path does) into the workspace.
-//   down    task = one matrix x 32 output features (32 rows of W_d over the whole K); after every
-//           CTA's gate/up tasks are done (a launch-wide counter, one addition per CTA) each CTA
-//           copies all of h into shared memory once; y (fp32) goes to the workspace.
+//           interleaved rows (8 gate, 8 up) over the whole K, worked by ONE warp with mma.sync
+//           m16n8k16 fragments (16 rows x 8 token columns, fp32): the fragment puts gate row g and
+//           up row g + 8 in the same lane, so SwiGLU runs in registers and h (fp16, as the
+//           tensor-core path rounds it) goes straight to the workspace.
+//   down    task = one matrix x 16 output features over the whole K, one warp; after every CTA's
+//           gate/up tasks are done (a launch-wide counter, one addition per CTA) each CTA copies
+//           all of h into shared memory once; y (fp32) goes to the workspace.
 //   combine after every down task (one addition per CTA), out[t] = sum_j g[t,j] y[t,j] + y_s[t]
 //           in fp32, slot order, one rounding to bf16, 8-column chunks spread over the CTAs.
 // Every sum has a fixed order: the result does not depend on which CTA did what.  Every wait is
@@ -298,7 +299,6 @@ __global__ void __launch_bounds__(kThreads, 1) layer_small_kernel(const LsArgs a
   const int fs_all = a.n_shared * a.f_s;                     // shared experts' hidden width, concatenated
   const int n_gu_s = fs_all / 8;                             // shared gate/up tasks (they come first)
   const int nk_gu = d / 64;                                  // K chunks of a gate/up row
-  const int n_dn_groups = d / 32;
 
   if (threadIdx.x == 0)
     for (int i = 0; i < 8; ++i) S.flags[i] = 0;
@@ -308,98 +308,82 @@ __global__ void __launch_bounds__(kThreads, 1) layer_small_kernel(const LsArgs a
   volatile int* abort_flag = S.flags;
 
   {
-    // ========================= compute warps =========================
-    const int cw = warp;                  // compute warp 0..15
-    const int ct = threadIdx.x;           // compute thread 0..511
+    // ========================= every warp =========================
+    const int cw = warp;                  // warp 0..15
+    const int ct = threadIdx.x;           // thread 0..511
+    const int NW = G * kConsumerWarps, W = b * kConsumerWarps + cw;  // warps of the launch, this one
     bool ok = true;
     uint8_t* ring = S.ring + cw * kSlots * kSlotBytes;
-    // ---- the CTA's piece sequence ----
     int n_touched = -1;
-    auto routing_ready = [&](bool wait) -> bool {
-      if (n_touched >= 0) return true;
-      if (!wait && !S.flags[4]) return false;
-      bool okw = true;
-      if (lane == 0) okw = wait_flag(&S.flags[4], abort_flag, a.err);
-      okw = __shfl_sync(0xffffffffu, okw, 0);
-      __syncwarp();
-      if (!okw) return false;
-      n_touched = S.touched[E];
-      return true;
+    // A task is one matrix x 16 rows over its whole K: gate/up = the 16 interleaved rows of 8
+    // features (8 gate rows, then their 8 up rows), down = 16 output features.  Gate/up task i goes
+    // to warp i mod NW, down task j to warp NW - 1 - j mod NW; a piece is one 64-K chunk.
+    struct Task {
+      int kind, m, group, nk;
     };
-    // piece state for issuing (ahead) and computing (behind)
     struct Seq {
-      int gu_i, dn_i, pc, npieces, nk;
-      Piece cur;
+      int gu_i, dn_i, kc;  // next gate/up / down task of this warp, K chunk within the current one
+      Task cur;
     };
-    auto start_task = [&](Seq& q, bool wait) -> int {  // 1: a task, 0: end, -1: routing not ready
+    auto task_at = [&](Seq& q) -> int {  // the next task into q.cur; 1 a task, 0 none, -1 routing not ready
       if (q.gu_i < n_gu_s) {
-        q.cur = Piece{kGuShared, -1, q.gu_i, 0, 0, 0};
-        q.gu_i += G;
-      } else {
-        if (!routing_ready(wait)) return -1;
-        const int n_gu = n_gu_s + n_touched * (f / 8);
-        const int nmat = n_touched + (a.n_shared > 0 ? 1 : 0);
-        if (q.gu_i < n_gu) {
-          const int v = q.gu_i - n_gu_s;
-          q.cur = Piece{kGuRouted, S.touched[v / (f / 8)], v % (f / 8), 0, 0, 0};
-          q.gu_i += G;
-        } else if (q.dn_i < nmat * n_dn_groups) {
-          const int g = q.dn_i / nmat, mi = q.dn_i % nmat;  // feature-group major
-          if (a.n_shared > 0 && mi == 0)
-            q.cur = Piece{kDnShared, -1, g, 0, 0, 0};
-          else
-            q.cur = Piece{kDnRouted, S.touched[mi - (a.n_shared > 0 ? 1 : 0)], g, 0, 0, 0};
-          q.dn_i += G;
-        } else {
-          q.cur = Piece{kEnd, -1, 0, 0, 0, 1};
-          return 0;
-        }
+        q.cur = Task{kGuShared, -1, q.gu_i, nk_gu};
+        q.gu_i += NW;
+        return 1;
       }
-      const bool gu = q.cur.kind == kGuShared || q.cur.kind == kGuRouted;
-      q.nk = gu ? nk_gu : ((q.cur.kind == kDnShared ? fs_all : f) / 64);
-      const int per = gu ? 16 : 8;
-      q.npieces = (q.nk + per - 1) / per;
-      q.pc = 0;
-      q.cur.kc0 = 0;
-      q.cur.nkc = min(per, q.nk);
-      q.cur.last = q.npieces == 1 ? 1 : 0;
-      return 1;
+      if (n_touched < 0) return -1;
+      const int n_gu = n_gu_s + n_touched * (f / 8);
+      const int nmat = n_touched + (a.n_shared > 0 ? 1 : 0);
+      if (q.gu_i < n_gu) {
+        const int v = q.gu_i - n_gu_s;
+        q.cur = Task{kGuRouted, S.touched[v / (f / 8)], v % (f / 8), nk_gu};
+        q.gu_i += NW;
+        return 1;
+      }
+      if (q.dn_i < nmat * (d / 16)) {
+        const int g = q.dn_i / nmat, mi = q.dn_i % nmat;  // feature-group major
+        if (a.n_shared > 0 && mi == 0)
+          q.cur = Task{kDnShared, -1, g, fs_all / 64};
+        else
+          q.cur = Task{kDnRouted, S.touched[mi - (a.n_shared > 0 ? 1 : 0)], g, f / 64};
+        q.dn_i += NW;
+        return 1;
+      }
+      q.cur = Task{kEnd, -1, 0, 0};
+      return 0;
     };
-    // advance q to its next piece; 1: a piece, 0: end, -1: routing not ready (q unchanged)
-    auto advance = [&](Seq& q, bool wait) -> int {
+    // the piece after the current one: 1 a piece, 0 the end, -1 routing not ready (q unchanged)
+    auto advance = [&](Seq& q) -> int {
       if (q.cur.kind == kEnd) return 0;
-      if (q.pc >= 0 && q.pc + 1 < q.npieces) {
-        const int per = (q.cur.kind == kGuShared || q.cur.kind == kGuRouted) ? 16 : 8;
-        q.pc += 1;
-        q.cur.kc0 += per;
-        q.cur.nkc = min(per, q.nk - q.cur.kc0);
-        q.cur.last = q.pc + 1 == q.npieces ? 1 : 0;
+      if (q.kc >= 0 && q.kc + 1 < q.cur.nk) {
+        ++q.kc;
         return 1;
       }
       Seq save = q;
-      const int r = start_task(q, wait);
-      if (r < 0) q = save;
+      const int r = task_at(q);
+      if (r < 0) {
+        q = save;
+        return -1;
+      }
+      q.kc = 0;
       return r;
     };
-    // this warp's 16 rows x 128 bytes of a piece into ring slot `sl` (nothing past the task's K)
-    auto issue = [&](const Piece& pc, int sl) {
-      const bool gu = pc.kind == kGuShared || pc.kind == kGuRouted;
-      const int kci = gu ? cw : (cw & 7);
-      if (pc.kind != kEnd && kci < pc.nkc) {
-        int nk, tiles, tile, r0;
+    // this warp's piece (16 rows x one 128-byte K chunk) into ring slot `sl`
+    auto issue = [&](const Task& t, int kc, int sl) {
+      if (t.kind != kEnd) {
+        const bool gu = t.kind == kGuShared || t.kind == kGuRouted;
+        int tiles, nk = t.nk, tile, r0;
         const uint16_t* base;
         if (gu) {
-          tiles = (pc.kind == kGuShared ? fs_all : f) / 64;
-          nk = nk_gu;
-          tile = pc.group / 8, r0 = 16 * (pc.group % 8);
-          base = pc.kind == kGuShared ? a.w_gu_s : a.w_gu + static_cast<size_t>(pc.m) * tiles * nk * kTileElems;
+          tiles = (t.kind == kGuShared ? fs_all : f) / 64;
+          tile = t.group / 8, r0 = 16 * (t.group % 8);
+          base = t.kind == kGuShared ? a.w_gu_s : a.w_gu + static_cast<size_t>(t.m) * tiles * nk * kTileElems;
         } else {
           tiles = d / 128;
-          nk = (pc.kind == kDnShared ? fs_all : f) / 64;
-          tile = pc.group / 4, r0 = 32 * (pc.group % 4) + 16 * (cw >> 3);
-          base = pc.kind == kDnShared ? a.w_down_s : a.w_down + static_cast<size_t>(pc.m) * tiles * nk * kTileElems;
+          tile = t.group / 8, r0 = 16 * (t.group % 8);
+          base = t.kind == kDnShared ? a.w_down_s : a.w_down + static_cast<size_t>(t.m) * tiles * nk * kTileElems;
         }
-        const uint16_t* src = base + tile_chunk_offset(tile, pc.kc0 + kci, tiles, nk) + static_cast<size_t>(r0) * 64;
+        const uint16_t* src = base + tile_chunk_offset(tile, kc, tiles, nk) + static_cast<size_t>(r0) * 64;
         const uint32_t dst = smem_u32(ring + sl * kSlotBytes);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {  // 16 rows x 8 chunks of 16 bytes: 4 per lane
@@ -410,27 +394,31 @@ __global__ void __launch_bounds__(kThreads, 1) layer_small_kernel(const LsArgs a
       cp_async_commit();  // one group per piece, empty or not: the group count stays in step
     };
 
-    // ---- x into shared memory, then the router logits of this CTA's experts (full K) ----
+    // ---- x into shared memory (rows padded by 16 bytes against ldmatrix bank conflicts) ----
     {
       const uint4* src = reinterpret_cast<const uint4*>(a.x);
-      for (int i = ct; i < T * d / 8; i += kConsumers) {  // rows padded by 16 bytes (ldmatrix banks)
+      for (int i = ct; i < T * d / 8; i += kConsumers) {
         const int t = i / (d / 8), c = i % (d / 8);
         reinterpret_cast<uint4*>(S.uni + static_cast<size_t>(t) * (d + 8))[c] = __ldg(src + i);
       }
     }
     // the first pieces that need no routing stream while the logits are computed
-    Seq iq{b, (G - 1) - b, -1, 0, 0, Piece{kGuShared, -1, 0, 0, 0, 0}};  // issue cursor
+    Seq iq{W, (NW - 1) - W, -1, Task{kGuShared, -1, 0, 0}};  // issue cursor
     int issued = 0;
-    Piece pend[kSlots];  // the pieces in the ring, by slot
+    Task pend_t[kSlots];
+    int pend_kc[kSlots];
     while (issued < kSlots) {
-      const int r = advance(iq, false);
+      const int r = advance(iq);
       if (r < 0) break;
-      pend[issued % kSlots] = iq.cur;
-      issue(iq.cur, issued % kSlots);
+      pend_t[issued % kSlots] = iq.cur;
+      pend_kc[issued % kSlots] = iq.kc;
+      issue(iq.cur, iq.kc, issued % kSlots);
       ++issued;
       if (r == 0) break;
     }
+    if (ct == 0) S.flags[1] = S.flags[2] = 0;  // this CTA's finished gate/up and down tasks
     consumers_sync();
+    // ---- router logits of this CTA's experts (full K: no partial sums) ----
     {
       const int ks = d / kConsumerWarps;  // K slice per warp (a multiple of 8)
       for (int e = b; e < E; e += G) {
@@ -485,29 +473,59 @@ __global__ void __launch_bounds__(kThreads, 1) layer_small_kernel(const LsArgs a
     }
     consumers_sync();
     ok = S.flags[4] != 0;
+    if (ok) n_touched = S.touched[E];
     // ---- the pieces: wait for this warp's copies of piece p, compute, refill the slot ----
     while (ok && issued < kSlots && iq.cur.kind != kEnd) {  // the rest of the prologue
-      const int r = advance(iq, true);
-      if (r < 0) {
-        ok = false;
-        break;
-      }
-      pend[issued % kSlots] = iq.cur;
-      issue(iq.cur, issued % kSlots);
+      const int r = advance(iq);
+      pend_t[issued % kSlots] = iq.cur;
+      pend_kc[issued % kSlots] = iq.kc;
+      issue(iq.cur, iq.kc, issued % kSlots);
       ++issued;
+      if (r == 0) break;
     }
-    float dacc[4];     // this warp's 16 rows x 8 token columns (mma.sync accumulator fragment)
-    int brow = 0;      // per task: the x row (gate/up) or h row (down) of token lane % 8
-    int n_tok = 0;
-    bool h_loaded = false, gu_signalled = false;
-    uint32_t n_gu_mine = 0, n_dn_mine = 0;  // tasks this CTA finished
-    const int hr_ld = f + 8, hs_ld = fs_all + 8;           // h row strides in shared memory (padded)
-    uint16_t* h_r = S.uni;                                 // routed h rows [R][f + 8]
+    const int hr_ld = f + 8, hs_ld = fs_all + 8;             // h row strides in shared memory (padded)
+    uint16_t* h_r = S.uni;                                   // routed h rows [R][f + 8]
     uint16_t* h_s = S.uni + static_cast<size_t>(R) * hr_ld;  // shared h rows [T][n_s f_s + 8]
+    float dacc[4];      // this warp's 16 rows x 8 token columns (mma.sync accumulator fragment)
+    int brow = 0;       // per task: the x row (gate/up) or h row (down) of token lane % 8
+    int n_tok = 0, r0 = 0;
+    bool gu_done_here = false;  // this warp has passed the gate/up -> down barrier
+    // The gate/up -> down barrier of the CTA: every warp passes it exactly once, before its first
+    // down piece or at its end.  Then the CTA's gate/up count goes out, every CTA's is awaited, and
+    // all of h comes into shared memory (x is no longer needed).
+    auto gate_up_barrier = [&]() -> bool {
+      gu_done_here = true;
+      consumers_sync();
+      if (ct == 0) {
+        __threadfence();
+        atomicAdd(&sy->gu_done, static_cast<uint32_t>(S.flags[1]));
+        const uint32_t n_gu = static_cast<uint32_t>(n_gu_s + n_touched * (f / 8));
+        S.flags[5] = wait_counter(&sy->gu_done, n_gu, abort_flag, a.err) ? 1 : 0;
+      }
+      consumers_sync();
+      if (!S.flags[5]) return false;
+      __threadfence();
+      const uint4* src_r = reinterpret_cast<const uint4*>(a.h);
+      for (int i = ct; i < R * f / 8; i += kConsumers)
+        reinterpret_cast<uint4*>(h_r + static_cast<size_t>(i / (f / 8)) * hr_ld)[i % (f / 8)] = __ldcg(src_r + i);
+      const uint4* src_s = reinterpret_cast<const uint4*>(a.h_s);
+      for (int i = ct; i < T * fs_all / 8; i += kConsumers)
+        reinterpret_cast<uint4*>(h_s + static_cast<size_t>(i / (fs_all / 8)) * hs_ld)[i % (fs_all / 8)] =
+            __ldcg(src_s + i);
+      consumers_sync();
+      return true;
+    };
     for (int p = 0; ok && p < issued; ++p) {
       const int sl = p % kSlots;
-      const Piece pc = pend[sl];
-      if (pc.kind == kEnd) break;
+      const Task t = pend_t[sl];
+      const int kc = pend_kc[sl];
+      if (t.kind == kEnd) break;
+      const bool gu = t.kind == kGuShared || t.kind == kGuRouted;
+      const bool routed = t.kind == kGuRouted || t.kind == kDnRouted;
+      if (!gu && !gu_done_here) {
+        ok = gate_up_barrier();
+        if (!ok) break;
+      }
       // groups committed after piece p's: issued - p - 1 (at most kSlots - 1)
       switch (issued - p - 1) {
         case 0: cp_async_wait<0>(); break;
@@ -516,40 +534,11 @@ __global__ void __launch_bounds__(kThreads, 1) layer_small_kernel(const LsArgs a
         default: cp_async_wait<3>(); break;
       }
       __syncwarp();
-      const bool gu = pc.kind == kGuShared || pc.kind == kGuRouted;
-      const bool routed = pc.kind == kGuRouted || pc.kind == kDnRouted;
-      if (!gu && !h_loaded) {
-        // this CTA's gate/up tasks are done (pieces come in task order): count them, then wait for
-        // every CTA's; all of h then goes into shared memory (x is no longer needed)
-        consumers_sync();
-        if (ct == 0) {
-          __threadfence();
-          atomicAdd(&sy->gu_done, n_gu_mine);
-          const uint32_t n_gu = static_cast<uint32_t>(n_gu_s + S.touched[E] * (f / 8));
-          S.flags[5] = wait_counter(&sy->gu_done, n_gu, abort_flag, a.err) ? 1 : 0;
-        }
-        gu_signalled = true;
-        consumers_sync();
-        if (!S.flags[5]) {
-          ok = false;
-          break;
-        }
-        __threadfence();
-        const uint4* src_r = reinterpret_cast<const uint4*>(a.h);
-        for (int i = ct; i < R * f / 8; i += kConsumers)
-          reinterpret_cast<uint4*>(h_r + static_cast<size_t>(i / (f / 8)) * hr_ld)[i % (f / 8)] = __ldcg(src_r + i);
-        const uint4* src_s = reinterpret_cast<const uint4*>(a.h_s);
-        for (int i = ct; i < T * fs_all / 8; i += kConsumers)
-          reinterpret_cast<uint4*>(h_s + static_cast<size_t>(i / (fs_all / 8)) * hs_ld)[i % (fs_all / 8)] =
-              __ldcg(src_s + i);
-        consumers_sync();
-        h_loaded = true;
-      }
-      if (pc.kc0 == 0) {  // a new task: its tokens, and fresh accumulators
+      if (kc == 0) {  // a new task: its tokens, and a fresh accumulator
         const int n = lane & 7;  // the B row (token) whose address this lane gives ldmatrix
         if (routed) {
-          const int r0 = S.off[pc.m];
-          n_tok = S.off[pc.m + 1] - r0;
+          r0 = S.off[t.m];
+          n_tok = S.off[t.m + 1] - r0;
           const int nn = n < n_tok ? n : 0;  // columns past the task's tokens repeat its first (ignored)
           brow = gu ? S.perm[r0 + nn] / k : r0 + nn;
         } else {
@@ -558,18 +547,16 @@ __global__ void __launch_bounds__(kThreads, 1) layer_small_kernel(const LsArgs a
         }
         dacc[0] = dacc[1] = dacc[2] = dacc[3] = 0.f;
       }
-      // ---- this warp's K chunk of the piece: 16 rows x 64 K on the tensor core (4 x m16n8k16) ----
-      const int kci = gu ? cw : (cw & 7);           // K chunk within the piece
-      if (kci < pc.nkc) {
-        const int kc = pc.kc0 + kci;
+      // ---- 16 rows x 64 K on the tensor core (4 x m16n8k16) ----
+      {
         const uint32_t slot_a = smem_u32(ring + sl * kSlotBytes);
         // A: lane i gives row (i % 8) + 8 ((i / 8) % 2), K half (i / 16) of each 16-K step; the rows
         // keep the weight layout's 16-byte chunk swizzle (chunk c of row r at c ^ (r % 8))
         const int ar = (lane & 7) + 8 * ((lane >> 3) & 1), ah = lane >> 4;
         // B: lane i (< 16) gives token row i % 8, K half i / 8
         const uint16_t* bb = gu ? S.uni + static_cast<size_t>(brow) * (d + 8)
-                                : (pc.kind == kDnRouted ? h_r + static_cast<size_t>(brow) * hr_ld
-                                                        : h_s + static_cast<size_t>(brow) * hs_ld);
+                                : (t.kind == kDnRouted ? h_r + static_cast<size_t>(brow) * hr_ld
+                                                       : h_s + static_cast<size_t>(brow) * hs_ld);
         const uint32_t b_addr = smem_u32(bb + kc * 64 + 8 * ((lane >> 3) & 1));
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
@@ -584,87 +571,64 @@ __global__ void __launch_bounds__(kThreads, 1) layer_small_kernel(const LsArgs a
       }
       __syncwarp();  // every lane is done with the slot: refill it with the piece kSlots ahead
       if (iq.cur.kind != kEnd) {
-        const int r = advance(iq, true);  // the routing is in shared memory by now: never waits
-        if (r < 0) {
-          ok = false;
-          break;
-        }
-        pend[issued % kSlots] = iq.cur;
-        issue(iq.cur, issued % kSlots);
+        advance(iq);  // the routing is known by now: never blocks
+        pend_t[issued % kSlots] = iq.cur;
+        pend_kc[issued % kSlots] = iq.kc;
+        issue(iq.cur, iq.kc, issued % kSlots);
         ++issued;
       }
-      if (!pc.last) continue;
-      // ---- end of task: each warp's 16 x 8 fragment to shared memory, then the warps in K order ----
-      {
-        const int gr = lane >> 2, tc = 2 * (lane & 3);  // fragment row, token column
-        float* rw = S.red + cw * 16 * kLsTMax;
-        rw[gr * kLsTMax + tc] = dacc[0];
-        rw[gr * kLsTMax + tc + 1] = dacc[1];
-        rw[(gr + 8) * kLsTMax + tc] = dacc[2];
-        rw[(gr + 8) * kLsTMax + tc + 1] = dacc[3];
-      }
-      consumers_sync();
+      if (kc + 1 < t.nk) continue;
+      // ---- end of the task, inside the warp: lane (g, c) holds rows g and g + 8, tokens 2c, 2c + 1 ----
+      const int g = lane >> 2, tc = 2 * (lane & 3);
       if (gu) {
-        if (ct < 16 * kLsTMax) {  // (row, token): the 16 warps' partial sums in K order
-          const int rho = ct / kLsTMax, t = ct % kLsTMax;
-          float v = 0.f;
-          for (int w = 0; w < kConsumerWarps; ++w) v += S.red[(w * 16 + rho) * kLsTMax + t];
-          S.sums[rho * kLsTMax + t] = v;
-        }
-        consumers_sync();
-        if (ct < 8 * kLsTMax) {  // rows i (gate) and 8 + i (up) of feature 8 group + i
-          const int i = ct / kLsTMax, t = ct % kLsTMax;
-          if (t < n_tok) {
-            float hv = swiglu(S.sums[i * kLsTMax + t], S.sums[(8 + i) * kLsTMax + t]);
+        // rows g (gate) and g + 8 (up) of feature 8 group + g: SwiGLU in registers, h to fp16
+        const int feat = 8 * t.group + g;
+        bool sat = false;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int tk = tc + c;
+          if (tk < n_tok) {
+            float hv = swiglu(dacc[c], dacc[2 + c]);
             if (!(fabsf(hv) <= kF16Max)) {
-              set_error(a.err, MOE_DEVERR_RANGE);
+              sat = true;
               hv = fminf(fmaxf(hv, -kF16Max), kF16Max);
             }
-            const int feat = 8 * pc.group + i;
-            if (pc.kind == kGuRouted)
-              a.h[static_cast<size_t>(S.off[pc.m] + t) * f + feat] = f32_to_f16_bits_rn(hv);
+            if (t.kind == kGuRouted)
+              a.h[static_cast<size_t>(r0 + tk) * f + feat] = f32_to_f16_bits_rn(hv);
             else
-              a.h_s[static_cast<size_t>(t) * fs_all + feat] = f32_to_f16_bits_rn(hv);
+              a.h_s[static_cast<size_t>(tk) * fs_all + feat] = f32_to_f16_bits_rn(hv);
           }
         }
-        ++n_gu_mine;  // counted once, when this CTA is done with gate/up
+        if (sat) set_error(a.err, MOE_DEVERR_RANGE);
+        __syncwarp();
+        if (lane == 0) atomicAdd(const_cast<int*>(&S.flags[1]), 1);
       } else {
-        if (ct < 32 * kLsTMax) {  // (row, token): the 8 warps of the row's half in K order
-          const int rho = ct / kLsTMax, t = ct % kLsTMax;
-          const int half = rho >> 4;
-          float v = 0.f;
-          for (int w = 0; w < 8; ++w) v += S.red[((8 * half + w) * 16 + (rho & 15)) * kLsTMax + t];
-          if (t < n_tok) {
-            const int feat = 32 * pc.group + rho;
-            if (pc.kind == kDnRouted)
-              a.y32[static_cast<size_t>(S.perm[S.off[pc.m] + t]) * d + feat] = v;
-            else
-              a.ys32[static_cast<size_t>(t) * d + feat] = v;
+        // output features 16 group + g and + g + 8 of tokens tc, tc + 1
+        const int feat = 16 * t.group + g;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int tk = tc + c;
+          if (tk < n_tok) {
+            float* yr = t.kind == kDnRouted ? a.y32 + static_cast<size_t>(S.perm[r0 + tk]) * d
+                                            : a.ys32 + static_cast<size_t>(tk) * d;
+            yr[feat] = dacc[c];
+            yr[feat + 8] = dacc[2 + c];
           }
         }
-        ++n_dn_mine;
-        consumers_sync();  // the next task's reduction reuses S.red
+        __syncwarp();
+        if (lane == 0) atomicAdd(const_cast<int*>(&S.flags[2]), 1);
       }
-      if (gu) consumers_sync();  // S.sums / S.red are reused by the next task
     }
     cp_async_wait<0>();  // nothing of this warp's is still in flight
+    if (ok && !gu_done_here) ok = gate_up_barrier();  // a warp without down pieces passes it here
     ok = consumers_all(ok);
-    // ---- after the last piece: the gate/up count if not given yet, then the down count; once
-    // every CTA's down tasks are done, this CTA combines its share of the outputs ----
-    if (ok && !gu_signalled) {
-      if (ct == 0) {
-        __threadfence();
-        atomicAdd(&sy->gu_done, n_gu_mine);
-      }
-      gu_signalled = true;
-    }
+    // ---- every CTA's down tasks done (one addition per CTA), then this CTA's share of the combine ----
     if (ok) {
-      consumers_sync();  // this CTA's y writes precede its count
       if (ct == 0) {
         __threadfence();
-        if (n_dn_mine) atomicAdd(&sy->dn_done, n_dn_mine);
-        const uint32_t nmat = static_cast<uint32_t>(S.touched[E]) + (a.n_shared > 0 ? 1u : 0u);
-        S.flags[6] = wait_counter(&sy->dn_done, nmat * static_cast<uint32_t>(n_dn_groups), abort_flag, a.err) ? 1 : 0;
+        if (S.flags[2]) atomicAdd(&sy->dn_done, static_cast<uint32_t>(S.flags[2]));
+        const uint32_t nmat = static_cast<uint32_t>(n_touched) + (a.n_shared > 0 ? 1u : 0u);
+        S.flags[6] = wait_counter(&sy->dn_done, nmat * static_cast<uint32_t>(d / 16), abort_flag, a.err) ? 1 : 0;
       }
       consumers_sync();
       ok = S.flags[6] != 0;
@@ -677,11 +641,12 @@ __global__ void __launch_bounds__(kThreads, 1) layer_small_kernel(const LsArgs a
         const int t = (8 * c) / d, j = (8 * c) % d;
         float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int sl = 0; sl < k; ++sl) {
-          const float g = S.gates[t * k + sl];
+          const float gt = S.gates[t * k + sl];
           const float4* yp = reinterpret_cast<const float4*>(a.y32 + static_cast<size_t>(t * k + sl) * d + j);
           const float4 y0 = __ldcg(yp), y1 = __ldcg(yp + 1);
-          o[0] = fmaf(g, y0.x, o[0]), o[1] = fmaf(g, y0.y, o[1]), o[2] = fmaf(g, y0.z, o[2]), o[3] = fmaf(g, y0.w, o[3]);
-          o[4] = fmaf(g, y1.x, o[4]), o[5] = fmaf(g, y1.y, o[5]), o[6] = fmaf(g, y1.z, o[6]), o[7] = fmaf(g, y1.w, o[7]);
+          o[0] = fmaf(gt, y0.x, o[0]), o[1] = fmaf(gt, y0.y, o[1]), o[2] = fmaf(gt, y0.z, o[2]);
+          o[3] = fmaf(gt, y0.w, o[3]), o[4] = fmaf(gt, y1.x, o[4]), o[5] = fmaf(gt, y1.y, o[5]);
+          o[6] = fmaf(gt, y1.z, o[6]), o[7] = fmaf(gt, y1.w, o[7]);
         }
         if (a.n_shared > 0) {
           const float4* sp = reinterpret_cast<const float4*>(a.ys32 + static_cast<size_t>(t) * d + j);

@@ -35,6 +35,23 @@ def plan_for(spec):
     return make_plan(w, T_max=T_max)
 
 
+@functools.lru_cache(maxsize=None)
+def fused_plan_for(spec):
+    """A plan whose steps of at most 8 tokens run the one-launch layer (MOE_SMALL_STEP=fused)."""
+    import os
+    old = os.environ.get("MOE_SMALL_STEP")
+    os.environ["MOE_SMALL_STEP"] = "fused"
+    try:
+        T_max = {synth.TINY: 64, synth.QWEN_A3B_LIKE: 64}[spec]
+        w = {synth.TINY: workload("tiny", 0), synth.QWEN_A3B_LIKE: workload("decode", 0)}[spec]
+        return make_plan(w, T_max=T_max)
+    finally:
+        if old is None:
+            del os.environ["MOE_SMALL_STEP"]
+        else:
+            os.environ["MOE_SMALL_STEP"] = old
+
+
 def paths_for(spec):
     return ["simt", "tc"]
 
@@ -226,14 +243,15 @@ def test_untiled_shape_runs_the_reference_path():
 FP4_SMALL = synth.LayerSpec(E=16, k=4, d=256, f=128, n_shared=1, f_s=128, wdtype="mxfp4")
 
 
-@pytest.mark.parametrize("path", ["simt", "tc", "tc-dequant"])
+@pytest.mark.parametrize("path", ["simt", "tc", "tc-mx"])
 @pytest.mark.parametrize("T", [1, 77, 300])
 def test_fp4_small_layer_both_paths(T, path, monkeypatch):
     """4-bit routed weights with a bf16 shared expert, every token: the CUDA-core path, the
-    tensor-core path with the block-scaled gate/up (e2m1 weights x two e4m3 terms of x) and with
-    the dequantising gate/up."""
-    if path == "tc-dequant":
-        monkeypatch.setenv("MOE_FP4_GATEUP", "dequant")
+    tensor-core path with the dequantising GEMMs and with the block-scaled ones (e2m1 weights x
+    two e4m3 terms of x or h)."""
+    if path == "tc-mx":
+        monkeypatch.setenv("MOE_FP4_GATEUP", "mx")
+        monkeypatch.setenv("MOE_FP4_DOWN", "mx")
         path = "tc"
     w = synth.custom(FP4_SMALL, T, n_prefill=T - 1, name=f"fp4small{T}")
     plan = make_plan(w)
@@ -254,8 +272,14 @@ def test_fp4_small_layer_both_paths(T, path, monkeypatch):
 FP4_ODD = synth.LayerSpec(E=12, k=3, d=384, f=192, n_shared=0, f_s=0, wdtype="mxfp4", zipf_s=1.2)
 
 
+@pytest.mark.parametrize("variant", ["mx", "dequant"])
 @pytest.mark.parametrize("T", [5, 390])
-def test_fp4_odd_k_blocks_tc(T):
+def test_fp4_odd_k_blocks_tc(T, variant, monkeypatch):
+    """d_ff / 64 odd: the down projection's last 128-deep stage holds one 64-wide block (the
+    block-scaled kernels issue two MMAs there, the dequantising ones one slice)."""
+    if variant == "mx":
+        monkeypatch.setenv("MOE_FP4_GATEUP", "mx")
+        monkeypatch.setenv("MOE_FP4_DOWN", "mx")
     w = synth.custom(FP4_ODD, T, n_prefill=T, name=f"fp4odd{T}")
     plan = make_plan(w)
     plan.set_path("tc")
@@ -342,7 +366,7 @@ def test_small_step_one_launch_vs_oracle(spec_name, T):
     oracle, the same answer twice (bit for bit), and close to the tensor-core path's."""
     spec = workload(spec_name, 0).spec
     w = synth.custom(spec, T, n_prefill=T // 2, name=f"small{spec_name}{T}")
-    plan = plan_for(spec)
+    plan = fused_plan_for(spec)
     plan.set_path("auto")
     x = to_dev(w.x(), "bf16")
     a = plan.forward(x, n_prefill=w.n_prefill).clone()
