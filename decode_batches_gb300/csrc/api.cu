@@ -52,7 +52,7 @@ namespace {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t logits, parts, ids, gates, masks, chunk_base, counts, offsets, perm, inv, segs, n_segs, h, h_s, y, y_s, x16;
+  size_t logits, parts, ids, gates, masks, counts, offsets, perm, inv, segs, n_segs, h, h_s, y, y_s, x16;
   size_t touched, y32;  // the one-launch small-step layer: touched-expert list, fp32 expert outputs
   size_t xq, xs;        // the block-scaled 4-bit gate/up: x as two e4m3 terms and their e8m0 scales
   size_t hq, hs;        // ... and down: h as two e4m3 terms and their e8m0 scales
@@ -77,6 +77,7 @@ struct moe_plan {
   float* b_router = nullptr;
   uint16_t* w_router3 = nullptr;  // W_r split into three bf16 pieces [3][E][d] (tensor-core router)
   CUtensorMap map_router3{};
+  CUtensorMap map_x{};  // the current call's x [T][d] (tensor-core router), encoded per call
   bool router_tc = false;
   uint8_t* w_gu = nullptr;
   uint8_t* s_gu = nullptr;
@@ -145,8 +146,7 @@ static WsLayout layout_for(const moe_plan* p, int T_max) {
   L.parts = take(part_rows * p->E * sizeof(float));
   L.ids = take(R * sizeof(int32_t));
   L.gates = take(R * sizeof(float));
-  L.masks = take(n_chunks * p->E * sizeof(uint32_t));
-  L.chunk_base = take(n_chunks * p->E * sizeof(int32_t));
+  L.masks = take(static_cast<size_t>(group_mask_stride(static_cast<int>(n_chunks))) * p->E * sizeof(uint32_t));
   L.counts = take(p->E * sizeof(int32_t));
   L.offsets = take((p->E + 1) * sizeof(int32_t));
   L.perm = take(R * sizeof(int32_t));
@@ -812,7 +812,9 @@ static moe_status router_step(moe_plan* p, const uint16_t* x, int T, const float
   float* parts = ws_ptr<float>(p, p->L.parts);
   if (p->router_tc && T > kRouterTcMinT) {
     const int ns = router_tc_splits(T, p->E, p->d, p->num_sms);
-    LAUNCH(p, "router_tc", st, launch_router_tc(&p->map_router3, x, T, p->E, p->d, ns, parts, p->err, st));
+    moe_status s = make_map_16(&p->map_x, x, p->d, T, 128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+    if (s != MOE_OK) return s;
+    LAUNCH(p, "router_tc", st, launch_router_tc(&p->map_router3, &p->map_x, T, p->E, p->d, ns, parts, p->err, p->num_sms, st));
     *parts_out = parts, *nsplit = ns, *bias = p->b_router;
   } else if (T <= 128 && p->d % 128 == 0) {
     LAUNCH(p, "router_logits", st, launch_router_parts_small(x, p->w_router, T, p->E, p->d, parts, st));
@@ -844,6 +846,9 @@ static moe_status route_step(moe_plan* p, const uint16_t* x, int T, float* logit
   return MOE_OK;
 }
 
+// Device rows are read and written as 16-byte vectors (cp.async, TMA, uint4 stores).
+static bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
+
 extern "C" moe_status moe_layer_forward(moe_plan* p, const void* x, int T, int n_prefill, void* out,
                                         moe_stream_t stream) {
   moe_status s = check_ready(p, T, true);
@@ -852,6 +857,7 @@ extern "C" moe_status moe_layer_forward(moe_plan* p, const void* x, int T, int n
   p->launch_count = 0;
   if (T == 0) return MOE_OK;
   if (!x || !out) return fail(MOE_ERR_INVALID_ARG, "x and out are required");
+  if (!aligned16(x) || !aligned16(out)) return fail(MOE_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const uint16_t* xb = static_cast<const uint16_t*>(x);
   if (use_small_layer(p, T)) {
@@ -886,14 +892,12 @@ extern "C" moe_status moe_layer_forward(moe_plan* p, const void* x, int T, int n
   int32_t* ids = ws_ptr<int32_t>(p, p->L.ids);
   float* gates = ws_ptr<float>(p, p->L.gates);
   uint32_t* masks = ws_ptr<uint32_t>(p, p->L.masks);
-  int32_t* chunk_base = ws_ptr<int32_t>(p, p->L.chunk_base);
   int32_t* counts = ws_ptr<int32_t>(p, p->L.counts);
   int32_t* offsets = ws_ptr<int32_t>(p, p->L.offsets);
   int32_t* perm = ws_ptr<int32_t>(p, p->L.perm);
   int32_t* inv = ws_ptr<int32_t>(p, p->L.inv);
   uint16_t* y = ws_ptr<uint16_t>(p, p->L.y);
   uint16_t* y_s = p->n_shared > 0 ? ws_ptr<uint16_t>(p, p->L.y_s) : nullptr;
-  const int n_chunks = (T + kChunk - 1) / kChunk;
   const bool tc = use_tc(p);
   Seg* segs = tc ? ws_ptr<Seg>(p, p->L.segs) : nullptr;
   const bool forked = shared_gate_up_beside(p, T);
@@ -936,10 +940,9 @@ extern "C" moe_status moe_layer_forward(moe_plan* p, const void* x, int T, int n
     xc = XConv{};
     s = route_step(p, xb, T, nullptr, ids, gates, masks, st);
     if (s != MOE_OK) return s;
-    LAUNCH(p, "chunk_scan", st, launch_chunk_scan(masks, n_chunks, p->E, chunk_base, counts, st));
-    LAUNCH(p, "scatter", st,
-           launch_scatter(ids, masks, chunk_base, counts, T, p->E, p->k, perm, inv, offsets, segs,
-                          ws_ptr<int32_t>(p, p->L.n_segs), p->L.max_segs, p->err, st));
+    LAUNCH(p, "group", st,
+           launch_group(ids, masks, T, p->E, p->k, counts, offsets, perm, inv, segs, ws_ptr<int32_t>(p, p->L.n_segs),
+                        p->L.max_segs, p->err, st));
   }
   s = run_experts(p, xb, T, offsets, perm, y, y_s, st, forked, xc.x16 != nullptr);
   if (s != MOE_OK) return s;
@@ -956,6 +959,7 @@ extern "C" moe_status moe_route(moe_plan* p, const void* x, int T, float* logits
   p->launch_count = 0;
   if (T == 0) return MOE_OK;
   if (!x || !ids || !gates) return fail(MOE_ERR_INVALID_ARG, "x, ids and gates are required");
+  if (!aligned16(x)) return fail(MOE_ERR_INVALID_ARG, "x must be 16-byte aligned");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   return route_step(p, static_cast<const uint16_t*>(x), T, logits, ids, gates, nullptr, st);
   return MOE_OK;
@@ -988,14 +992,10 @@ extern "C" moe_status moe_permute(moe_plan* p, const int32_t* ids, int T, int32_
   if (s != MOE_OK) return s;
   p->launch_count = 0;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int n_chunks = (T + kChunk - 1) / kChunk;
   uint32_t* masks = ws_ptr<uint32_t>(p, p->L.masks);
-  int32_t* chunk_base = ws_ptr<int32_t>(p, p->L.chunk_base);
   if (T > 0) LAUNCH(p, "masks_from_ids", st, launch_masks_from_ids(ids, T, p->E, p->k, masks, p->err, st));
-  LAUNCH(p, "chunk_scan", st, launch_chunk_scan(masks, n_chunks, p->E, chunk_base, counts, st));
-  LAUNCH(p, "scatter", st,
-         launch_scatter(ids, masks, chunk_base, counts, T, p->E, p->k, perm, inv_perm, offsets, nullptr, nullptr, 0,
-                        p->err, st));
+  LAUNCH(p, "group", st,
+         launch_group(ids, masks, T, p->E, p->k, counts, offsets, perm, inv_perm, nullptr, nullptr, 0, p->err, st));
   return MOE_OK;
 }
 
@@ -1007,6 +1007,8 @@ extern "C" moe_status moe_experts(moe_plan* p, const void* x, int T, const int32
   if (T == 0) return MOE_OK;
   if (!x || !offsets || !perm || !y) return fail(MOE_ERR_INVALID_ARG, "x, offsets, perm and y are required");
   if (p->n_shared > 0 && !shared_y) return fail(MOE_ERR_INVALID_ARG, "shared_y is required when n_shared > 0");
+  if (!aligned16(x) || !aligned16(y) || (p->n_shared > 0 && !aligned16(shared_y)))
+    return fail(MOE_ERR_INVALID_ARG, "x, y and shared_y must be 16-byte aligned");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (use_tc(p))
     LAUNCH(p, "segments", st,
@@ -1024,6 +1026,8 @@ extern "C" moe_status moe_combine(moe_plan* p, const float* y, const float* gate
   if (T == 0) return MOE_OK;
   if (!y || !gates || !inv_perm || !out) return fail(MOE_ERR_INVALID_ARG, "y, gates, inv_perm and out are required");
   if (p->d % 8) return fail(MOE_ERR_UNSUPPORTED, "moe_combine needs d_model %% 8 == 0");
+  if (!aligned16(y) || !aligned16(out) || (shared_y && !aligned16(shared_y)))
+    return fail(MOE_ERR_INVALID_ARG, "y, shared_y and out must be 16-byte aligned");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   LAUNCH(p, "combine", st, launch_combine_f32(y, gates, inv_perm, shared_y, T, p->k, p->d, static_cast<uint16_t*>(out), st));
   return MOE_OK;

@@ -52,6 +52,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const Y* __restrict__ y, c
   const uint64_t pol = l2_policy_evict_first();  // y and y_s are read once, here
   for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    Row8<Y> vs;  // the shared term: requested with the first slots, added last
+    if (ys) vs.load(ys + static_cast<size_t>(t) * d + c, pol);
     for (int j0 = 0; j0 < k; j0 += 8) {  // the loads of 8 slots are in flight together
       Row8<Y> v[8];
 #pragma unroll
@@ -73,10 +75,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const Y* __restrict__ y, c
       }
     }
     if (ys) {
-      Row8<Y> v;
-      v.load(ys + static_cast<size_t>(t) * d + c, pol);
       float sf[8];
-      v.to_f32(sf);
+      vs.to_f32(sf);
 #pragma unroll
       for (int q = 0; q < 8; ++q) acc[q] += sf[q];
     }

@@ -277,6 +277,8 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
   } else if (warp < 6) {
     // ---------------- epilogue ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // h and y are read back by the next launch: keep them in L2 ahead of the streamed weights
+    const uint64_t pol_out = l2_policy_evict_last();
     uint32_t j = 0;
     for (int u = blockIdx.x; u < total_units && !*abort_flag; u += gridDim.x, ++j) {
       const Unit un = decode_unit(u, a, tiles_r, tiles_s, n_shared_units);
@@ -330,7 +332,7 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
               const int cl = lane >> 1, half = lane & 1;
               if (c0 + cl < un.rows) {
                 const uint4 v = *reinterpret_cast<const uint4*>(stg + cl * 16 + 8 * half);
-                *reinterpret_cast<uint4*>(hout + static_cast<size_t>(un.row_start + c0 + cl) * ldh + feat0 + 8 * half) = v;
+                st_global_v4_hint(hout + static_cast<size_t>(un.row_start + c0 + cl) * ldh + feat0 + 8 * half, v, pol_out);
               }
             }
             __syncwarp();
@@ -358,7 +360,7 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
               const int cl = idx >> 2, g = idx & 3;
               if (c0 + cl < un.rows) {
                 const uint4 v = *reinterpret_cast<const uint4*>(stg + cl * 32 + 8 * g);
-                *reinterpret_cast<uint4*>(yout + static_cast<size_t>(un.row_start + c0 + cl) * a.d + feat0 + 8 * g) = v;
+                st_global_v4_hint(yout + static_cast<size_t>(un.row_start + c0 + cl) * a.d + feat0 + 8 * g, v, pol_out);
               }
             }
             __syncwarp();

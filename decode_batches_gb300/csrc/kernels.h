@@ -23,6 +23,9 @@ struct XConv {
 
 // Tokens per chunk of the grouping step: one 32-bit mask word per (chunk, expert).
 constexpr int kChunk = 32;
+// Row stride (32-bit words) of the per-chunk expert masks masks[e][c] for n_chunks chunks: a
+// multiple of 4, so that rows are read as 16-byte vectors.
+__host__ __device__ inline int group_mask_stride(int n_chunks) { return (n_chunks + 3) & ~3; }
 // Largest number of rows one tensor-core unit handles (the MMA's N).
 constexpr int kSegRowsMax = 128;
 
@@ -77,22 +80,20 @@ cudaError_t launch_route_small(const float* parts, int nsplit, const float* bias
                                float* gates, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, Seg* segs,
                                int32_t* n_segs, int max_segs, uint32_t* done, uint32_t* err, cudaStream_t st,
                                const XConv& xc = XConv{});
-cudaError_t launch_router_tc(const CUtensorMap* w3, const uint16_t* x, int T, int E, int d, int nsplit, float* parts,
-                             uint32_t* err, cudaStream_t st);
+// Persistent: min(items, num_sms) CTAs over the (expert tile, K split, token tile) items.
+// xm: x [T][d] bf16, box {64, 128}, 128-byte swizzle.
+cudaError_t launch_router_tc(const CUtensorMap* w3, const CUtensorMap* xm, int T, int E, int d, int nsplit,
+                             float* parts, uint32_t* err, int num_sms, cudaStream_t st);
 cudaError_t launch_split_router(const float* w, uint16_t* w3, size_t n, cudaStream_t st);
 // Per-chunk expert masks from given ids (validates range / duplicates).
 cudaError_t launch_masks_from_ids(const int32_t* ids, int T, int E, int k, uint32_t* masks,
                                   uint32_t* err, cudaStream_t st);
-// Per-expert scan over the chunk masks: chunk_base[e][c] (assignments of e in earlier chunks)
-// and counts[e].
-cudaError_t launch_chunk_scan(const uint32_t* masks, int n_chunks, int E, int32_t* chunk_base, int32_t* counts,
-                              cudaStream_t st);
-// perm / inv_perm, and offsets (exclusive scan of counts, offsets[E] = total); if segs is given
-// also the segment list of the routed experts for the grouped GEMMs.
-cudaError_t launch_scatter(const int32_t* ids, const uint32_t* masks, const int32_t* chunk_base,
-                           const int32_t* counts, int T, int E, int k, int32_t* perm, int32_t* inv,
-                           int32_t* offsets, Seg* segs, int32_t* n_segs, int max_segs, uint32_t* err,
-                           cudaStream_t st);
+// Grouping in one launch from the chunk masks and the ids: counts, offsets (exclusive scan of
+// counts, offsets[E] = total), perm / inv_perm (-1 for a dropped assignment) and, if segs is
+// given, the segment list of the routed experts for the grouped GEMMs.
+cudaError_t launch_group(const int32_t* ids, const uint32_t* masks, int T, int E, int k, int32_t* counts,
+                         int32_t* offsets, int32_t* perm, int32_t* inv, Seg* segs, int32_t* n_segs, int max_segs,
+                         uint32_t* err, cudaStream_t st);
 // Segment list from offsets only (used by the separate experts entry point).
 cudaError_t launch_segments_from_offsets(const int32_t* offsets, int E, Seg* segs, int32_t* n_segs,
                                          int max_segs, uint32_t* err, cudaStream_t st);

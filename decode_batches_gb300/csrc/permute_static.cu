@@ -1,14 +1,14 @@
 // Allocation-free grouping entry point.
 //
-// moe_permute needs scratch memory (per-chunk expert masks and chunk bases), which normally
+// moe_permute needs scratch memory (the per-chunk expert masks), which normally
 // lives in the workspace the caller allocated for a plan.  Some callers cannot allocate device
 // memory at all: engines whose memory planner owns every byte of the device and forbids a
 // component from allocating outside its pool, and code on a latency-critical path, where
 // cudaMalloc would synchronise the device.  moe_permute_static serves them: its scratch is a
 // fixed, file-scope device array that exists as soon as the library is loaded on a device.
 //
-// The array is kStaticWords 32-bit words for the masks plus the same for the chunk bases
-// (2 MiB in all).  Every GPU that loads the library holds it until the process exits.  All calls
+// The array is kStaticWords 32-bit words for the masks (1 MiB).  Every GPU that loads the
+// library holds it until the process exits.  All calls
 // on a device share it: calls that can overlap on the GPU (different streams without ordering)
 // race on it.  Each call rewrites every scratch word it reads, so nothing needs clearing.
 #include <mutex>
@@ -18,9 +18,9 @@
 
 namespace moe {
 
-constexpr size_t kStaticWords = size_t(1) << 18;  // per array: n_chunks * E <= 262144
+constexpr size_t kStaticWords = size_t(1) << 18;  // mask words: group_mask_stride(n_chunks) * E <= 262144
 
-static __device__ __align__(256) uint32_t g_static_scratch[2 * kStaticWords];
+static __device__ __align__(256) uint32_t g_static_scratch[kStaticWords];
 
 // Device address of g_static_scratch in the current CUDA context.  The module (and the array)
 // is loaded per context, so the address is cached under the context's unique id: a context that
@@ -61,17 +61,16 @@ extern "C" moe_status moe_permute_static(int E, int k, const int32_t* ids, int T
   if (E < 1 || E > 1024 || k < 1 || k > 32 || k > E || T < 0) return MOE_ERR_INVALID_ARG;
   if (!counts || !offsets || (T > 0 && (!ids || !perm || !inv_perm))) return MOE_ERR_INVALID_ARG;
   const size_t n_chunks = (static_cast<size_t>(T) + kChunk - 1) / kChunk;
-  if (n_chunks * static_cast<size_t>(E) > kStaticWords) return MOE_ERR_WORKSPACE;
+  if (n_chunks > (kStaticWords >> 2) ||
+      static_cast<size_t>(group_mask_stride(static_cast<int>(n_chunks))) * static_cast<size_t>(E) > kStaticWords)
+    return MOE_ERR_WORKSPACE;
   void* base = nullptr;
   if (static_scratch(&base) != cudaSuccess) return MOE_ERR_CUDA;
   uint32_t* masks = static_cast<uint32_t*>(base);
-  int32_t* chunk_base = reinterpret_cast<int32_t*>(masks + kStaticWords);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (T > 0 && launch_masks_from_ids(ids, T, E, k, masks, nullptr, st) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_chunk_scan(masks, static_cast<int>(n_chunks), E, chunk_base, counts, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (launch_scatter(ids, masks, chunk_base, counts, T, E, k, perm, inv_perm, offsets, nullptr, nullptr, 0, nullptr,
-                     st) != cudaSuccess)
+  if (launch_group(ids, masks, T, E, k, counts, offsets, perm, inv_perm, nullptr, nullptr, 0, nullptr, st) !=
+      cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

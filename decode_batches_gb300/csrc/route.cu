@@ -3,11 +3,11 @@
 //   router logits      l[t,e] = x[t] . W_r[e] + b[e]        (fp32 accumulation)
 //   top-k + gates      warp per token; total order (value desc, index asc), NaN lowest;
 //                      gates = softmax of the k selected logits (fp32)
-//   grouping           per 32-token chunk a 32-bit mask per expert; a scan over
-//                      (chunk, expert) gives counts, exclusive offsets and chunk bases; the
-//                      scatter ranks each assignment inside its chunk with one popcount, so
-//                      the permutation is a stable counting sort with no atomics-order
-//                      dependence (identical on every run).  Steps of at most 64 assignments
+//   grouping           per 32-token chunk a 32-bit mask per expert; one launch reads the
+//                      masks for counts, exclusive offsets and chunk bases and ranks each
+//                      assignment inside its chunk with one popcount, so the permutation is a
+//                      stable counting sort with no atomics-order dependence (identical on
+//                      every run).  Steps of at most 64 assignments
 //                      sort unique (expert, assignment) keys in one warp instead (group_tiny):
 //                      the same permutation, with one block barrier.
 // Sources: "DeepSeek V4.1F Q4 with native DSpark MTP on M3 Ultra", Decode paragraph (the
@@ -254,14 +254,14 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* w_router, const
 // Top-k with gates
 // ============================================================================================
 
-// One block per 32-token chunk, one warp per token (two per warp for E > 384).  Lane l holds the
-// keys of experts l, l + 32, ..., l + 32 (PL - 1).  Each of the k rounds takes every lane's best
-// remaining key and a warp-wide maximum (redux on the high word, then on the low word among the
-// lanes that hold that high word); the owner lane retires the winner.  Masks are stored
-// expert-major: masks[e * n_chunks + c].  The logits are the sum of `nsplit` partial matrices
-// parts[s][T][E] (s ascending) plus the optional bias; they are written to logits_out if given.
-template <int PL>
-constexpr int topk_threads() { return PL >= 16 ? 512 : 1024; }  // 64 registers/thread at 1024
+// Two blocks per 32-token chunk (16 tokens each), one warp per token.  Lane l holds the
+// logits of experts l, l + 32, ..., l + 32 (PL - 1); topk_select takes k rounds of a warp-wide
+// maximum.  Masks are stored expert-major, masks[e * mstride + c], bit tl for token tl of the
+// chunk: each block writes its 16-bit half of the word.  The logits are the sum of `nsplit`
+// partial matrices parts[s][T][E] (s ascending) plus the optional bias; they are written to
+// logits_out if given.
+constexpr int kTopkTokens = kChunk / 2;       // tokens per block
+constexpr int kTopkThreads = 32 * kTopkTokens;
 
 // Top-k of token t by one warp: sums the partial logits (split order fixed) and the bias,
 // optionally stores the logits, then selects (topk_select).
@@ -304,31 +304,34 @@ MOE_DEVICE int topk_token(const float* __restrict__ parts, int nsplit, const flo
 }
 
 template <int PL>
-__global__ void __launch_bounds__(topk_threads<PL>()) topk_kernel(const float* __restrict__ parts, int nsplit,
-                                                                  const float* __restrict__ bias,
-                                                                  float* __restrict__ logits_out, int T, int E, int k,
-                                                                  int n_chunks, int32_t* __restrict__ ids,
-                                                                  float* __restrict__ gates,
-                                                                  uint32_t* __restrict__ masks, uint32_t* err,
-                                                                  const XConv xc) {
-  extern __shared__ uint32_t smask[];  // [E]
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ parts, int nsplit,
+                                                            const float* __restrict__ bias,
+                                                            float* __restrict__ logits_out, int T, int E, int k,
+                                                            int n_chunks, int32_t* __restrict__ ids,
+                                                            float* __restrict__ gates,
+                                                            uint32_t* __restrict__ masks, uint32_t* err,
+                                                            const XConv xc) {
+  extern __shared__ uint32_t smask[];  // [E]: bits of this block's 16 tokens
   pdl_trigger();
   pdl_wait();
   convert_x16(xc, err);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = blockIdx.x;
+  const int c = blockIdx.x >> 1, half = blockIdx.x & 1;
   if (masks)
     for (int e = threadIdx.x; e < E; e += blockDim.x) smask[e] = 0u;
   __syncthreads();
-  for (int tl = warp; tl < kChunk; tl += blockDim.x / 32) {
-    const int t = c * kChunk + tl;
-    if (t >= T) break;
+  const int t = c * kChunk + kTopkTokens * half + warp;
+  if (t < T) {
     const int sel = topk_token<PL>(parts, nsplit, bias, logits_out, t, T, E, k, ids, gates, err);
-    if (masks && lane < k) atomicOr(&smask[sel], 1u << tl);
+    if (masks && lane < k) atomicOr(&smask[sel], 1u << warp);
   }
   if (masks) {
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) masks[static_cast<size_t>(e) * n_chunks + c] = smask[e];
+    // little-endian: half h of the 32-bit mask word is the 16-bit word 2 w + h
+    uint16_t* m16 = reinterpret_cast<uint16_t*>(masks);
+    const size_t mstride = group_mask_stride(n_chunks);
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+      m16[2 * (static_cast<size_t>(e) * mstride + c) + half] = static_cast<uint16_t>(smask[e]);
   }
 }
 
@@ -336,7 +339,7 @@ template <int PL>
 static cudaError_t launch_topk_pl(const float* parts, int nsplit, const float* bias, float* logits_out, int T, int E,
                                   int k, int n_chunks, int32_t* ids, float* gates, uint32_t* masks, uint32_t* err,
                                   const XConv& xc, cudaStream_t st) {
-  return launch_pdl(topk_kernel<PL>, dim3(n_chunks), dim3(topk_threads<PL>()), masks ? E * sizeof(uint32_t) : 0, st,
+  return launch_pdl(topk_kernel<PL>, dim3(2 * n_chunks), dim3(kTopkThreads), masks ? E * sizeof(uint32_t) : 0, st,
                     parts, nsplit, bias, logits_out, T, E, k, n_chunks, ids, gates, masks, err, xc);
 }
 
@@ -391,7 +394,8 @@ __global__ void __launch_bounds__(256) masks_from_ids_kernel(const int32_t* __re
     atomicOr(&smask[e], 1u << tl);
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) masks[static_cast<size_t>(e) * n_chunks + c] = smask[e];
+  const size_t mstride = group_mask_stride(n_chunks);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) masks[static_cast<size_t>(e) * mstride + c] = smask[e];
 }
 
 cudaError_t launch_masks_from_ids(const int32_t* ids, int T, int E, int k, uint32_t* masks,
@@ -400,51 +404,6 @@ cudaError_t launch_masks_from_ids(const int32_t* ids, int T, int E, int k, uint3
   const int n_chunks = (T + kChunk - 1) / kChunk;
   return launch_pdl(masks_from_ids_kernel, dim3(n_chunks), dim3(256), E * sizeof(uint32_t), st, ids, T, E, k, n_chunks,
                     masks, err);
-}
-
-// Per-expert scan over chunks: one warp per expert, 32 chunk masks per load (masks are
-// expert-major), the loads of up to kBatch 32-chunk groups issued before any is used.
-// chunk_base[e][c] = number of assignments of expert e in chunks before c; counts[e] = total.
-__global__ void __launch_bounds__(256) chunk_scan_kernel(const uint32_t* __restrict__ masks, int n_chunks, int E,
-                                                         int32_t* __restrict__ chunk_base,
-                                                         int32_t* __restrict__ counts) {
-  constexpr int kBatch = 8;
-  pdl_trigger();
-  pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (e >= E) return;
-  const uint32_t* m = masks + static_cast<size_t>(e) * n_chunks;
-  int32_t* cb = chunk_base + static_cast<size_t>(e) * n_chunks;
-  const int groups = (n_chunks + 31) / 32;
-  int run = 0;
-  for (int g0 = 0; g0 < groups; g0 += kBatch) {
-    int pc[kBatch];
-#pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      const int c = (g0 + b) * 32 + lane;
-      pc[b] = c < n_chunks ? __popc(m[c]) : 0;
-    }
-#pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      if (g0 + b >= groups) break;
-      int inc = pc[b];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int up = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += up;
-      }
-      const int c = (g0 + b) * 32 + lane;
-      if (c < n_chunks) cb[c] = run + inc - pc[b];
-      run += __shfl_sync(0xffffffffu, inc, 31);
-    }
-  }
-  if (lane == 0) counts[e] = run;
-}
-
-cudaError_t launch_chunk_scan(const uint32_t* masks, int n_chunks, int E, int32_t* chunk_base, int32_t* counts,
-                              cudaStream_t st) {
-  return launch_pdl(chunk_scan_kernel, dim3((E + 7) / 8), dim3(256), 0, st, masks, n_chunks, E, chunk_base, counts);
 }
 
 // Exclusive scan over the block (blockDim.x a multiple of 32, <= 1024) of v; *total = block sum.
@@ -523,69 +482,136 @@ MOE_DEVICE int block_offsets(const int32_t* __restrict__ counts, int E, int* s_o
   return total;
 }
 
-// One block per 32-token chunk.  Every block scans the expert counts into shared offsets (E
-// values, cheaper than another launch); block 0 also publishes offsets and, if segs is given,
-// the segment list of the grouped GEMMs.  Each assignment's row is offsets[e] + its chunk's
-// base + the popcount of the earlier bits of the chunk's mask word: a stable counting sort.
-__global__ void __launch_bounds__(kScanThreads) scatter_kernel(
-    const int32_t* __restrict__ ids, const uint32_t* __restrict__ masks, const int32_t* __restrict__ chunk_base,
-    const int32_t* __restrict__ counts, int T, int E, int k, int n_chunks, int32_t* __restrict__ perm,
-    int32_t* __restrict__ inv, int32_t* __restrict__ offsets, Seg* segs, int32_t* n_segs, int max_segs,
-    uint32_t* err) {
-  __shared__ int s_off[1025];
+// Grouping from the per-chunk expert masks in one launch.  masks[e * mstride + c] holds bit tl
+// for token 32 c + tl of chunk c when that token chose expert e (valid assignments only);
+// mstride is a multiple of 4, so a mask row is read as 16-byte vectors.  Block b owns the
+// chunks [b cpb, (b + 1) cpb).  Every block first reads the whole mask matrix (a few threads
+// per expert): each expert's total, its count in the chunks before the block's, and the block's
+// own mask words; a block scan of the totals gives the offsets.  Each assignment of the block's
+// chunks then takes its row from shared memory alone -- a stable counting sort:
+//   row = offsets[e] + (rows of e before the block) + (rows of e in the block's earlier chunks)
+//         + popc(mask word & bits of the earlier tokens of the chunk).
+// An assignment whose id is out of range or repeats an earlier slot gets inv = -1 (the mask
+// builder flags it).  Block 0 also writes counts, offsets and, if segs is given, the segment
+// list of the grouped GEMMs.
+constexpr int kGroupThreads = 1024;
+constexpr int kGroupBlocksMax = 256;
+constexpr int kGroupLoads = 8;  // 16-byte mask loads in flight per thread
+
+static int group_cpb(int n_chunks) {
+  return n_chunks <= kGroupBlocksMax ? 1 : (n_chunks + kGroupBlocksMax - 1) / kGroupBlocksMax;
+}
+
+__global__ void __launch_bounds__(kGroupThreads) group_kernel(
+    const int32_t* __restrict__ ids, const uint32_t* __restrict__ masks, int mstride, int T, int E, int k,
+    int n_chunks, int cpb, int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+    int32_t* __restrict__ inv, Seg* segs, int32_t* n_segs, int max_segs, uint32_t* err) {
+  extern __shared__ int g_sm[];
+  int* s_tot = g_sm;                                            // [E]
+  int* s_pre = s_tot + E;                                       // [E]: rows of e before chunk c0
+  int* s_off = s_pre + E;                                       // [E + 1]
+  uint32_t* s_w = reinterpret_cast<uint32_t*>(s_off + E + 1);  // [cpb][E]: the block's mask words
+  int32_t* s_ids = reinterpret_cast<int32_t*>(s_w + cpb * E);  // [cpb * 32][k]: the block's ids
   pdl_trigger();
   pdl_wait();
-  block_offsets(counts, E, s_off);
+  const int c0 = blockIdx.x * cpb, c1 = min(c0 + cpb, n_chunks);
+  // the block's ids: the first share is requested now and lands while the masks are read
+  const int nt = max(0, min(cpb * kChunk, T - c0 * kChunk));  // tokens of the block
+  const int na = nt * k;
+  const int32_t* ids_blk = ids + static_cast<size_t>(c0) * kChunk * k;
+  const int id0 = static_cast<int>(threadIdx.x) < na ? ids_blk[threadIdx.x] : 0;
+  // threads per expert: a power of two <= 32 (consecutive lanes of one warp)
+  int tpe = 1;
+  while (tpe < 32 && 2 * tpe * E <= kGroupThreads) tpe *= 2;
+  const int e = threadIdx.x / tpe, q = threadIdx.x % tpe;
+  int tot = 0, pre = 0;
+  if (e < E) {
+    const uint4* row = reinterpret_cast<const uint4*>(masks + static_cast<size_t>(e) * mstride);
+    const int n4 = (n_chunks + 3) / 4;
+    for (int i0 = q; i0 < n4; i0 += kGroupLoads * tpe) {
+      uint4 v[kGroupLoads];
+#pragma unroll
+      for (int u = 0; u < kGroupLoads; ++u) {  // every load of the batch before any use
+        const int i = i0 + u * tpe;
+        v[u] = i < n4 ? __ldcg(row + i) : make_uint4(0u, 0u, 0u, 0u);  // written by the previous launch
+      }
+#pragma unroll
+      for (int u = 0; u < kGroupLoads; ++u) {
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int c = 4 * (i0 + u * tpe) + b;
+          const int pc = c < n_chunks ? __popc(w[b]) : 0;  // the row's padding words are not masks
+          tot += pc;
+          if (c < c0) pre += pc;
+          else if (c < c1) s_w[(c - c0) * E + e] = w[b];
+        }
+      }
+    }
+  }
+  for (int o = 1; o < tpe; o <<= 1) {
+    tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    pre += __shfl_xor_sync(0xffffffffu, pre, o);
+  }
+  if (q == 0 && e < E) {
+    s_tot[e] = tot;
+    s_pre[e] = pre;
+  }
+  if (static_cast<int>(threadIdx.x) < na) s_ids[threadIdx.x] = id0;
+  for (int a = threadIdx.x + blockDim.x; a < na; a += blockDim.x) s_ids[a] = ids_blk[a];
+  __syncthreads();
+  int total;
+  const int mine = static_cast<int>(threadIdx.x) < E ? s_tot[threadIdx.x] : 0;
+  const int ex = block_exclusive_scan(mine, &total);
+  if (static_cast<int>(threadIdx.x) < E) s_off[threadIdx.x] = ex;
+  if (threadIdx.x == 0) s_off[E] = total;
+  __syncthreads();
   if (blockIdx.x == 0) {
-    for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = s_off[e];
+    for (int x = threadIdx.x; x <= E; x += blockDim.x) {
+      offsets[x] = s_off[x];
+      if (x < E) counts[x] = s_tot[x];
+    }
     if (segs) {
-      int ns[kScanPerThread];
-      int mine = 0;
-#pragma unroll
-      for (int q = 0; q < kScanPerThread; ++q) {
-        const int e = threadIdx.x * kScanPerThread + q;
-        ns[q] = e < E ? num_segments(s_off[e + 1] - s_off[e]) : 0;
-        mine += ns[q];
-      }
+      const int ns = static_cast<int>(threadIdx.x) < E ? num_segments(mine) : 0;
       int seg_total;
-      int base = block_exclusive_scan(mine, &seg_total);
-#pragma unroll
-      for (int q = 0; q < kScanPerThread; ++q) {
-        const int e = threadIdx.x * kScanPerThread + q;
-        if (e < E) write_segments(segs, base, max_segs, e, s_off[e], s_off[e + 1] - s_off[e], err);
-        base += ns[q];
-      }
+      const int base = block_exclusive_scan(ns, &seg_total);
+      if (static_cast<int>(threadIdx.x) < E) write_segments(segs, base, max_segs, threadIdx.x, ex, mine, err);
       if (threadIdx.x == 0) *n_segs = min(seg_total, max_segs);
     }
   }
-  const int c = blockIdx.x;
-  if (c >= n_chunks) return;
-  for (int a = threadIdx.x; a < kChunk * k; a += blockDim.x) {
-    const int tl = a / k, j = a % k;
-    const int t = c * kChunk + tl;
-    if (t >= T) continue;
-    const int32_t* row = ids + static_cast<size_t>(t) * k;
-    const int e = row[j];
-    const size_t ai = static_cast<size_t>(t) * k + j;
-    if (!assignment_valid(row, j, e, E)) {
+  for (int a = threadIdx.x; a < na; a += blockDim.x) {
+    const int tb = a / k, j = a % k;  // token within the block, slot
+    const int32_t* id_row = s_ids + tb * k;
+    const int ee = id_row[j];
+    const size_t ai = (static_cast<size_t>(c0) * kChunk + tb) * k + j;
+    if (!assignment_valid(id_row, j, ee, E)) {
       inv[ai] = -1;
       continue;
     }
-    const size_t me = static_cast<size_t>(e) * n_chunks + c;
-    const int rank = __popc(masks[me] & ((1u << tl) - 1u));
-    const int r = s_off[e] + chunk_base[me] + rank;
+    const int cc = tb / kChunk, tl = tb % kChunk;
+    int r = s_off[ee] + s_pre[ee];
+    for (int c2 = 0; c2 < cc; ++c2) r += __popc(s_w[c2 * E + ee]);
+    r += __popc(s_w[cc * E + ee] & ((1u << tl) - 1u));
     perm[r] = static_cast<int32_t>(ai);
     inv[ai] = r;
   }
 }
 
-cudaError_t launch_scatter(const int32_t* ids, const uint32_t* masks, const int32_t* chunk_base,
-                           const int32_t* counts, int T, int E, int k, int32_t* perm, int32_t* inv,
-                           int32_t* offsets, Seg* segs, int32_t* n_segs, int max_segs, uint32_t* err,
-                           cudaStream_t st) {
+cudaError_t launch_group(const int32_t* ids, const uint32_t* masks, int T, int E, int k, int32_t* counts,
+                         int32_t* offsets, int32_t* perm, int32_t* inv, Seg* segs, int32_t* n_segs, int max_segs,
+                         uint32_t* err, cudaStream_t st) {
   const int n_chunks = (T + kChunk - 1) / kChunk;
-  return launch_pdl(scatter_kernel, dim3(n_chunks > 0 ? n_chunks : 1), dim3(kScanThreads), 0, st, ids, masks, chunk_base,
-                    counts, T, E, k, n_chunks, perm, inv, offsets, segs, n_segs, max_segs, err);
+  const int cpb = group_cpb(n_chunks);
+  const int blocks = n_chunks > 0 ? (n_chunks + cpb - 1) / cpb : 1;
+  const size_t smem =
+      (3 * static_cast<size_t>(E) + 1 + static_cast<size_t>(cpb) * E + static_cast<size_t>(cpb) * kChunk * k) *
+      sizeof(int32_t);
+  if (smem > 48 * 1024) {
+    cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(group_kernel), static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  return launch_pdl(group_kernel, dim3(blocks), dim3(kGroupThreads), smem, st, ids, masks, group_mask_stride(n_chunks),
+                    T, E, k, n_chunks, cpb, counts, offsets, perm, inv, segs, n_segs, max_segs, err);
 }
 
 // Routing and grouping of a small step in one launch.  One block per token adds its partial
@@ -593,7 +619,7 @@ cudaError_t launch_scatter(const int32_t* ids, const uint32_t* masks, const int3
 // arithmetic as the top-k kernel) into shared memory, and one warp selects the top k and
 // publishes ids / gates.  The last block to finish (a counter the plan owns, reset by that
 // block) groups the step: per-chunk expert masks from the ids, counts, chunk bases, offsets,
-// segments and the stable scatter -- the rows of chunk_scan + scatter, without their
+// segments and the stable scatter -- the steps of the masks and group launches, without their
 // launches.  Needs route_small_ok(T, E, k, nsplit).
 constexpr int kSmallSplitsMax = 16;
 constexpr int kRgThreads = 256;
@@ -608,7 +634,7 @@ size_t route_small_smem(int T, int E, int k) {
 
 // Grouping of a small step by one block of kRgThreads threads, from the step's ids held in
 // shared memory: per-chunk expert masks, counts, chunk bases, offsets, segments and the
-// stable scatter (the rows of chunk_scan + scatter).  sm: [2 n_chunks E] words of scratch, then
+// stable scatter (the steps of the group launch).  sm: [2 n_chunks E] words of scratch, then
 // ids [T][k], then [E + 1] words.
 MOE_DEVICE void group_small(int T, int E, int k, uint32_t* sm, int32_t* __restrict__ counts,
                             int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,

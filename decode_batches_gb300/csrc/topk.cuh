@@ -8,45 +8,44 @@
 
 namespace moe {
 
-// Sortable 64-bit key of (logit v, expert e): a larger key ranks first.  The high word maps the
-// float to an unsigned integer that grows with v (-0 is first turned into +0, so the two
-// compare equal); NaN maps to 0, below -inf.  The low word is ~e, so on equal values the lower
-// index ranks first.  Padding lanes (e >= E) get key 0, below every real candidate.
-MOE_DEVICE uint64_t rank_key(float v, int e) {
-  uint32_t hi = 0u;
-  if (!isnan(v)) {
-    const uint32_t b = __float_as_uint(v + 0.0f);
-    hi = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-  }
-  return (static_cast<uint64_t>(hi) << 32) | static_cast<uint32_t>(~e);
+// Ordered 32-bit key of a logit: a larger key ranks first.  A float maps to an unsigned integer
+// that grows with its value (-0 is first turned into +0, so the two compare equal); every real
+// value maps above 2.  NaN maps to 2, below -inf; 1 marks a padding lane (e >= E) and 0 a
+// candidate already taken.  Equal keys rank by expert index, lower first.
+MOE_DEVICE uint32_t rank_key(float v) {
+  if (isnan(v)) return 2u;
+  const uint32_t b = __float_as_uint(v + 0.0f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
 // Selection and gates of token t by one warp from its logits v (lane l holds experts
 // l + 32 i): writes ids / gates of the token and returns, in lane j < k, the expert chosen in
-// round j.
+// round j.  Each round every lane offers its best remaining candidate (largest key, then lowest
+// index); the warp takes the largest key and, among the lanes offering it, the lowest expert.
 template <int PL>
 MOE_DEVICE int topk_select(const float (&v)[PL], int t, int E, int k, int32_t* __restrict__ ids,
                            float* __restrict__ gates, uint32_t* err) {
   const int lane = threadIdx.x & 31;
-  uint64_t key[PL];
+  uint32_t key[PL];
 #pragma unroll
-  for (int i = 0; i < PL; ++i) {
-    const int e = lane + 32 * i;
-    key[i] = e < E ? rank_key(v[i], e) : 0ull;
-  }
+  for (int i = 0; i < PL; ++i) key[i] = lane + 32 * i < E ? rank_key(v[i]) : 1u;
   int sel_i = 0;  // lane j keeps the expert chosen in round j
   for (int j = 0; j < k; ++j) {
-    uint64_t best = key[0];
+    uint32_t best = key[0];
+    int bi = 0;
 #pragma unroll
-    for (int i = 1; i < PL; ++i) best = key[i] > best ? key[i] : best;
-    const uint32_t hi = static_cast<uint32_t>(best >> 32);
-    const uint32_t win_hi = __reduce_max_sync(0xffffffffu, hi);
-    const uint32_t win_lo = __reduce_max_sync(0xffffffffu, hi == win_hi ? static_cast<uint32_t>(best) : 0u);
-    const int win_e = static_cast<int>(~win_lo);
+    for (int i = 1; i < PL; ++i) {
+      const bool gt = key[i] > best;  // strict: the lowest index keeps a tie
+      best = gt ? key[i] : best;
+      bi = gt ? i : bi;
+    }
+    const uint32_t win_key = __reduce_max_sync(0xffffffffu, best);
+    const uint32_t cand = best == win_key ? static_cast<uint32_t>(lane + 32 * bi) : 0xffffffffu;
+    const int win_e = static_cast<int>(__reduce_min_sync(0xffffffffu, cand));
     // the owner lane retires the winner (a select per key: the keys stay in registers)
-    const int win_slot = (win_e & 31) == lane ? (win_e >> 5) : -1;
+    const bool owner = (win_e & 31) == lane;
 #pragma unroll
-    for (int i = 0; i < PL; ++i) key[i] = i == win_slot ? 0ull : key[i];
+    for (int i = 0; i < PL; ++i) key[i] = (owner && i == bi) ? 0u : key[i];
     if (lane == j) sel_i = win_e;
   }
   // gates: softmax over the k selected logits, slot 0 holds the maximum

@@ -21,6 +21,9 @@
  *     caller owns them and keeps them alive until the work queued on `stream` has finished.
  *   - Layouts are row-major with the last index contiguous.  bf16 tensors are passed as
  *     `void*` holding IEEE bfloat16 bit patterns.
+ *   - The activation tensors x, y, shared_y and out of moe_layer_forward, moe_route,
+ *     moe_experts and moe_combine are moved as 16-byte vectors: their base addresses must be
+ *     16-byte aligned (MOE_ERR_INVALID_ARG otherwise).
  *   - Calls that take a plan and a stream only enqueue work; they never synchronise the host,
  *     never allocate device memory and are safe to capture in a CUDA graph once the plan has its
  *     weights and workspace.  T == 0 is a no-op that returns MOE_OK.
@@ -224,8 +227,9 @@ moe_status moe_permute(moe_plan* plan, const int32_t* ids, int T, int32_t* count
  * code on a latency-critical path, where cudaMalloc would synchronise the device.  Same inputs and outputs as moe_permute
  * (ids int32 [T][k] -> counts [E], offsets [E+1], perm and inv_perm [T*k], all device
  * pointers; invalid or repeated ids are dropped with inv_perm = -1, but there is no error word).
- * Scratch is a fixed 2 MiB device array inside the library, present on every GPU that loads it
- * until the process exits; ceil(T / 32) * E must not exceed 262144 (T <= 32768 at E = 256),
+ * Scratch is a fixed 1 MiB device array inside the library, present on every GPU that loads it
+ * until the process exits; ceil(ceil(T / 32) / 4) * 4 * E must not exceed 262144 (T <= 32768 at
+ * E = 256),
  * else MOE_ERR_WORKSPACE and nothing is enqueued.  The first call in a CUDA context (the first
  * on a device, and the first after that device's context was destroyed and re-created, e.g. by
  * cudaDeviceReset) looks up the array's device address (cudaGetSymbolAddress); make that first

@@ -211,6 +211,13 @@ def test_forward_edge_arguments_and_canaries():
     big = synth.custom(w.spec, 65).x()
     with pytest.raises(MoeError):
         plan.forward(to_dev(big, "bf16"))                 # T > T_max of the workspace
+    # x 2 bytes past a 16-byte boundary: refused on the host, before any launch
+    flat = torch.zeros(w.T * w.spec.d + 8, dtype=torch.bfloat16, device="cuda")
+    x_mis = flat[1:1 + w.T * w.spec.d].view(w.T, w.spec.d)
+    x_mis.copy_(x)
+    assert x_mis.data_ptr() % 16 == 2
+    with pytest.raises(MoeError):
+        plan.forward(x_mis)
     # output written into the middle of a guarded buffer: guards untouched
     guard = 1024
     buf = torch.full((guard * 2 + w.T * w.spec.d,), 12345, dtype=torch.int16, device="cuda")

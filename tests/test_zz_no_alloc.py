@@ -135,7 +135,8 @@ def test_static_permute_drops_invalid_and_repeated_ids():
 
 
 def test_static_permute_at_the_capacity_limit():
-    """ceil(T / 32) * E == 262144 exactly: both scratch arrays are filled completely."""
+    """ceil(T / 32) * E == 262144 exactly (1024 chunks, a multiple of 4): the mask array is
+    filled completely."""
     from decode_batches_gb300 import MoePlan
     lib = _lib()
     E, k, T = 256, 8, 32768
