@@ -25,8 +25,9 @@
 // Roles (persistent CTAs, one per SM, every role walks the same unit sequence):
 //   warp 0      producer: A by bulk copy; B by TMA (down kernel)
 //   warp 1      TMEM owner and MMA issuer
-//   warps 2-5   epilogue (TMEM lanes 32*(warp%4) .. +31)
-//   warps 6-13  gate/up only: cp.async gather of the token rows, two warps per stage slot
+//   warps 2-9   epilogue (TMEM lanes 32*(warp%4) .. +31; the two warps of a lane quarter take
+//               alternate 16-column chunks, so the epilogue keeps pace with 128-row segments)
+//   warps 10-17 gate/up only: cp.async gather of the token rows, two warps per stage slot
 // Producer and MMA loops run converged and issue under elect_one() (warp-uniform operands: an
 // MMA issues in a few tens of cycles), and the MMA warp probes the next stage's barrier before
 // issuing the current stage, so the barrier round trip hides behind the issue.
@@ -59,8 +60,11 @@ constexpr int kGatherPerSlot = 2;                // gate/up B producers per stag
 constexpr int kGatherWarps = kGatherPerSlot * kStages;
 constexpr int kTokBytes = kGatherWarps * kSegRowsMax * 4;  // per gather warp: token of each row
 constexpr int kEpiStageBytes = 16 * 32 * 2;     // per epilogue warp: 16 columns x 32 fp16 rows
+constexpr int kEpiWarps = 8;                     // two per TMEM lane quarter, alternate 16-column chunks
+constexpr int kFirstGather = 2 + kEpiWarps;      // gate/up: first gather warp
+constexpr int kBaseThreads = 32 * kFirstGather;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*align slack*/ + kTokBytes +
-                           4 * kEpiStageBytes;
+                           kEpiWarps * kEpiStageBytes;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct Unit {
@@ -119,7 +123,7 @@ MOE_DEVICE Unit decode_unit(int u, const TcArgs& a, int tiles_r, int tiles_s, in
 MOE_DEVICE int pad16(int rows) { return rows <= 16 ? 16 : ((rows + 15) & ~15); }
 
 template <bool kGateUp>
-__global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
+__global__ void __launch_bounds__(kGateUp ? kBaseThreads + 32 * kGatherWarps : kBaseThreads, 1)
     tc_ffn_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -142,7 +146,7 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
+      mbar_init(&acc_empty[b], kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -274,7 +278,7 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
     if (elect_one()) mma_commit(drain);
     __syncwarp();
     mbar_wait_warp(drain, 0, nullptr, a.err);
-  } else if (warp < 6) {
+  } else if (warp < kFirstGather) {
     // ---------------- epilogue ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     // h and y are read back by the next launch: keep them in L2 ahead of the streamed weights
@@ -289,6 +293,7 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
       // Each 16-column chunk goes through a per-warp shared tile [column][row] so that the
       // global stores are 16-byte vectors of 8 consecutive features of one token.
       uint16_t* stg = epi_stage + (warp - 2) * (kEpiStageBytes / 2);
+      const int c_first = 16 * ((warp - 2) / 4);  // this warp's 16-column chunks: c_first + 32 i
       bool sat = false;
       for (int t = 0; t < un.ntile; ++t) {
         const int tile = un.tile + t;
@@ -309,7 +314,7 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
             hout = a.h;
             ldh = a.f;
           }
-          for (int c0 = 0; c0 < un.rows; c0 += 16) {
+          for (int c0 = c_first; c0 < un.rows; c0 += 32) {
             uint32_t r[16];
             tmem_ld_32x32b_x16(tbase + c0, r);
             tmem_wait_ld();
@@ -340,7 +345,7 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
         } else {
           const int feat0 = tile * BM + 32 * q;
           uint16_t* yout = un.shared ? a.y_s : a.y;
-          for (int c0 = 0; c0 < un.rows; c0 += 16) {
+          for (int c0 = c_first; c0 < un.rows; c0 += 32) {
             uint32_t r[16];
             tmem_ld_32x32b_x16(tbase + c0, r);
             tmem_wait_ld();
@@ -377,7 +382,7 @@ __global__ void __launch_bounds__(kGateUp ? 192 + 32 * kGatherWarps : 192, 1)
     // Warps w and w + kStages own stage slot w: they fill every stage g with g % kStages == w
     // (each half of the rows), wait for their own copies, fence them for the tensor core and
     // arrive.  8 consecutive lanes copy the 8 16-byte chunks of one row (a 128-byte line).
-    const int gw = warp - 6;
+    const int gw = warp - kFirstGather;
     const int slot = gw % kStages, half = gw / kStages;
     int32_t* tok = tok_tab + kSegRowsMax * gw;  // token of each row of this warp's unit
     const int ch = lane & 7;
@@ -428,7 +433,8 @@ static cudaError_t launch_tc(const TcMaps* maps, const TcArgs& a, int num_sms, c
   auto kern = tc::tc_ffn_kernel<kGateUp>;
   cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), tc::kSmemBytes);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(num_sms), dim3(kGateUp ? 192 + 32 * tc::kGatherWarps : 192), tc::kSmemBytes, st,
+  return launch_pdl(kern, dim3(num_sms), dim3(kGateUp ? tc::kBaseThreads + 32 * tc::kGatherWarps : tc::kBaseThreads),
+                    tc::kSmemBytes, st,
                     *maps, a);
 }
 
