@@ -229,6 +229,27 @@ def test_forward_edge_arguments_and_canaries():
     compare_layer(bf16_tensor_to_f64(out_view), ref, w.spec.k, TOL_BF16)
 
 
+@pytest.mark.parametrize("T", [200, 400, 700])
+def test_multi_part_experts_against_the_oracle(T):
+    """Experts with ~100 rows (one segment, T = 200), ~200 rows (two parts, T = 400) and ~350
+    rows (three parts, T = 700) on the tensor-core path, and several shared-expert segments;
+    every output against the oracle, through the layer and through the experts entry point."""
+    spec = synth.LayerSpec(E=4, k=2, d=256, f=512, n_shared=1, f_s=256, wdtype="bf16")
+    w = synth.custom(spec, T, n_prefill=T - 3, name=f"parts{T}")
+    plan = make_plan(w)
+    plan.set_path("tc")
+    x = to_dev(w.x(), "bf16")
+    out = bf16_tensor_to_f64(plan.forward(x, n_prefill=w.n_prefill))
+    _, ids, _ = plan.route(x, want_logits=False)
+    ref = oracle_layer(w)
+    compare_layer(out, ref, spec.k, TOL_BF16, ids.cpu().numpy())
+    # the experts entry point builds its own segments from the oracle's offsets
+    y, _ = plan.experts(x, to_dev(ref["offsets"]), to_dev(ref["perm"]))
+    rms = np.sqrt(np.mean(ref["y_perm"] ** 2))
+    assert np.abs(y.double().cpu().numpy() - ref["y_perm"]).max() <= TOL_BF16 * rms
+    assert plan.device_error() == 0
+
+
 def test_untiled_shape_runs_the_reference_path():
     """d and d_ff that the tensor-core tiles do not divide: the plan keeps the row-interleaved
     layout and the CUDA-core path computes the layer (with shared experts)."""
