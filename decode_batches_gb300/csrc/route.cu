@@ -537,14 +537,22 @@ __global__ void __launch_bounds__(kGroupThreads) group_kernel(
       }
 #pragma unroll
       for (int u = 0; u < kGroupLoads; ++u) {
-        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const int c = 4 * (i0 + u * tpe) + b;
-          const int pc = c < n_chunks ? __popc(w[b]) : 0;  // the row's padding words are not masks
+        const int cb = 4 * (i0 + u * tpe);  // chunk of the vector's first word
+        if (cb + 3 < n_chunks && (cb + 3 < c0 || cb >= c1)) {
+          // the common case: four mask words, none of them the block's own or padding
+          const int pc = __popc(v[u].x) + __popc(v[u].y) + __popc(v[u].z) + __popc(v[u].w);
           tot += pc;
-          if (c < c0) pre += pc;
-          else if (c < c1) s_w[(c - c0) * E + e] = w[b];
+          if (cb < c0) pre += pc;
+        } else if (cb < n_chunks) {
+          const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const int c = cb + b;
+            const int pc = c < n_chunks ? __popc(w[b]) : 0;  // the row's padding words are not masks
+            tot += pc;
+            if (c < c0) pre += pc;
+            else if (c < c1) s_w[(c - c0) * E + e] = w[b];
+          }
         }
       }
     }
