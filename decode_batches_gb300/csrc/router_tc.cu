@@ -52,8 +52,8 @@ MOE_DEVICE Item decode_item(int i, int tiles_e, int nsplit, int nk, int T) {
 
 // Persistent CTAs (at most one per SM) walk the items b, b + gridDim.x, ...; the stage ring runs
 // on across items and the two TMEM accumulator pairs let the epilogue of one item overlap the
-// main loop of the next.  Roles: warp 0 TMA producer of the W pieces, warp 1 TMEM owner and MMA
-// issuer, warps 2-5 epilogue (TMEM lanes 32 (warp % 4) ..).
+// main loop of the next.  Roles: warp 0 TMA producer (the W pieces and the token rows), warp 1
+// TMEM owner and MMA issuer, warps 2-5 epilogue (TMEM lanes 32 (warp % 4) ..).
 __global__ void __launch_bounds__(kThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap w3, const __grid_constant__ CUtensorMap xm, int T, int E,
                      int d, int nsplit, float* __restrict__ parts, uint32_t* err) {
