@@ -250,6 +250,22 @@ def test_multi_part_experts_against_the_oracle(T):
     assert plan.device_error() == 0
 
 
+@pytest.mark.parametrize("E,k,T", [(16, 1, 37), (16, 1, 300), (8, 8, 300), (40, 3, 37), (40, 3, 300)])
+def test_unusual_top_k_against_the_oracle(E, k, T):
+    """k = 1 (no mixing), k = E (every expert, dense mixture) and E = 40 (not a multiple of 32 or
+    of the router's 128-expert tile: the CUDA-core router) through the tensor-core layer, on the
+    one-block routing front end (T = 37) and the general one (T = 300)."""
+    spec = synth.LayerSpec(E=E, k=k, d=256, f=256, n_shared=1, f_s=128, wdtype="bf16")
+    w = synth.custom(spec, T, n_prefill=T // 2, name=f"topk{E}_{k}_{T}")
+    plan = make_plan(w)
+    plan.set_path("tc")
+    x = to_dev(w.x(), "bf16")
+    out = bf16_tensor_to_f64(plan.forward(x, n_prefill=w.n_prefill))
+    _, ids, _ = plan.route(x, want_logits=False)
+    compare_layer(out, oracle_layer(w), spec.k, TOL_BF16, ids.cpu().numpy())
+    assert plan.device_error() == 0
+
+
 def test_untiled_shape_runs_the_reference_path():
     """d and d_ff that the tensor-core tiles do not divide: the plan keeps the row-interleaved
     layout and the CUDA-core path computes the layer (with shared experts)."""
