@@ -220,7 +220,7 @@ MOE_DEVICE void router_parts_block(const uint16_t* __restrict__ x, const float* 
 }
 
 template <int G>
-__global__ void __launch_bounds__(256) router_parts_small_kernel(const uint16_t* __restrict__ x,
+__global__ void __launch_bounds__(256, 1) router_parts_small_kernel(const uint16_t* __restrict__ x,
                                                                  const float* __restrict__ wr, int T, int E, int d,
                                                                  float* __restrict__ parts) {
   __shared__ __align__(16) uint16_t xs[G * kRouterKS];
