@@ -266,6 +266,31 @@ def test_unusual_top_k_against_the_oracle(E, k, T):
     assert plan.device_error() == 0
 
 
+def test_two_plans_on_two_streams():
+    """Two plans (bf16 mixed step, 4-bit verify step) used at the same time on two streams: each
+    has its own workspace and plan words (routing counter, unit hand-out words, error word), so
+    the interleaved steps do not disturb each other; both results match their oracles."""
+    wa, wb = workload("mixed", 512), workload("verify", 0)
+    pa, pb = plan_for(wa.spec), plan_for(wb.spec)
+    pa.set_path("auto")
+    pb.set_path("auto")
+    xa, xb = to_dev(wa.x(), "bf16"), to_dev(wb.x(), "bf16")
+    oa = torch.empty((wa.T, wa.spec.d), dtype=torch.bfloat16, device="cuda")
+    ob = torch.empty((wb.T, wb.spec.d), dtype=torch.bfloat16, device="cuda")
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for _ in range(4):
+        pa.forward(xa, n_prefill=wa.n_prefill, out=oa, stream=sa)
+        pb.forward(xb, n_prefill=wb.n_prefill, out=ob, stream=sb)
+    torch.cuda.synchronize()
+    rows = sample_rows(wa, 48)
+    _, ids_a, _ = pa.route(xa, want_logits=False)
+    compare_layer(bf16_tensor_to_f64(oa)[rows], oracle_layer(wa, rows), wa.spec.k, TOL_BF16, ids_a.cpu().numpy()[rows])
+    _, ids_b, _ = pb.route(xb, want_logits=False)
+    compare_layer(bf16_tensor_to_f64(ob), oracle_layer(wb), wb.spec.k, TOL_FP4, ids_b.cpu().numpy())
+    assert pa.device_error() == 0 and pb.device_error() == 0
+
+
 def test_untiled_shape_runs_the_reference_path():
     """d and d_ff that the tensor-core tiles do not divide: the plan keeps the row-interleaved
     layout and the CUDA-core path computes the layer (with shared experts)."""
